@@ -1,0 +1,146 @@
+"""fp64 CPU oracle for exact softmax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package.  The product (the CUDA library and its
+Python binding in ``exact_attention_60_gb300``) never imports it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain loops, double precision,
+materialised score and probability rows); this module only compiles it with
+gcc, loads it with ctypes and marshals numpy arrays.  See that file's header
+for the passages each step follows:
+
+* "Triton Ascend Attention" (skillmd.com), section 标准 Attention 计算流程:
+  the three-stage definition softmax(Q K^T / sqrt(d_k)) V.
+* wsisp.com post "FlashAttention-2 forward in Triton", the passage that FA
+  computes exactly S = QK^T, P = softmax(S), O = PV, and the outer-kernel
+  epilogue storing m + log(l) per row.
+* "flash-attention-kernel" skill card: causal keeps ``offs_m >= offs_n``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle source into a shared library (gcc, OpenMP, -O2)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + ".tmp"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _dptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening to a contiguous float64 array (bf16 values are exact in fp64)."""
+    if hasattr(a, "detach"):  # a torch tensor: widen through float32, which holds bf16 exactly
+        a = a.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+class OracleLib:
+    """ctypes front end of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lp = ctypes.POINTER(ctypes.c_long)
+        lib.oracle_attn_head.restype = ctypes.c_int
+        lib.oracle_attn_head.argtypes = [dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                         ctypes.c_long, ctypes.c_int, ctypes.c_double,
+                                         lp, ctypes.c_long, dp, dp, dp, ctypes.c_int]
+        lib.oracle_attn_full.restype = ctypes.c_int
+        lib.oracle_attn_full.argtypes = [dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                         ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                         ctypes.c_int, ctypes.c_double, dp, dp, dp,
+                                         ctypes.c_int]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        self.lib = lib
+        self.path = path
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
+
+    def attn_head(self, q, k, v, causal: bool, scale: float, rows=None,
+                  want_p: bool = False, nthreads: int = 0):
+        """Attention of one (batch, head) slice.
+
+        q: [Lq, D]; k, v: [Lk, D].  ``rows``: query indices to compute (default all).
+        Returns (O [n, D], LSE [n]) or (O, LSE, P [n, Lk]) with ``want_p``.
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        Lq, D = q.shape
+        Lk = k.shape[0]
+        if k.shape != (Lk, D) or v.shape != (Lk, D):
+            raise ValueError("k and v must be [Lk, D] with the same D as q")
+        if rows is None:
+            n, rp = Lq, None
+        else:
+            rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+            n = rows_arr.shape[0]
+            rp = rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+        O = np.empty((n, D), dtype=np.float64)
+        L = np.empty((n,), dtype=np.float64)
+        P = np.empty((n, Lk), dtype=np.float64) if want_p else None
+        rc = self.lib.oracle_attn_head(_dptr(q), _dptr(k), _dptr(v), Lq, Lk, D,
+                                       int(bool(causal)), float(scale), rp, n,
+                                       _dptr(O), _dptr(L), _dptr(P), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_head failed with code {rc}")
+        return (O, L, P) if want_p else (O, L)
+
+    def attn_full(self, q, k, v, causal: bool, scale: float, want_p: bool = False,
+                  nthreads: int = 0):
+        """Attention over contiguous [B, H, L, D] tensors: returns (O, LSE[, P])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, Lq, D = q.shape
+        Lk = k.shape[2]
+        if k.shape != (B, H, Lk, D) or v.shape != (B, H, Lk, D):
+            raise ValueError("k and v must be [B, H, Lk, D] matching q")
+        O = np.empty((B, H, Lq, D), dtype=np.float64)
+        L = np.empty((B, H, Lq), dtype=np.float64)
+        P = np.empty((B, H, Lq, Lk), dtype=np.float64) if want_p else None
+        rc = self.lib.oracle_attn_full(_dptr(q), _dptr(k), _dptr(v), B, H, Lq, Lk, D,
+                                       int(bool(causal)), float(scale), _dptr(O),
+                                       _dptr(L), _dptr(P), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_full failed with code {rc}")
+        return (O, L, P) if want_p else (O, L)
+
+
+_default = None
+
+
+def _get() -> OracleLib:
+    global _default
+    if _default is None:
+        _default = OracleLib(build())
+    return _default
+
+
+def max_threads() -> int:
+    return _get().max_threads()
+
+
+def attn_head(*args, **kwargs):
+    return _get().attn_head(*args, **kwargs)
+
+
+def attn_full(*args, **kwargs):
+    return _get().attn_full(*args, **kwargs)

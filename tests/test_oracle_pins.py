@@ -1,0 +1,242 @@
+"""Pins for the fp64 oracle: facts fixed by the pages and by the mathematics.
+
+None of these compares the oracle with itself or with the CUDA path.  They use
+closed forms, invariants, special cases that reduce to a library routine
+(torch fp64 softmax / logsumexp), an independent online-softmax recurrence, and
+hand-worked fixtures under tests/golden/.  The last test plants plausible
+mistakes in a copy of the oracle source and checks that the pins catch each.
+"""
+import json
+import math
+import os
+import shutil
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def _allowed(i, Lk, causal):
+    return min(i + 1, Lk) if causal else Lk
+
+
+# --------------------------------------------------------------------------
+# The individual pins, each taking an oracle library so the mutation test can
+# run them against a deliberately broken copy.
+# --------------------------------------------------------------------------
+
+def pin_rows_sum_to_one(lib):
+    """Every probability row sums to 1 and is exactly 0 on masked keys."""
+    for causal, (Lq, Lk) in [(False, (7, 11)), (True, (9, 9)), (True, (12, 5)), (True, (4, 10))]:
+        q, k, v = _rand((Lq, 16), 1), _rand((Lk, 16), 2), _rand((Lk, 16), 3)
+        _, _, P = lib.attn_head(q, k, v, causal, 0.25, want_p=True)
+        assert np.allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        for i in range(Lq):
+            n = _allowed(i, Lk, causal)
+            assert np.all(P[i, n:] == 0.0)
+            assert np.all(P[i, :n] > 0.0)
+
+
+def pin_single_key(lib):
+    """Lk = 1: O is exactly V's only row; LSE is that row's scaled score."""
+    q, k, v = _rand((6, 32), 4), _rand((1, 32), 5), _rand((1, 32), 6)
+    for causal in (False, True):
+        O, L = lib.attn_head(q, k, v, causal, 0.3)
+        assert np.array_equal(O, np.repeat(v, 6, axis=0))
+        np.testing.assert_allclose(L, 0.3 * (q @ k[0]), rtol=0, atol=1e-12)
+
+
+def pin_constant_v(lib):
+    """All value rows equal c: every output row is c."""
+    q, k = _rand((10, 8), 7), _rand((13, 8), 8)
+    c = _rand((8,), 9)
+    v = np.tile(c, (13, 1))
+    for causal in (False, True):
+        O, _ = lib.attn_head(q, k, v, causal, 0.5)
+        np.testing.assert_allclose(O, np.tile(c, (10, 1)), rtol=0, atol=1e-12)
+
+
+def pin_causal_row0(lib):
+    """Causal row 0 sees only key 0: O_0 = V_0, LSE_0 = scale * q_0 . k_0."""
+    q, k, v = _rand((5, 8), 10), _rand((7, 8), 11), _rand((7, 8), 12)
+    O, L = lib.attn_head(q, k, v, True, 0.7)
+    np.testing.assert_allclose(O[0], v[0], rtol=0, atol=1e-12)
+    assert abs(L[0] - 0.7 * (q[0] @ k[0])) < 1e-12
+
+
+def pin_uniform_scores(lib):
+    """Q = 0 makes every score 0: O_i is the mean of the allowed value rows and
+    LSE_i = ln(number of allowed keys).  Pins the causal key count per row."""
+    for causal, (Lq, Lk) in [(False, (5, 9)), (True, (9, 9)), (True, (11, 6)), (True, (3, 8))]:
+        q, k, v = np.zeros((Lq, 4)), _rand((Lk, 4), 13), _rand((Lk, 4), 14)
+        O, L = lib.attn_head(q, k, v, causal, 1.0)
+        for i in range(Lq):
+            n = _allowed(i, Lk, causal)
+            np.testing.assert_allclose(O[i], v[:n].mean(axis=0), rtol=0, atol=1e-12)
+            assert abs(L[i] - math.log(n)) < 1e-12
+
+
+def pin_permutation(lib):
+    """Non-causal attention is invariant under one permutation of K and V rows."""
+    q, k, v = _rand((6, 8), 15), _rand((10, 8), 16), _rand((10, 8), 17)
+    perm = np.random.default_rng(18).permutation(10)
+    O1, L1 = lib.attn_head(q, k, v, False, 0.4)
+    O2, L2 = lib.attn_head(q, k[perm], v[perm], False, 0.4)
+    np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L1, L2, rtol=0, atol=1e-12)
+
+
+def pin_key_shift(lib):
+    """Adding u to every key row leaves O unchanged and moves LSE_i by scale*q_i.u."""
+    q, k, v = _rand((6, 8), 19), _rand((9, 8), 20), _rand((9, 8), 21)
+    u = _rand((8,), 22)
+    for causal in (False, True):
+        O1, L1 = lib.attn_head(q, k, v, causal, 0.35)
+        O2, L2 = lib.attn_head(q, k + u, v, causal, 0.35)
+        np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(L2 - L1, 0.35 * (q @ u), rtol=0, atol=1e-11)
+
+
+def pin_torch_f64(lib):
+    """Brute force on tiny shapes: torch fp64 softmax / logsumexp with a mask."""
+    cases = [(1, 1, 3, 3, 4, False), (2, 3, 5, 7, 8, True), (1, 2, 9, 4, 16, True),
+             (2, 1, 6, 6, 8, False), (1, 1, 4, 11, 8, True)]
+    for (B, H, Lq, Lk, D, causal) in cases:
+        g = torch.Generator().manual_seed(Lq * 100 + Lk)
+        q = torch.randn(B, H, Lq, D, generator=g, dtype=torch.float64)
+        k = torch.randn(B, H, Lk, D, generator=g, dtype=torch.float64)
+        v = torch.randn(B, H, Lk, D, generator=g, dtype=torch.float64)
+        scale = 1.0 / math.sqrt(D)
+        s = torch.einsum("bhid,bhjd->bhij", q, k) * scale
+        if causal:
+            keep = torch.arange(Lq)[:, None] >= torch.arange(Lk)[None, :]
+            s = s.masked_fill(~keep, float("-inf"))
+        ref_o = torch.softmax(s, dim=-1) @ v
+        ref_l = torch.logsumexp(s, dim=-1)
+        O, L = lib.attn_full(q.numpy(), k.numpy(), v.numpy(), causal, scale)
+        np.testing.assert_allclose(O, ref_o.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L, ref_l.numpy(), rtol=0, atol=1e-12)
+
+
+def _online(q, k, v, causal, scale, block):
+    """Online softmax over key blocks of size ``block``, as the "Triton Ascend
+    Attention" page's 在线 Softmax 算法 sketch states it (running max m, running
+    exp-sum l, accumulator rescaled by alpha = exp(m_old - m_new)), applied to
+    rows of scores, with the final divide by l and the statistic m + log(l)."""
+    Lq, Lk = q.shape[0], k.shape[0]
+    O = np.zeros((Lq, v.shape[1]))
+    L = np.zeros(Lq)
+    for i in range(Lq):
+        n = _allowed(i, Lk, causal)
+        m, l, acc = -np.inf, 0.0, np.zeros(v.shape[1])
+        for j0 in range(0, n, block):
+            j1 = min(n, j0 + block)
+            s = scale * (k[j0:j1] @ q[i])
+            m_new = max(m, s.max())
+            p = np.exp(s - m_new)
+            alpha = math.exp(m - m_new)
+            l = l * alpha + p.sum()
+            acc = acc * alpha + p @ v[j0:j1]
+            m = m_new
+        O[i] = acc / l
+        L[i] = m + math.log(l)
+    return O, L
+
+
+def pin_online_recurrence(lib):
+    """The online recurrence, for every key-block size, equals the definition."""
+    q, k, v = _rand((6, 8), 23, 2.0), _rand((9, 8), 24, 2.0), _rand((9, 8), 25)
+    for causal in (False, True):
+        O, L = lib.attn_head(q, k, v, causal, 0.6)
+        for block in range(1, 10):
+            O2, L2 = _online(q, k, v, causal, 0.6, block)
+            np.testing.assert_allclose(O, O2, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(L, L2, rtol=0, atol=1e-12)
+
+
+def pin_golden(lib):
+    """Hand-worked closed forms (tests/golden/closed_forms.json)."""
+    with open(os.path.join(HERE, "golden", "closed_forms.json")) as f:
+        cases = json.load(f)["cases"]
+    env = {"e": math.e, "exp": math.exp, "log": math.log, "sqrt": math.sqrt, "__builtins__": {}}
+    for c in cases:
+        q, k, v = (np.array(c[x], dtype=np.float64) for x in ("Q", "K", "V"))
+        O, L = lib.attn_head(q, k, v, c["causal"], c["scale"])
+        exp_o = np.array([[eval(x, env) for x in row] for row in c["O"]])
+        exp_l = np.array([eval(x, env) for x in c["LSE"]])
+        np.testing.assert_allclose(O, exp_o, rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(L, exp_l, rtol=0, atol=1e-14, err_msg=c["name"])
+
+
+def pin_row_subset(lib):
+    """Computing a subset of rows gives exactly those rows of the full result."""
+    q, k, v = _rand((20, 8), 26), _rand((17, 8), 27), _rand((17, 8), 28)
+    for causal in (False, True):
+        O, L = lib.attn_head(q, k, v, causal, 0.5)
+        rows = [19, 0, 7, 7, 16]
+        Os, Ls = lib.attn_head(q, k, v, causal, 0.5, rows=rows)
+        assert np.array_equal(Os, O[rows]) and np.array_equal(Ls, L[rows])
+
+
+PINS = [pin_rows_sum_to_one, pin_single_key, pin_constant_v, pin_causal_row0,
+        pin_uniform_scores, pin_permutation, pin_key_shift, pin_torch_f64,
+        pin_online_recurrence, pin_golden, pin_row_subset]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(oracle_mod, pin):
+    pin(oracle_mod._get())
+
+
+def test_bad_arguments_rejected(oracle_mod):
+    q, k, v = _rand((3, 4), 1), _rand((2, 4), 2), _rand((2, 4), 3)
+    with pytest.raises(ValueError):
+        oracle_mod.attn_head(q, k, v, False, 1.0, rows=[3])
+    with pytest.raises(ValueError):
+        oracle_mod.attn_head(q, k[:0], v[:0], False, 1.0)
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: each textual mutation of the oracle source must make at
+# least one pin fail.  The mutated copies are built in a temporary directory.
+# --------------------------------------------------------------------------
+
+MUTATIONS = {
+    "dropped_scale": ("S[j] = scale * dot;", "S[j] = dot;"),
+    "max_sign_flip": ("P[j] = exp(S[j] - m);", "P[j] = exp(S[j] + m);"),
+    "diagonal_excluded": ("return (i + 1 < Lk) ? (i + 1) : Lk;", "return (i < Lk) ? i : Lk;"),
+    "keys_as_values": ("o[d] += w * V[j * D + d];", "o[d] += w * K[j * D + d];"),
+    "reversed_feature_index": ("dot += q[d] * K[j * D + d];", "dot += q[d] * K[j * D + (D - 1 - d)];"),
+    "lse_missing_max": ("*lse = m + log(l);", "*lse = log(l);"),
+    "no_normalisation": ("for (long j = 0; j < n_allowed; ++j) P[j] /= l;", ";"),
+    "causal_ignored": ("if (!causal) return Lk;", "return Lk;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    src = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+    text = open(src).read()
+    old, new = MUTATIONS[name]
+    assert text.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / f"oracle_{name}.c"
+    mutated.write_text(text.replace(old, new))
+    lib = oracle.OracleLib(oracle.build(force=True, src=str(mutated),
+                                        out=str(tmp_path / f"lib_{name}.so")))
+    failures = 0
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(lib)
+        except (AssertionError, ValueError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {name}"
+    shutil.rmtree(tmp_path, ignore_errors=True)
