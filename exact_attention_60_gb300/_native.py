@@ -1,0 +1,83 @@
+"""ctypes binding of libfa.so: the C ABI of include/fa.h under the same names.
+
+Argument marshalling only -- every step of the attention runs in the CUDA
+library.  Loading fails loudly (``RuntimeError``) when the library has not been
+built; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+# Every symbol include/fa.h declares.
+EXPORTED = ("fa_fwd", "fa_status_string", "fa_last_device_status", "fa_debug_set")
+
+_lib = None
+
+
+def load(path: str = LIB) -> ctypes.CDLL:
+    """Load libfa.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing: run __graft_entry__.build() "
+                           "(or python -m exact_attention_60_gb300.build) first")
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_last_device_status.restype = ctypes.c_int
+    lib.fa_last_device_status.argtypes = [vp]
+    lib.fa_debug_set.restype = ctypes.c_int
+    lib.fa_debug_set.argtypes = [ctypes.c_uint, ctypes.c_ulonglong]
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() or None
+    return int(x) or None
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream or None
+    return int(s) or None
+
+
+def fa_fwd(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, stream=None) -> int:
+    """C ``fa_fwd``.  Pointers may be ints or tensors (their ``data_ptr()``);
+    ``stream`` may be an int handle, a torch stream, or None (torch's current stream)."""
+    return load().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
+                         int(Lq), int(Lk), int(D), int(bool(causal)), float(scale),
+                         _stream(stream))
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def fa_last_device_status(stream=None) -> int:
+    return load().fa_last_device_status(_stream(stream))
+
+
+def fa_debug_set(flags: int, wait_limit_ns: int) -> int:
+    return load().fa_debug_set(int(flags), int(wait_limit_ns))

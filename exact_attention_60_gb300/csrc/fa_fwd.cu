@@ -1,0 +1,639 @@
+// fa_fwd.cu -- FlashAttention-2 forward for GB300 (sm_103a), and its C ABI.
+//
+// What is computed (per batch b, head h, query row i):
+//   O[i,:] = sum_j softmax_j(scale * Q[i,:].K[j,:]) V[j,:],  LSE[i] = ln sum_j exp(scale * Q[i,:].K[j,:])
+// over all keys j < Lk, or only j <= i when causal.  The method is the one of the
+// wsisp.com post "FlashAttention-2 forward in Triton": each query tile streams
+// the K/V tiles of its head through an online softmax (running row max m,
+// running exp-sum l, unnormalised fp32 accumulator rescaled when m grows), the
+// score matrix never reaches global memory, and the epilogue writes O / l and
+// m + log(l).  Causal runs skip the tiles past the diagonal and mask only the
+// diagonal tile ("flash-attention-kernel" skill card, causal tips; the post's
+// STAGE 1/2 split).  exp is taken as exp2 with log2(e) folded into the scale
+// ("Triton Ascend Attention", 在线 Softmax 算法, which multiplies by 1.44269504).
+//
+// How it runs on sm_103a (one CTA = one pair of 128-row query tiles of one head):
+//   warp 8      : load warp.  TMA brings Q (once) and a ring of K/V tiles into
+//                 shared memory, 128B-swizzled, completing on mbarriers.
+//   warp 9      : MMA warp.  One thread issues tcgen05.mma:
+//                   S_i = Q_i K_j^T   (A and B from shared memory)  -> TMEM
+//                   O_i += P_i V_j    (A = P from TMEM, B = V from shared memory)
+//                 and tcgen05.commit signals completion on mbarriers.  It also
+//                 owns the TMEM allocation (512 columns).
+//   warps 0-3/4-7: softmax warpgroups, one per query tile; thread r owns row r
+//                 (TMEM lane r): reads its S row, masks, takes the row max,
+//                 exponentiates, writes P (bf16) back over S, rescales its O row
+//                 in TMEM when the max grew by more than 2^8 (lazy rescale),
+//                 and finally writes O / l (bf16) and the LSE.
+// The two tiles alternate on the tensor cores: while one warpgroup turns S into
+// P, the MMA warp runs the other tile's GEMMs.
+//
+// Every pipeline wait is bounded in time.  A wait that runs out sets the
+// library's device status word (FA_ERR_TIMEOUT), all roles stop, wait for
+// their own copies and MMAs still in flight, free the TMEM and return.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <climits>
+#include <mutex>
+
+#include "fa.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Device status word: 0, or an fa_status code in bits 0..7 and the wait site in bits 8..15.
+__device__ unsigned int g_status;
+
+constexpr int kBlockM = 128;        // query rows per tile (one tcgen05 M=128 MMA)
+constexpr int kBlockN = 128;        // keys per K/V tile
+constexpr int kThreads = 320;       // 8 softmax warps + load warp + MMA warp
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold on the running max (log2 units)
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // one second per wait
+
+enum WaitSite : uint32_t {
+  kSiteLoadKV = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteSoftS, kSiteSoftO
+};
+
+template <int HD>
+struct Layout {
+  static constexpr int kTileBytes = kBlockM * HD * 2;    // one 128 x HD bf16 tile
+  static constexpr int kRegionBytes = kBlockM * 128;     // 128 rows x 128 B (64 bf16): one swizzle column
+  static constexpr int kRegions = HD / 64;
+  static constexpr int kStages = (HD == 128) ? 4 : 8;    // K/V ring slots
+  static constexpr int kOffQ = 0;                        // two Q tiles
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarKVFull = 2;
+  static constexpr int kBarKVEmpty = kBarKVFull + kStages;
+  static constexpr int kBarSFull = kBarKVEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarOFull = kBarPFull + 2;
+  static constexpr int kBarDrain = kBarOFull + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kBytes = kOffAbort + 4;
+  static constexpr int kAlloc = kBytes + 1024;           // slack to align the base to 1 KB
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: S_0 | S_1 | O_0 | O_1.  P_i (bf16 pairs) overwrites the first 64 columns of S_i.
+  __host__ __device__ static constexpr uint32_t col_s(int i) { return 128u * i; }
+  __host__ __device__ static constexpr uint32_t col_o(int i) { return 256u + HD * i; }
+};
+
+static_assert(Layout<128>::kAlloc <= 232448, "shared memory budget (D=128)");
+static_assert(Layout<64>::kAlloc <= 232448, "shared memory budget (D=64)");
+
+struct Params {
+  CUtensorMap tm_q;   // 3-D views [B*H][L][D] of Q, K, V; box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  __nv_bfloat16* o;
+  float* lse;
+  int bh_count;
+  int Lq;
+  int Lk;
+  int causal;
+  int n_pairs;        // ceil(Lq / 256)
+  float scale_log2;   // scale * log2(e)
+  uint32_t flags;     // test hooks (fa_debug_set)
+  unsigned long long wait_limit_ns;
+};
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
+// A K-major, B K-major or (b_mn_major) MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4)                            // D format: f32
+         | (1u << 7)                          // A format: bf16
+         | (1u << 10)                         // B format: bf16
+         | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a 128B-swizzled operand (tcgen05 format).
+// lbo/sbo in bytes: for K-major operands sbo is the distance between 8-row
+// groups (1024 B) and lbo is unused; for MN-major operands lbo is the distance
+// between 64-element column blocks and sbo the distance between 8-row K groups.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu)
+         | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16)
+         | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32)
+         | (1ull << 46)     // descriptor version for tcgen05
+         | (2ull << 61);    // 128-byte swizzle
+}
+
+// Bounded wait on an mbarrier phase.  Gives up when another role aborted or after
+// `limit_ns`, in which case it records FA_ERR_TIMEOUT and raises the CTA abort flag.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        unsigned long long limit_ns, uint32_t site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicCAS(&g_status, 0u, static_cast<unsigned>(FA_ERR_TIMEOUT) | (site << 8));
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used while draining: ignores the abort flag (the copy or MMA being
+// waited for completes on its own), still limited in time.
+__device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
+  using L = Layout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_addr(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work unit: heaviest query-tile pairs first (they have the most key tiles when causal).
+  const int unit = blockIdx.x;
+  const int pair = p.n_pairs - 1 - unit / p.bh_count;
+  const int bh = unit % p.bh_count;
+  const int q0 = pair * 2 * kBlockM;
+  const int nkv = (p.Lk + kBlockN - 1) / kBlockN;
+  int nblk[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int qi = q0 + i * kBlockM;
+    nblk[i] = (qi >= p.Lq) ? 0 : (p.causal ? min(nkv, qi / kBlockN + 1) : nkv);
+  }
+  const int nmax = max(nblk[0], nblk[1]);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(L::kBarQFull + i), 1);
+      ptx::mbar_init(bar(L::kBarSFull + i), 1);
+      ptx::mbar_init(bar(L::kBarPFull + i), 4 * 32);
+      ptx::mbar_init(bar(L::kBarOFull + i), 1);
+    }
+#pragma unroll
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(L::kBarKVFull + s), 1);
+      ptx::mbar_init(bar(L::kBarKVEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(L::kBarDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const unsigned long long limit = p.wait_limit_ns;
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int wg = warp >> 2;           // query tile 0 or 1 of the pair
+    const int rw = warp & 3;            // TMEM lane quarter this warp may access
+    const int row = rw * 32 + lane;     // row of the tile == TMEM lane
+    const int n_blocks = nblk[wg];
+    if (n_blocks > 0) {
+      const int qt = q0 + wg * kBlockM;
+      const int q = qt + row;
+      const int key_lim = p.causal ? min(p.Lk, q + 1) : p.Lk;
+      const int first_diag = p.causal ? qt / kBlockN : INT_MAX;
+      const uint32_t lane_off = static_cast<uint32_t>(rw * 32) << 16;
+      const uint32_t t_s = tmem + lane_off + L::col_s(wg);
+      const uint32_t t_o = tmem + lane_off + L::col_o(wg);
+      const float sl2 = p.scale_log2;
+      float m = -INFINITY;   // running max of scaled scores, log2 units (possibly stale by < 8)
+      float l = 0.0f;        // running sum of exp2(s*sl2 - m)
+      bool ok = true;
+      for (int j = 0; j < n_blocks; ++j) {
+        ok = wait_phase(bar(L::kBarSFull + wg), j & 1, abort_flag, limit, kSiteSoftS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[128];
+        ptx::tmem_ld32x32b_x128(t_s, sr);
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        if (j >= first_diag || (j + 1) * kBlockN > p.Lk) {
+          const int lim = key_lim - j * kBlockN;   // columns c < lim are allowed keys
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = s[k];
+#pragma unroll
+        for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[c + k]);
+        }
+        const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = fmaxf(m, rmax * sl2);
+        const bool rescale = m_new > m + kRescaleLog2;
+        float alpha = 1.0f;
+        if (rescale) {
+          alpha = ptx::ex2_approx(m - m_new);
+          m = m_new;
+        }
+        const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float a = ptx::ex2_approx(fmaf(s[2 * c], sl2, neg_m));
+          const float b = ptx::ex2_approx(fmaf(s[2 * c + 1], sl2, neg_m));
+          sum[c & 3] += a + b;
+          pk[c] = ptx::pack_bf16x2(a, b);
+        }
+        l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+        ptx::tmem_st32x32b_x64(t_s, pk);
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t o[32];
+            ptx::tmem_ld32x32b_x32(t_o + c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            ptx::tmem_st32x32b_x32(t_o + c0, o);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarPFull + wg));
+      }
+      if (ok) {
+        ok = wait_phase(bar(L::kBarOFull + wg), 0, abort_flag, limit, kSiteSoftO);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const bool store = q < p.Lq;
+        __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + (store ? q : 0)) * HD;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld32x32b_x32(t_o + c0, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                     __uint_as_float(o[2 * c + 1]) * inv_l);
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        if (store) {
+          p.lse[static_cast<size_t>(bh) * p.Lq + q] = (m + log2f(l)) * 0.69314718055994531f;
+        }
+      }
+    }
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ load warp
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&p.tm_q);
+      ptx::prefetch_tensormap(&p.tm_k);
+      ptx::prefetch_tensormap(&p.tm_v);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (nblk[i] > 0) {
+          ptx::mbar_arrive_expect_tx(bar(L::kBarQFull + i), L::kTileBytes);
+#pragma unroll
+          for (int r = 0; r < L::kRegions; ++r)
+            ptx::tma_load_3d(sbase + L::kOffQ + i * L::kTileBytes + r * L::kRegionBytes, &p.tm_q,
+                             bar(L::kBarQFull + i), 64 * r, q0 + i * kBlockM, bh);
+        }
+      }
+      int last_fill[L::kStages];
+#pragma unroll
+      for (int s = 0; s < L::kStages; ++s) last_fill[s] = -1;
+      bool ok = true;
+      for (int j = 0; j < nmax && ok; ++j) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {   // t = 0: K_j, t = 1: V_j
+          const int it = 2 * j + t;
+          const int s = it % L::kStages;
+          const uint32_t ph = (it / L::kStages) & 1;
+          if (!wait_phase(bar(L::kBarKVEmpty + s), ph ^ 1u, abort_flag, limit, kSiteLoadKV)) {
+            ok = false;
+            break;
+          }
+          if ((p.flags & 1u) && j == 0 && t == 1) continue;   // test hook: withhold V_0
+          ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
+#pragma unroll
+          for (int r = 0; r < L::kRegions; ++r)
+            ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + r * L::kRegionBytes,
+                             t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * r, j * kBlockN, bh);
+          last_fill[s] = it;
+        }
+      }
+      // Drain: every copy this thread started has landed before the CTA may exit.
+#pragma unroll
+      for (int s = 0; s < L::kStages; ++s)
+        if (last_fill[s] >= 0)
+          drain_phase(bar(L::kBarKVFull + s), (last_fill[s] / L::kStages) & 1, limit);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (nblk[i] > 0) drain_phase(bar(L::kBarQFull + i), 0, limit);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ MMA warp
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false);
+      constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true);
+      auto issue_s = [&](int i, int slot) {
+        const uint32_t a0 = sbase + L::kOffQ + i * L::kTileBytes;
+        const uint32_t b0 = sbase + L::kOffKV + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kRegionBytes + (kk & 3) * 32;
+          ptx::mma_ss(tmem + L::col_s(i), sw128_desc(a0 + off, 16, 1024),
+                      sw128_desc(b0 + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int slot, bool accumulate) {
+        const uint32_t b0 = sbase + L::kOffKV + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          ptx::mma_ts(tmem + L::col_o(i), tmem + L::col_s(i) + kk * 8,
+                      sw128_desc(b0 + kk * 16 * 128, L::kRegionBytes, 1024), kIdescPV,
+                      (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (ok && nblk[i] > 0)
+          ok = wait_phase(bar(L::kBarQFull + i), 0, abort_flag, limit, kSiteMmaQ);
+      if (ok && nmax > 0) ok = wait_phase(bar(L::kBarKVFull + 0), 0, abort_flag, limit, kSiteMmaK);
+      if (ok && nmax > 0) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (nblk[i] > 0) {
+            issue_s(i, 0);
+            ptx::mma_commit(bar(L::kBarSFull + i));
+          }
+        }
+        ptx::mma_commit(bar(L::kBarKVEmpty + 0));
+      }
+      for (int j = 0; j < nmax && ok; ++j) {
+        const int it_v = 2 * j + 1;
+        const int slot_v = it_v % L::kStages;
+        if (!wait_phase(bar(L::kBarKVFull + slot_v), (it_v / L::kStages) & 1, abort_flag, limit,
+                        kSiteMmaV)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const int it_k = 2 * j + 2;
+        const int slot_k = it_k % L::kStages;
+        bool k_ready = false;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (j >= nblk[i]) continue;
+          if (!wait_phase(bar(L::kBarPFull + i), j & 1, abort_flag, limit, kSiteMmaP)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          issue_pv(i, slot_v, j > 0);
+          if (j == nblk[i] - 1) ptx::mma_commit(bar(L::kBarOFull + i));
+          if (j + 1 < nblk[i]) {
+            if (!k_ready) {
+              if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
+                              limit, kSiteMmaK)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(i, slot_k);
+            ptx::mma_commit(bar(L::kBarSFull + i));
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(L::kBarKVEmpty + slot_v));
+        if (k_ready) ptx::mma_commit(bar(L::kBarKVEmpty + slot_k));
+      }
+      // Drain: every MMA this thread issued has completed before TMEM is freed.
+      ptx::mma_commit(bar(L::kBarDrain));
+      drain_phase(bar(L::kBarDrain), 0, limit);
+    }
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+}  // namespace fa
+
+// ============================================================================ host side
+namespace {
+
+using fa::Params;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  bool attr64 = false;
+  bool attr128 = false;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<unsigned> g_debug_flags{0};
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return na && nb && pa < pb + nb && pb < pa + na;
+}
+
+// Per-device set-up: capability check, kernel attributes, encoder entry point.
+fa_status prepare_device(int dev, int D) {
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& info = g_devices[dev];
+  if (!info.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    info.supported = (major == 10 && minor == 3);
+    info.ready = true;
+  }
+  if (!info.supported) return FA_ERR_UNSUPPORTED;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return FA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (D == 64 && !info.attr64) {
+    if (cudaFuncSetAttribute(fa::fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             fa::Layout<64>::kAlloc) != cudaSuccess)
+      return FA_ERR_CUDA;
+    info.attr64 = true;
+  }
+  if (D == 128 && !info.attr128) {
+    if (cudaFuncSetAttribute(fa::fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             fa::Layout<128>::kAlloc) != cudaSuccess)
+      return FA_ERR_CUDA;
+    info.attr128 = true;
+  }
+  return FA_OK;
+}
+
+// 3-D tensor map over a contiguous [BH][L][D] bf16 tensor; box = 64 features x 128 rows x 1 head.
+bool encode_map(CUtensorMap* map, const void* base, long long BH, long long L, int D) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L) * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estrides[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int B, int H, int Lq, int Lk, int D, int causal, float scale,
+                            cudaStream_t stream) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long rows_q = bh * Lq;
+  if (rows_q == 0) return FA_OK;
+  if (Lk < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  const uintptr_t align_bits = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                               reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                               reinterpret_cast<uintptr_t>(LSE);
+  if (align_bits & 15u) return FA_ERR_INVALID_ARG;
+  const long long elems_q = rows_q * D, elems_k = bh * Lk * D;
+  if (elems_q > (1ll << 40) || elems_k > (1ll << 40)) return FA_ERR_INVALID_ARG;
+  const size_t bytes_q = static_cast<size_t>(elems_q) * 2, bytes_k = static_cast<size_t>(elems_k) * 2;
+  const size_t bytes_lse = static_cast<size_t>(rows_q) * 4;
+  if (overlaps(O, bytes_q, Q, bytes_q) || overlaps(O, bytes_q, K, bytes_k) ||
+      overlaps(O, bytes_q, V, bytes_k) || overlaps(O, bytes_q, LSE, bytes_lse) ||
+      overlaps(LSE, bytes_lse, Q, bytes_q) || overlaps(LSE, bytes_lse, K, bytes_k) ||
+      overlaps(LSE, bytes_lse, V, bytes_k))
+    return FA_ERR_INVALID_ARG;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  const fa_status prep = prepare_device(dev, D);
+  if (prep != FA_OK) return prep;
+
+  Params p;
+  if (!encode_map(&p.tm_q, Q, bh, Lq, D) || !encode_map(&p.tm_k, K, bh, Lk, D) ||
+      !encode_map(&p.tm_v, V, bh, Lk, D))
+    return FA_ERR_CUDA;
+  p.o = static_cast<__nv_bfloat16*>(O);
+  p.lse = LSE;
+  p.bh_count = static_cast<int>(bh);
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.causal = causal ? 1 : 0;
+  p.n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.flags = g_debug_flags.load();
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitNs;
+  if (bh > INT_MAX || static_cast<long long>(p.n_pairs) * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  if (p.flags & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_pairs * bh));
+  cfg.blockDim = dim3(fa::kThreads);
+  cfg.stream = stream;
+  cudaError_t err;
+  if (D == 64) {
+    cfg.dynamicSmemBytes = fa::Layout<64>::kAlloc;
+    err = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<64>, p);
+  } else {
+    cfg.dynamicSmemBytes = fa::Layout<128>::kAlloc;
+    err = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<128>, p);
+  }
+  return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dim or device";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel pipeline wait ran out of time";
+  }
+  return "unknown fa_status";
+}
+
+extern "C" fa_status fa_last_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, fa::g_status, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return static_cast<fa_status>(v & 0xffu);
+}
+
+extern "C" fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns) {
+  g_debug_flags.store(flags);
+  g_wait_limit_ns.store(wait_limit_ns);
+  return FA_OK;
+}

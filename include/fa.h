@@ -1,0 +1,107 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library, libfa.so.
+ *
+ * Operation (one call = one forward pass over a whole batch):
+ *   For every batch b, head h and query row i < Lq,
+ *     S_ij  = scale * <Q[b,h,i,:], K[b,h,j,:]>           for allowed keys j
+ *     O[b,h,i,:] = sum_j softmax_j(S_i.) * V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp(S_ij)                      (natural log)
+ *   Allowed keys: all j < Lk; with causal != 0 only j <= i (top-left aligned,
+ *   diagonal kept).
+ *
+ * Where the operation is defined:
+ *   - "Triton Ascend Attention" (skillmd.com), section 标准 Attention 计算流程:
+ *     Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V.
+ *   - wsisp.com post "FlashAttention-2 forward in Triton": the host wrapper
+ *     (Q, K, V of shape [B, H, L, D]; output O like Q; per-row statistic M of
+ *     shape [B, H, Lq] in fp32; scale 1/sqrt(D)), the outer kernel's epilogue
+ *     (M = m + log(l), O = O / l), and the inner loop (online softmax over
+ *     streamed K/V tiles, causal mask offs_q >= offs_kv).
+ *   - "flash-attention-kernel" skill card (skillsmp.com): head dims 64 and 128,
+ *     causal keeps offs_m >= offs_n (diagonal included), tiles past the
+ *     diagonal are skipped.
+ *
+ * Layout: Q [B,H,Lq,D], K and V [B,H,Lk,D], O [B,H,Lq,D], all bf16, contiguous,
+ * row-major (D fastest).  LSE [B,H,Lq] fp32, contiguous.  All five pointers are
+ * DEVICE pointers on the current CUDA device.
+ *
+ * Ownership: the caller allocates and owns every buffer.  The library keeps no
+ * pointer after the call returns and allocates no device memory.  Q, K and V
+ * are only read; O and LSE are only written and must not overlap Q, K, V or
+ * each other.
+ *
+ * Execution: asynchronous on `stream` (0 = the legacy default stream).  The
+ * call returns after the launch is queued.  Launch failures are reported by
+ * the return value; failures detected by the kernel itself (a pipeline wait
+ * that ran out of time) are reported by fa_last_device_status().
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* a null/misaligned/overlapping pointer, a bad size or scale */
+    FA_ERR_UNSUPPORTED = 2,   /* D not in {64,128}, or the device is not sm_103 */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch, attributes, ...) */
+    FA_ERR_TIMEOUT = 4        /* a kernel pipeline wait ran out of time (device status only) */
+} fa_status;
+
+/*
+ * fa_fwd -- exact attention forward (the FlashAttention-2 forward pass).
+ *
+ *   Q, K, V : const bf16 device pointers, contiguous [B,H,Lq,D] / [B,H,Lk,D] / [B,H,Lk,D].
+ *   O       : bf16 device pointer, [B,H,Lq,D], written (round to nearest even).
+ *   LSE     : fp32 device pointer, [B,H,Lq], written: ln of the sum of exp of the
+ *             scaled scores over the allowed keys of each row.
+ *   B, H    : batch size and head count, >= 0.
+ *   Lq, Lk  : query and key sequence lengths; Lq >= 0, Lk >= 1 (Lk = 0 would make
+ *             every softmax empty).  Any lengths, not only multiples of 128.
+ *   D       : head dimension, 64 or 128.
+ *   causal  : 0 = every key; nonzero = key j allowed for row i iff j <= i.
+ *   scale   : multiplies Q.K before the softmax; finite and > 0 (1/sqrt(D) is the
+ *             usual choice).
+ *   stream  : CUDA stream to launch on.
+ *
+ * Returns FA_OK once the kernel is queued.  B*H*Lq == 0 returns FA_OK without a
+ * launch (pointers may then be NULL).  Argument errors return
+ * FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED before anything is launched; all
+ * pointers must be 16-byte aligned (the tensor-memory-access unit requires it).
+ * Rows and keys are limited to 2^31-1 and B*H*L*D elements to 2^40.
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int H, int Lq, int Lk, int D, int causal, float scale,
+                 cudaStream_t stream);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * fa_last_device_status -- synchronise `stream`, then read and clear the
+ * library's device status word on the current device.  Returns FA_OK if no
+ * kernel launched since the last read reported a problem, FA_ERR_TIMEOUT if a
+ * pipeline wait inside a kernel gave up (the kernel then stops early and its
+ * outputs are undefined), or FA_ERR_CUDA if the synchronisation failed.
+ */
+fa_status fa_last_device_status(cudaStream_t stream);
+
+/*
+ * fa_debug_set -- test hook, process-wide.  `wait_limit_ns` bounds every
+ * pipeline wait inside the kernels (0 restores the default of one second).
+ * `flags` bit 0 makes the load warp withhold the first value-tile load, so
+ * that the consumers' waits run out and the kernel reports FA_ERR_TIMEOUT
+ * through fa_last_device_status() instead of completing.  Not for production
+ * use; returns FA_OK.
+ */
+fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

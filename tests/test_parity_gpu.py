@@ -1,0 +1,189 @@
+"""GPU parity: fa_fwd (through the C ABI) against the fp64 oracle.
+
+Tolerances: max-abs 2e-2 on O (bf16 output) and 1e-3 on LSE (fp32), the bar
+the method's specification sets.  Small cases are compared element by element
+on every row; the full-size workloads on a seeded sample of rows (plus rows at
+tile edges), computed one by one by the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_60_gb300 as fa
+from exact_attention_60_gb300.workloads import WORKLOADS, make_qkv, make_workload_inputs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 2e-2
+TOL_LSE = 1e-3
+
+
+def run_fa(q, k, v, causal, scale=None):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = fa.attention(qd, kd, vd, causal=causal, scale=scale)
+    st = fa.fa_last_device_status()
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check_full(oracle_mod, q, k, v, causal, scale):
+    o, lse = run_fa(q, k, v, causal, scale)
+    ref_o, ref_l = oracle_mod.attn_full(q, k, v, causal, scale)
+    err_o = np.abs(o - ref_o).max()
+    err_l = np.abs(lse - ref_l).max()
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert err_o <= TOL_O, f"max|dO| = {err_o}"
+    assert err_l <= TOL_LSE, f"max|dLSE| = {err_l}"
+    return err_o, err_l
+
+
+def check_rows(oracle_mod, q, k, v, causal, scale, pairs, o, lse):
+    """Compare sampled (bh, i) rows of a GPU result with the oracle, row by row."""
+    B, H = q.shape[0], q.shape[1]
+    worst_o = worst_l = 0.0
+    for bh in np.unique(pairs[:, 0]):
+        rows = pairs[pairs[:, 0] == bh, 1]
+        b, h = divmod(int(bh), H)
+        ref_o, ref_l = oracle_mod.attn_head(q[b, h], k[b, h], v[b, h], causal, scale, rows=rows)
+        got_o = o[b, h][rows].float().numpy()
+        got_l = lse[b, h][rows].numpy()
+        worst_o = max(worst_o, float(np.abs(got_o - ref_o).max()))
+        worst_l = max(worst_l, float(np.abs(got_l - ref_l).max()))
+    assert worst_o <= TOL_O, f"max|dO| = {worst_o}"
+    assert worst_l <= TOL_LSE, f"max|dLSE| = {worst_l}"
+    return worst_o, worst_l
+
+
+@pytest.mark.parametrize("name", ["tiny_d64", "seq1k_d64", "seq1k_d64_causal"])
+def test_workload_full(oracle_mod, name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    check_full(oracle_mod, q, k, v, w.causal, w.scale)
+
+
+@pytest.mark.parametrize("name", ["seq4k_d128_causal", "seq16k_d128_causal",
+                                  "cross_q500_k8191_d128"])
+def test_workload_sampled(oracle_mod, name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=w.causal, scale=w.scale)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse = o.cpu(), lse.cpu()
+    extra = (383, 384, 499) if w.Lq == 500 else ()
+    pairs = sample_rows(w, 512, extra)
+    check_rows(oracle_mod, q, k, v, w.causal, w.scale, pairs, o, lse)
+    # properties that hold at any size, on every row: finite outputs, and
+    # |O| bounded by the largest |V| entry of the head (a convex combination).
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    vmax = v.float().abs().amax(dim=(2, 3), keepdim=True)
+    assert (o.float().abs() <= vmax + 1e-2).all()
+
+
+EDGE_LQ = [1, 127, 128, 129, 255, 257, 500]
+EDGE_LK = [1, 2, 128, 129, 255, 500]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lk", EDGE_LK)
+@pytest.mark.parametrize("Lq", EDGE_LQ)
+def test_edge_shapes(oracle_mod, Lq, Lk, causal, D):
+    q, k, v = make_qkv(1, 2, Lq, Lk, D, seed=Lq * 1000 + Lk + D)
+    check_full(oracle_mod, q, k, v, causal, 1.0 / math.sqrt(D))
+
+
+@pytest.mark.parametrize("Lq,Lk,causal,D", [(8191, 8191, True, 128), (1000, 3000, True, 64),
+                                             (3000, 1000, True, 128), (777, 4099, False, 64)])
+def test_larger_ragged(oracle_mod, Lq, Lk, causal, D):
+    q, k, v = make_qkv(2, 3, Lq, Lk, D, seed=Lq + 7 * Lk)
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    rng = np.random.default_rng(Lq * 31 + Lk)
+    pairs = np.stack([rng.integers(0, 6, 96), rng.integers(0, Lq, 96)], axis=1)
+    edge = np.array([[0, 0], [5, Lq - 1], [1, min(127, Lq - 1)], [2, min(128, Lq - 1)],
+                     [3, min(255, Lq - 1)], [4, min(256, Lq - 1)]])
+    check_rows(oracle_mod, q, k, v, causal, 1.0 / math.sqrt(D), np.concatenate([pairs, edge]),
+               o.cpu(), lse.cpu())
+
+
+def test_non_default_scale(oracle_mod):
+    q, k, v = make_qkv(2, 2, 300, 260, 128, seed=99, sigma_qk=2.0)
+    for scale in (0.02, 0.3):
+        check_full(oracle_mod, q, k, v, True, scale)
+        check_full(oracle_mod, q, k, v, False, scale)
+
+
+def test_large_logits(oracle_mod):
+    """Scores spread over hundreds of units: the lazy rescale has to fire often."""
+    q, k, v = make_qkv(1, 2, 384, 640, 128, seed=5, sigma_qk=6.0)
+    check_full(oracle_mod, q, k, v, False, 1.0 / math.sqrt(128))
+    check_full(oracle_mod, q, k, v, True, 1.0 / math.sqrt(128))
+
+
+def test_increasing_scores(oracle_mod):
+    """Keys whose scores grow along the sequence force a new row max on every tile."""
+    Lk, D = 1024, 64
+    q = torch.ones(1, 1, 256, D)
+    ramp = torch.linspace(0.0, 40.0, Lk)[:, None] / D
+    k = (ramp * torch.ones(1, D)).reshape(1, 1, Lk, D)
+    v = torch.randn(1, 1, Lk, D, generator=torch.Generator().manual_seed(3))
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    check_full(oracle_mod, q, k, v, False, 1.0)
+    check_full(oracle_mod, q, k, v, True, 1.0)
+
+
+def test_guard_bands_untouched():
+    """O and LSE sit inside larger buffers whose margins hold a sentinel; the
+    kernel must write exactly [B,H,Lq,D] and [B,H,Lq] (ragged Lq included)."""
+    dev = torch.device("cuda:0")
+    B, H, Lq, Lk, D = 2, 3, 300, 200, 128
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, Lq, Lk, D, seed=11))
+    pad = 4096
+    n_o, n_l = B * H * Lq * D, B * H * Lq
+    o_buf = torch.full((n_o + 2 * pad,), float("nan"), device=dev, dtype=torch.bfloat16)
+    l_buf = torch.full((n_l + 2 * pad,), float("nan"), device=dev, dtype=torch.float32)
+    o = o_buf[pad:pad + n_o].view(B, H, Lq, D)
+    lse = l_buf[pad:pad + n_l].view(B, H, Lq)
+    for causal in (False, True):
+        fa.attention(q, k, v, causal=causal, out=o, lse=lse)
+        assert fa.fa_last_device_status() == fa.FA_OK
+        assert torch.isnan(o_buf[:pad].float()).all() and torch.isnan(o_buf[pad + n_o:].float()).all()
+        assert torch.isnan(l_buf[:pad]).all() and torch.isnan(l_buf[pad + n_l:]).all()
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+def test_deterministic():
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(2, 4, 700, 900, 128, seed=12))
+    o1, l1 = fa.attention(q, k, v, causal=True)
+    o2, l2 = fa.attention(q, k, v, causal=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_empty_batch_is_noop():
+    dev = torch.device("cuda:0")
+    q = torch.empty(0, 2, 16, 64, device=dev, dtype=torch.bfloat16)
+    k = torch.empty(0, 2, 16, 64, device=dev, dtype=torch.bfloat16)
+    o, lse = fa.attention(q, k, k, causal=False)
+    assert o.numel() == 0 and lse.numel() == 0
+    assert fa.fa_last_device_status() == fa.FA_OK
+
+
+def test_stream_argument():
+    """fa_fwd runs on the stream it is given."""
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(1, 2, 256, 256, 64, seed=13))
+    ref_o, ref_l = fa.attention(q, k, v)
+    s = torch.cuda.Stream()
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 256, device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    st = fa.fa_fwd(q, k, v, o, lse, 1, 2, 256, 256, 64, 0, 0.125, s)
+    assert st == fa.FA_OK
+    assert fa.fa_last_device_status(s) == fa.FA_OK
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
