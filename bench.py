@@ -1,0 +1,390 @@
+"""Benchmark: attention forward TFLOP/s on one GB300 (and % of dense bf16 peak).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one fa_fwd launch over the whole workload (every batch, head and
+query tile), inputs already resident in HBM.  TFLOP/s counts 4*D flops per
+unmasked (query, key) pair.  Between timed steps the inputs rotate over enough
+copies that their total exceeds twice the L2 cache.
+
+Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
+  e2e          the same metric through the public call with pinned host buffers,
+               host->device copies of Q, K, V and device->host copies of O, LSE
+               inside the timed region;
+  roofline     achieved TFLOP/s of the kernel against the measured bf16 peak;
+  cpu_baseline the fp64 oracle timed on the host cores on a bounded row sample;
+  clocks       SM clocks and throttle reasons sampled during the timed region.
+With --impl reference the fp64 CPU oracle is the measured arm (bounded row
+samples of the same workload per step), printed with "impl": "reference".
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the whole workload on
+its own GPU (independent problems, no collective on the data path); the time is
+the max over ranks and the value the total work of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_60_gb300.workloads import WORKLOADS, make_workload_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "seq16k_d128_causal"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_NAME = "fa_fwd_kernel"
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                data = json.load(f)
+            return data, "measured"
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks: dict, key: str, default: float) -> float:
+    v = peaks.get(key)
+    if isinstance(v, dict):  # tolerate {"value": x, ...}
+        v = v.get("value")
+    try:
+        return float(v)
+    except (TypeError, ValueError):
+        return default
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError as e:
+            self.error = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.error or "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"error": "no clock samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 or n_gpus > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=os.environ.get("BENCH_DIST_BACKEND", "nccl"))
+        return dist, dist.get_rank(), dist.get_world_size(), local
+    return None, rank, world, local
+
+
+def reduce_max(dist, value: float, device=None) -> float:
+    """Max of a float over all ranks (a timing reduction, not part of the data path)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def row_flops(w, rows) -> int:
+    if w.causal:
+        return int(sum(4 * w.D * min(int(i) + 1, w.Lk) for i in rows))
+    return 4 * w.D * w.Lk * len(rows)
+
+
+def time_oracle(w, q, k, v, budget_s: float, heads: int = 2, rows_per_call: int = 64, seed: int = 0):
+    """Run the oracle on batches of sampled rows of a few heads until ``budget_s``
+    seconds of oracle time are spent; return (flops, seconds, rows, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    head_ids = rng.choice(w.B * w.H, size=min(heads, w.B * w.H), replace=False)
+    per_head = []
+    for bh in head_ids:
+        b, h = divmod(int(bh), w.H)
+        per_head.append(tuple(np.ascontiguousarray(t[b, h].float().numpy(), dtype=np.float64)
+                              for t in (q, k, v)))
+    flops = 0
+    spent = 0.0
+    nrows = 0
+    it = 0
+    while spent < budget_s:
+        qq, kk, vv = per_head[it % len(per_head)]
+        rows = rng.integers(0, w.Lq, size=rows_per_call)
+        t0 = time.perf_counter()
+        oracle.attn_head(qq, kk, vv, w.causal, w.scale, rows=rows)
+        spent += time.perf_counter() - t0
+        flops += row_flops(w, rows)
+        nrows += rows_per_call
+        it += 1
+    return flops, spent, nrows, oracle.max_threads()
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, w):
+    """The fp64 CPU oracle as the measured arm: each step is a bounded row sample."""
+    dist, rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    q, k, v = make_workload_inputs(w)
+    per_step = max(0.5, min(args.ref_seconds_per_step, 120.0 / args.steps))
+    for s in range(args.warmup):
+        time_oracle(w, q, k, v, per_step / 4, seed=1000 + s)
+    tot_flops = 0
+    tot_time = 0.0
+    tot_rows = 0
+    threads = 1
+    for s in range(args.steps):
+        f, t, n, threads = time_oracle(w, q, k, v, per_step, seed=s)
+        tot_flops += f
+        tot_time += t
+        tot_rows += n
+    value = tot_flops / tot_time / 1e12
+    sample = (f"{tot_rows} query rows sampled uniformly from 2 heads of the workload, "
+              f"about {per_step:g} s of oracle time per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot_time / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import exact_attention_60_gb300 as fa
+    from exact_attention_60_gb300 import build as fa_build
+
+    fa_build.build()   # no-op when the library is up to date
+    fa._native.load()
+    dist, rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    q_h, k_h, v_h = make_workload_inputs(w)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+    out_bytes = q_h.numel() * 2 + w.B * w.H * w.Lq * 4
+    n_copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)) + 1)
+    bufs = []
+    base = tuple(t.to(dev) for t in (q_h, k_h, v_h))
+    for c in range(n_copies):
+        qkv = base if c == 0 else tuple(t.clone() for t in base)
+        o = torch.empty_like(qkv[0])
+        lse = torch.empty((w.B, w.H, w.Lq), device=dev, dtype=torch.float32)
+        bufs.append((*qkv, o, lse))
+    torch.cuda.synchronize(dev)
+
+    def launch(i):
+        q, k, v, o, lse = bufs[i % n_copies]
+        st = fa.fa_fwd(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.causal, w.scale, stream)
+        if st != fa.FA_OK:
+            raise RuntimeError(fa.fa_status_string(st))
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"warm-up reported {fa.fa_status_string(st)}")
+
+    sampler = ClockSampler(local)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    # ---------------- timed region: K launches, CUDA events on the launching stream
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        launch(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks = sampler.stop() if not args.no_clocks else None
+    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"timed region reported {fa.fa_status_string(st)}")
+    max_ms = reduce_max(dist, total_ms, dev)
+    flops = w.flops()
+    value = world * flops * args.steps / (max_ms / 1e3) / 1e12
+    ms_per_step = max_ms / args.steps
+    kernel_tflops = flops / (statistics.mean(per_launch_ms) / 1e3) / 1e12
+
+    # ---------------- end to end: pinned host buffers through the public call
+    e2e = None
+    if not args.skip_e2e:
+        q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
+        o_p = torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory()
+        l_p = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32).pin_memory()
+        q_d, k_d, v_d, o_d, l_d = bufs[0]
+
+        def e2e_step():
+            q_d.copy_(q_p, non_blocking=True)
+            k_d.copy_(k_p, non_blocking=True)
+            v_d.copy_(v_p, non_blocking=True)
+            fa.attention(q_d, k_d, v_d, causal=w.causal, scale=w.scale, out=o_d, lse=l_d,
+                         stream=stream)
+            o_p.copy_(o_d, non_blocking=True)
+            l_p.copy_(l_d, non_blocking=True)
+
+        e2e_steps = max(1, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
+        e2e = {"value": world * flops * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "ms_per_step": e2e_ms / e2e_steps}
+
+    peaks, peak_src = load_peaks()
+    peak = peak_value(peaks, "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    traffic = None
+    traffic_path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if os.path.exists(traffic_path):
+        with open(traffic_path) as f:
+            traffic = json.load(f).get(w.name)
+    roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
+                "frac": kernel_tflops / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense (burst)", "kernel": f"{KERNEL_NAME}<{w.D}>"}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu_baseline:
+        f, t, n, threads = time_oracle(w, q_h, k_h, v_h, args.cpu_seconds)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} query rows sampled uniformly from 2 heads of {w.name}, "
+                         f"{t:.1f} s of fp64 oracle time"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(),
+                       "flops_per_step": flops,
+                       "l2": f"inputs rotate over {n_copies} copies "
+                             f"({n_copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
+                       "parallelism": f"replica per GPU x{world}"},
+            "pct_of_peak": 100.0 * kernel_tflops / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds-per-step", type=float, default=5.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 0 or args.steps < 1:
+        ap.error("need --steps >= 1 and --warmup >= 0")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

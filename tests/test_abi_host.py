@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU.
+
+No test here launches a kernel, so the file runs on a machine without a GPU.
+Only argument errors that the library rejects before any CUDA call are used.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_attention_60_gb300 as fa
+from exact_attention_60_gb300 import _native
+from exact_attention_60_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return _native.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\*?\s+\*?(fa_[a-z_]+)\s*\(", text, re.M))
+
+
+def test_header_declares_the_binding_names():
+    assert header_functions() == set(_native.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fa_build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (fa_\w+)$", out, re.M))
+    assert header_functions() <= exported
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = fa.fa_status_string(code)
+        assert s.startswith("FA_"), s
+    assert "unknown" in fa.fa_status_string(99)
+
+
+# Every case below is rejected by argument checks that run before any CUDA call.
+ALIGNED = 1 << 20   # a non-null, 16-byte aligned dummy address (never dereferenced)
+
+
+def call(Q=ALIGNED, K=2 * ALIGNED, V=3 * ALIGNED, O=4 * ALIGNED, LSE=5 * ALIGNED, B=1, H=1,
+         Lq=16, Lk=16, D=64, causal=0, scale=0.125):
+    return fa.fa_fwd(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(Lq=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(Lk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(Q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(LSE=0), fa.FA_ERR_INVALID_ARG),
+    (dict(K=2 * ALIGNED + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(O=4 * ALIGNED + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(O=ALIGNED), fa.FA_ERR_INVALID_ARG),                  # O overlaps Q
+    (dict(LSE=4 * ALIGNED + 64), fa.FA_ERR_INVALID_ARG),       # LSE inside O
+    (dict(O=3 * ALIGNED + 1024), fa.FA_ERR_INVALID_ARG),       # O inside V
+])
+def test_bad_arguments_rejected(lib, kw, expect):
+    assert call(**kw) == expect
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(Lq=0),
+                                dict(B=0, Q=0, K=0, V=0, O=0, LSE=0),
+                                dict(Lq=0, Lk=0)])
+def test_empty_problem_is_ok_without_launch(lib, kw):
+    assert call(**kw) == fa.FA_OK
+
+
+def test_binding_is_argument_marshalling_only():
+    """The binding module holds no attention arithmetic and imports no oracle."""
+    src = open(_native.__file__).read() + open(fa.__file__).read()
+    assert "oracle" not in src
+    for word in ("softmax", "exp(", "exp2", "matmul", "einsum", "@"):
+        assert word not in src.replace("@property", ""), word
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    missing = str(tmp_path / "libfa_missing.so")
+    saved = _native._lib
+    _native._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            _native.load(missing)
+    finally:
+        _native._lib = saved
