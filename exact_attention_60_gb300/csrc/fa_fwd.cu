@@ -45,6 +45,13 @@
 #include "fa.h"
 #include "sm103_ptx.cuh"
 
+#ifndef FA_V2_SOFTMAX
+#define FA_V2_SOFTMAX 0
+#endif
+#ifndef FA_V2_MMA
+#define FA_V2_MMA 0
+#endif
+
 namespace fa {
 
 // Device status word: 0, or an fa_status code in bits 0..7 and the wait site in bits 8..15.
@@ -248,6 +255,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
         }
+#if FA_V2_SOFTMAX
+        float mx[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+        for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx[k] = ptx::fmax3(mx[k], s[c + 2 * k], s[c + 2 * k + 1]);
+        }
+        const float rmax = ptx::fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+#else
         float mx[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = s[k];
@@ -258,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+#endif
         const float m_new = fmaxf(m, rmax * sl2);
         const bool rescale = m_new > m + kRescaleLog2;
         float alpha = 1.0f;
@@ -266,6 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           m = m_new;
         }
         const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+#if FA_V2_SOFTMAX
+        const uint64_t k2 = ptx::pack_f32x2(sl2, sl2);
+        const uint64_t c2 = ptx::pack_f32x2(neg_m, neg_m);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            pk[c] = ptx::exp2_pair_bf16(s[64 * h + 2 * c], s[64 * h + 2 * c + 1], k2, c2, acc[c & 3]);
+          ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
+        }
+        float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
+        float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
+        l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
+#else
         float sum[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
@@ -277,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
         ptx::tmem_st32x32b_x64(t_s, pk);
+#endif
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -375,6 +411,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false);
       constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true);
+#if FA_V2_MMA
+      // Descriptors of the first operand blocks; later blocks differ only in the
+      // start-address field (bits 0..13, address >> 4), which never carries over.
+      const uint64_t desc_q0 = sw128_desc(sbase + L::kOffQ, 16, 1024);
+      const uint64_t desc_kv0 = sw128_desc(sbase + L::kOffKV, 16, 1024);
+      const uint64_t desc_v0 = sw128_desc(sbase + L::kOffKV, L::kRegionBytes, 1024);
+      auto issue_s = [&](int i, int slot) {
+        const uint64_t a = desc_q0 + ((i * L::kTileBytes) >> 4);
+        const uint64_t b = desc_kv0 + ((slot * L::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kRegionBytes + (kk & 3) * 32) >> 4;
+          ptx::mma_ss(tmem + L::col_s(i), a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int slot, bool accumulate) {
+        const uint64_t b = desc_v0 + ((slot * L::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          ptx::mma_ts(tmem + L::col_o(i), tmem + L::col_s(i) + kk * 8, b + ((kk * 16 * 128) >> 4),
+                      kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+#else
       auto issue_s = [&](int i, int slot) {
         const uint32_t a0 = sbase + L::kOffQ + i * L::kTileBytes;
         const uint32_t b0 = sbase + L::kOffKV + slot * L::kTileBytes;
@@ -394,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                       (accumulate || kk > 0) ? 1u : 0u);
         }
       };
+#endif
       bool ok = true;
 #pragma unroll
       for (int i = 0; i < 2; ++i)

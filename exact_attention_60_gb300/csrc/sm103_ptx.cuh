@@ -133,6 +133,45 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two exponentials of a pair: (x0, x1) -> (2^(x0*k + c), 2^(x1*k + c)), with the
+// scale-and-shift done by one packed fp32x2 FMA.  Returns the two values packed
+// as bf16x2 (x0 in bits 0..15) and adds them to the packed running sum `acc`.
+__device__ __forceinline__ uint32_t exp2_pair_bf16(float x0, float x1, uint64_t k2, uint64_t c2,
+                                                   uint64_t& acc) {
+  uint32_t packed;
+  asm("{\n\t.reg .b64 t;\n\t.reg .f32 a, b;\n\t"
+      "mov.b64 t, {%2, %3};\n\t"
+      "fma.rn.ftz.f32x2 t, t, %4, %5;\n\t"
+      "mov.b64 {a, b}, t;\n\t"
+      "ex2.approx.ftz.f32 a, a;\n\t"
+      "ex2.approx.ftz.f32 b, b;\n\t"
+      "cvt.rn.bf16x2.f32 %0, b, a;\n\t"
+      "mov.b64 t, {a, b};\n\t"
+      "add.rn.ftz.f32x2 %1, %1, t;\n\t}"
+      : "=r"(packed), "+l"(acc)
+      : "f"(x0), "f"(x1), "l"(k2), "l"(c2));
+  return packed;
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
 // Two floats to packed bf16x2 (round to nearest even); `lo` lands in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -118,11 +118,27 @@ def test_non_default_scale(oracle_mod):
         check_full(oracle_mod, q, k, v, False, scale)
 
 
+BF16_U = 2.0 ** -8   # unit roundoff of bf16 (8-bit significand, round to nearest)
+
+
 def test_large_logits(oracle_mod):
-    """Scores spread over hundreds of units: the lazy rescale has to fire often."""
+    """Scores spread over hundreds of units: the lazy rescale has to fire often.
+
+    The softmax is then almost one-hot, so |O| approaches max|V| (about 5 here)
+    and the bf16 rounding of P and of O dominates the error.  The bound used is
+    the one the arithmetic gives per element:
+        |dO| <= u * max|V| (P rounded to bf16) + u * |O| (O rounded to bf16) + 1e-3,
+    u = 2^-8.  The workloads of the specification keep the flat 2e-2 bound.
+    """
     q, k, v = make_qkv(1, 2, 384, 640, 128, seed=5, sigma_qk=6.0)
-    check_full(oracle_mod, q, k, v, False, 1.0 / math.sqrt(128))
-    check_full(oracle_mod, q, k, v, True, 1.0 / math.sqrt(128))
+    scale = 1.0 / math.sqrt(128)
+    vmax = v.float().abs().amax(dim=(2, 3)).numpy()[:, :, None, None]
+    for causal in (False, True):
+        o, lse = run_fa(q, k, v, causal, scale)
+        ref_o, ref_l = oracle_mod.attn_full(q, k, v, causal, scale)
+        bound = BF16_U * (vmax + np.abs(ref_o)) + 1e-3
+        assert (np.abs(o - ref_o) <= bound).all(), float((np.abs(o - ref_o) - bound).max())
+        assert np.abs(lse - ref_l).max() <= TOL_LSE
 
 
 def test_increasing_scores(oracle_mod):
