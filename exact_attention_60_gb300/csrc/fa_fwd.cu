@@ -45,13 +45,6 @@
 #include "fa.h"
 #include "sm103_ptx.cuh"
 
-#ifndef FA_V2_SOFTMAX
-#define FA_V2_SOFTMAX 0
-#endif
-#ifndef FA_V2_MMA
-#define FA_V2_MMA 0
-#endif
-
 namespace fa {
 
 // Device status word: 0, or an fa_status code in bits 0..7 and the wait site in bits 8..15.
@@ -140,7 +133,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 
 // Bounded wait on an mbarrier phase.  Gives up when another role aborted or after
 // `limit_ns`, in which case it records FA_ERR_TIMEOUT and raises the CTA abort flag.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                         unsigned long long limit_ns, uint32_t site) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -255,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
         }
-#if FA_V2_SOFTMAX
         float mx[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
@@ -265,18 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           for (int k = 0; k < 4; ++k) mx[k] = ptx::fmax3(mx[k], s[c + 2 * k], s[c + 2 * k + 1]);
         }
         const float rmax = ptx::fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-#else
-        float mx[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = s[k];
-#pragma unroll
-        for (int c = 8; c < 128; c += 8) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[c + k]);
-        }
-        const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-#endif
         const float m_new = fmaxf(m, rmax * sl2);
         const bool rescale = m_new > m + kRescaleLog2;
         float alpha = 1.0f;
@@ -285,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           m = m_new;
         }
         const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-#if FA_V2_SOFTMAX
         const uint64_t k2 = ptx::pack_f32x2(sl2, sl2);
         const uint64_t c2 = ptx::pack_f32x2(neg_m, neg_m);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -300,19 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
         float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
         l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
-#else
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float a = ptx::ex2_approx(fmaf(s[2 * c], sl2, neg_m));
-          const float b = ptx::ex2_approx(fmaf(s[2 * c + 1], sl2, neg_m));
-          sum[c & 3] += a + b;
-          pk[c] = ptx::pack_bf16x2(a, b);
-        }
-        l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
-        ptx::tmem_st32x32b_x64(t_s, pk);
-#endif
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -408,10 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     __syncwarp();
   } else {
     // ------------------------------------------------------------ MMA warp
-    if (lane == 0) {
+    if (lane == 0) {   // one thread issues every MMA and commit
       constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false);
       constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true);
-#if FA_V2_MMA
       // Descriptors of the first operand blocks; later blocks differ only in the
       // start-address field (bits 0..13, address >> 4), which never carries over.
       const uint64_t desc_q0 = sw128_desc(sbase + L::kOffQ, 16, 1024);
@@ -434,27 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-#else
-      auto issue_s = [&](int i, int slot) {
-        const uint32_t a0 = sbase + L::kOffQ + i * L::kTileBytes;
-        const uint32_t b0 = sbase + L::kOffKV + slot * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kRegionBytes + (kk & 3) * 32;
-          ptx::mma_ss(tmem + L::col_s(i), sw128_desc(a0 + off, 16, 1024),
-                      sw128_desc(b0 + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int i, int slot, bool accumulate) {
-        const uint32_t b0 = sbase + L::kOffKV + slot * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          ptx::mma_ts(tmem + L::col_o(i), tmem + L::col_s(i) + kk * 8,
-                      sw128_desc(b0 + kk * 16 * 128, L::kRegionBytes, 1024), kIdescPV,
-                      (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-#endif
       bool ok = true;
 #pragma unroll
       for (int i = 0; i < 2; ++i)
@@ -512,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         ptx::mma_commit(bar(L::kBarKVEmpty + slot_v));
         if (k_ready) ptx::mma_commit(bar(L::kBarKVEmpty + slot_k));
       }
-      // Drain: every MMA this thread issued has completed before TMEM is freed.
+      // Drain: every MMA issued has completed before TMEM is freed.
       ptx::mma_commit(bar(L::kBarDrain));
       drain_phase(bar(L::kBarDrain), 0, limit);
     }
