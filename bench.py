@@ -158,6 +158,29 @@ def barrier(dist, device=None):
             dist.barrier()
 
 
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ("exact_attention_60_gb300/csrc/fa_fwd.cu", "exact_attention_60_gb300/csrc/sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    capture was taken on a different kernel source (or never for this workload)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    if data.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    entry = data.get("workloads", {}).get(workload)
+    return None if entry is None else entry["bytes_per_launch"]
+
+
 # ----------------------------------------------------------------------------- CPU oracle legs
 def row_flops(w, rows) -> int:
     if w.causal:
@@ -328,11 +351,7 @@ def run_ours(args, w):
 
     peaks, peak_src = load_peaks()
     peak = peak_value(peaks, "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    traffic = None
-    traffic_path = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    if os.path.exists(traffic_path):
-        with open(traffic_path) as f:
-            traffic = json.load(f).get(w.name)
+    traffic = measured_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
                 "frac": kernel_tflops / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 dense (burst)", "kernel": f"{KERNEL_NAME}<{w.D}>"}

@@ -12,9 +12,12 @@
 // STAGE 1/2 split).  exp is taken as exp2 with log2(e) folded into the scale
 // ("Triton Ascend Attention", 在线 Softmax 算法, which multiplies by 1.44269504).
 //
-// How it runs on sm_103a (one CTA = one pair of 128-row query tiles of one head):
-//   warp 8      : load warp.  TMA brings Q (once) and a ring of K/V tiles into
-//                 shared memory, 128B-swizzled, completing on mbarriers.
+// How it runs on sm_103a.  The grid is persistent: one CTA per SM (shared memory
+// allows no more), each walking a static list of units.  A unit is a pair of
+// 128-row query tiles of one (batch, head); units are numbered heaviest first and
+// dealt out in boustrophedon order so the per-CTA totals stay balanced.
+//   warp 8      : load warp.  TMA brings Q (once per unit) and a ring of K/V tiles
+//                 into shared memory, 128B-swizzled, completing on mbarriers.
 //   warp 9      : MMA warp.  One thread issues tcgen05.mma:
 //                   S_i = Q_i K_j^T   (A and B from shared memory)  -> TMEM
 //                   O_i += P_i V_j    (A = P from TMEM, B = V from shared memory)
@@ -25,8 +28,10 @@
 //                 exponentiates, writes P (bf16) back over S, rescales its O row
 //                 in TMEM when the max grew by more than 2^8 (lazy rescale),
 //                 and finally writes O / l (bf16) and the LSE.
+//   warps 10-11 : spare (they give their registers to the softmax warpgroups).
 // The two tiles alternate on the tensor cores: while one warpgroup turns S into
-// P, the MMA warp runs the other tile's GEMMs.
+// P, the MMA warp runs the other tile's GEMMs.  Between units, the next unit's
+// Q loads and first S GEMMs overlap the current unit's epilogue.
 //
 // Every pipeline wait is bounded in time.  A wait that runs out sets the
 // library's device status word (FA_ERR_TIMEOUT), all roles stop, wait for
@@ -38,6 +43,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <mutex>
@@ -52,7 +58,12 @@ __device__ unsigned int g_status;
 
 constexpr int kBlockM = 128;        // query rows per tile (one tcgen05 M=128 MMA)
 constexpr int kBlockN = 128;        // keys per K/V tile
-constexpr int kThreads = 320;       // 8 softmax warps + load warp + MMA warp
+constexpr int kThreads = 384;       // 8 softmax warps, load warp, MMA warp, 2 spare warps
+// Register split between the warpgroups (setmaxnreg): each softmax thread holds a
+// whole 128-column score row; the load/MMA warpgroup needs far fewer registers.
+// 256 * kRegsSoftmax + 128 * kRegsOther must not exceed 384 * (registers at launch).
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr uint32_t kRegsOther = 112;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold on the running max (log2 units)
@@ -71,13 +82,15 @@ struct Layout {
   static constexpr int kOffQ = 0;                        // two Q tiles
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  static constexpr int kBarQFull = 0;
-  static constexpr int kBarKVFull = 2;
+  static constexpr int kBarQFull = 0;                    // [2]  Q_i landed
+  static constexpr int kBarQEmpty = 2;                   // [2]  last S_i MMA of a unit done
+  static constexpr int kBarKVFull = 4;                   // [kStages]
   static constexpr int kBarKVEmpty = kBarKVFull + kStages;
-  static constexpr int kBarSFull = kBarKVEmpty + kStages;
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarOFull = kBarPFull + 2;
-  static constexpr int kBarDrain = kBarOFull + 2;
+  static constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_i in TMEM
+  static constexpr int kBarPFull = kBarSFull + 2;           // [2] P_i in TMEM, O_i rescaled
+  static constexpr int kBarOFull = kBarPFull + 2;           // [2] last P_i V MMA of a unit done
+  static constexpr int kBarOEmpty = kBarOFull + 2;          // [2] epilogue has read O_i
+  static constexpr int kBarDrain = kBarOEmpty + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -103,10 +116,41 @@ struct Params {
   int Lk;
   int causal;
   int n_pairs;        // ceil(Lq / 256)
+  int n_units;        // n_pairs * bh_count
   float scale_log2;   // scale * log2(e)
   uint32_t flags;     // test hooks (fa_debug_set)
   unsigned long long wait_limit_ns;
 };
+
+// A unit of work: two consecutive 128-row query tiles of one (batch, head).
+// Units are numbered heaviest first (causal: the last query tiles attend to the
+// most keys); a CTA takes units in boustrophedon order over the grid (round r:
+// CTA g takes unit r*G + g when r is even, r*G + G-1-g when odd), which keeps
+// the per-CTA totals within a few percent of each other for causal loads.
+struct Unit {
+  int bh;
+  int q0;
+  int nblk[2];   // key tiles of query tile 0 and 1 (0 = tile absent)
+  int nmax;
+};
+
+__device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
+  const int G = static_cast<int>(gridDim.x);
+  const int g = static_cast<int>(blockIdx.x);
+  const int idx = r * G + ((r & 1) ? (G - 1 - g) : g);
+  if (idx >= p.n_units) return false;
+  const int pair = p.n_pairs - 1 - idx / p.bh_count;
+  u.bh = idx % p.bh_count;
+  u.q0 = pair * 2 * kBlockM;
+  const int nkv = (p.Lk + kBlockN - 1) / kBlockN;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int qi = u.q0 + i * kBlockM;
+    u.nblk[i] = (qi >= p.Lq) ? 0 : (p.causal ? min(nkv, qi / kBlockN + 1) : nkv);
+  }
+  u.nmax = max(u.nblk[0], u.nblk[1]);
+  return true;
+}
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
 // A K-major, B K-major or (b_mn_major) MN-major, shape M x N.
@@ -131,10 +175,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
          | (2ull << 61);    // 128-byte swizzle
 }
 
-// Bounded wait on an mbarrier phase.  Gives up when another role aborted or after
-// `limit_ns`, in which case it records FA_ERR_TIMEOUT and raises the CTA abort flag.
+// Bounded wait on an mbarrier phase (inlined: it sits on every pipeline handoff).
+// Gives up when another role aborted or after `limit_ns`, in which case it
+// records FA_ERR_TIMEOUT and raises the CTA abort flag.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                        unsigned long long limit_ns, uint32_t site) {
+                                           unsigned long long limit_ns, uint32_t site) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
@@ -174,27 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work unit: heaviest query-tile pairs first (they have the most key tiles when causal).
-  const int unit = blockIdx.x;
-  const int pair = p.n_pairs - 1 - unit / p.bh_count;
-  const int bh = unit % p.bh_count;
-  const int q0 = pair * 2 * kBlockM;
-  const int nkv = (p.Lk + kBlockN - 1) / kBlockN;
-  int nblk[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int qi = q0 + i * kBlockM;
-    nblk[i] = (qi >= p.Lq) ? 0 : (p.causal ? min(nkv, qi / kBlockN + 1) : nkv);
-  }
-  const int nmax = max(nblk[0], nblk[1]);
-
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(L::kBarQFull + i), 1);
+      ptx::mbar_init(bar(L::kBarQEmpty + i), 1);
       ptx::mbar_init(bar(L::kBarSFull + i), 1);
       ptx::mbar_init(bar(L::kBarPFull + i), 4 * 32);
       ptx::mbar_init(bar(L::kBarOFull + i), 1);
+      ptx::mbar_init(bar(L::kBarOEmpty + i), 4 * 32);
     }
 #pragma unroll
     for (int s = 0; s < L::kStages; ++s) {
@@ -217,24 +250,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
-    const int wg = warp >> 2;           // query tile 0 or 1 of the pair
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    const int wg = warp >> 2;           // query tile 0 or 1 of each unit
     const int rw = warp & 3;            // TMEM lane quarter this warp may access
     const int row = rw * 32 + lane;     // row of the tile == TMEM lane
-    const int n_blocks = nblk[wg];
-    if (n_blocks > 0) {
-      const int qt = q0 + wg * kBlockM;
+    const uint32_t lane_off = static_cast<uint32_t>(rw * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::col_s(wg);
+    const uint32_t t_o = tmem + lane_off + L::col_o(wg);
+    const float sl2 = p.scale_log2;
+    uint32_t s_base = 0;    // S_i tiles consumed in earlier units (s_full / p_full phase)
+    uint32_t o_count = 0;   // units finished by this warpgroup (o_full phase)
+    bool ok = true;
+    Unit u;
+    for (int r = 0; ok && unit_of(p, r, u); ++r) {
+      const int n_blocks = wg ? u.nblk[1] : u.nblk[0];
+      if (n_blocks == 0) continue;
+      const int bh = u.bh;
+      const int qt = u.q0 + wg * kBlockM;
       const int q = qt + row;
       const int key_lim = p.causal ? min(p.Lk, q + 1) : p.Lk;
       const int first_diag = p.causal ? qt / kBlockN : INT_MAX;
-      const uint32_t lane_off = static_cast<uint32_t>(rw * 32) << 16;
-      const uint32_t t_s = tmem + lane_off + L::col_s(wg);
-      const uint32_t t_o = tmem + lane_off + L::col_o(wg);
-      const float sl2 = p.scale_log2;
       float m = -INFINITY;   // running max of scaled scores, log2 units (possibly stale by < 8)
       float l = 0.0f;        // running sum of exp2(s*sl2 - m)
-      bool ok = true;
       for (int j = 0; j < n_blocks; ++j) {
-        ok = wait_phase(bar(L::kBarSFull + wg), j & 1, abort_flag, limit, kSiteSoftS);
+        ok = wait_phase(bar(L::kBarSFull + wg), (s_base + j) & 1, abort_flag, limit, kSiteSoftS);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
@@ -293,74 +332,91 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarPFull + wg));
       }
-      if (ok) {
-        ok = wait_phase(bar(L::kBarOFull + wg), 0, abort_flag, limit, kSiteSoftO);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        ptx::tc_fence_after();
-        const float inv_l = 1.0f / l;
-        const bool store = q < p.Lq;
-        __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + (store ? q : 0)) * HD;
+      if (!ok) break;
+      s_base += n_blocks;
+      ok = wait_phase(bar(L::kBarOFull + wg), o_count & 1, abort_flag, limit, kSiteSoftO);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ++o_count;
+      ptx::tc_fence_after();
+      // Epilogue: O / l as bf16 rows, LSE = ln2 * (m + log2 l); rows >= Lq are not stored.
+      const float inv_l = 1.0f / l;
+      const bool store = q < p.Lq;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + (store ? q : 0)) * HD;
 #pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-          uint32_t o[32];
-          ptx::tmem_ld32x32b_x32(t_o + c0, o);
-          uint32_t pk[16];
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t o[32];
+        ptx::tmem_ld32x32b_x32(t_o + c0, o);
+        uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                     __uint_as_float(o[2 * c + 1]) * inv_l);
-          if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
-        }
+        for (int c = 0; c < 16; ++c)
+          pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                   __uint_as_float(o[2 * c + 1]) * inv_l);
         if (store) {
-          p.lse[static_cast<size_t>(bh) * p.Lq + q] = (m + log2f(l)) * 0.69314718055994531f;
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
+      }
+      // O_i has been read into registers: the next unit's P_i V MMA may overwrite it.
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
+      if (store) {
+        p.lse[static_cast<size_t>(bh) * p.Lq + q] = (m + log2f(l)) * 0.69314718055994531f;
       }
     }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------------------ load warp
+    ptx::setmaxnreg_dec<kRegsOther>();
     if (lane == 0) {
       ptx::prefetch_tensormap(&p.tm_q);
       ptx::prefetch_tensormap(&p.tm_k);
       ptx::prefetch_tensormap(&p.tm_v);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (nblk[i] > 0) {
-          ptx::mbar_arrive_expect_tx(bar(L::kBarQFull + i), L::kTileBytes);
-#pragma unroll
-          for (int r = 0; r < L::kRegions; ++r)
-            ptx::tma_load_3d(sbase + L::kOffQ + i * L::kTileBytes + r * L::kRegionBytes, &p.tm_q,
-                             bar(L::kBarQFull + i), 64 * r, q0 + i * kBlockM, bh);
-        }
-      }
+      uint32_t q_count[2] = {0, 0};   // Q_i loads issued so far
+      uint32_t it = 0;                // K/V ring position (K_j and V_j alternate)
       int last_fill[L::kStages];
 #pragma unroll
       for (int s = 0; s < L::kStages; ++s) last_fill[s] = -1;
       bool ok = true;
-      for (int j = 0; j < nmax && ok; ++j) {
+      bool first = true;
+      Unit u;
+      for (int r = 0; ok && unit_of(p, r, u); ++r) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {   // t = 0: K_j, t = 1: V_j
-          const int it = 2 * j + t;
-          const int s = it % L::kStages;
-          const uint32_t ph = (it / L::kStages) & 1;
-          if (!wait_phase(bar(L::kBarKVEmpty + s), ph ^ 1u, abort_flag, limit, kSiteLoadKV)) {
+        for (int i = 0; i < 2; ++i) {
+          if (u.nblk[i] == 0) continue;
+          if (q_count[i] > 0 && !wait_phase(bar(L::kBarQEmpty + i), (q_count[i] - 1) & 1,
+                                            abort_flag, limit, kSiteLoadKV)) {
             ok = false;
             break;
           }
-          if ((p.flags & 1u) && j == 0 && t == 1) continue;   // test hook: withhold V_0
-          ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
+          ptx::mbar_arrive_expect_tx(bar(L::kBarQFull + i), L::kTileBytes);
 #pragma unroll
-          for (int r = 0; r < L::kRegions; ++r)
-            ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + r * L::kRegionBytes,
-                             t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * r, j * kBlockN, bh);
-          last_fill[s] = it;
+          for (int rg = 0; rg < L::kRegions; ++rg)
+            ptx::tma_load_3d(sbase + L::kOffQ + i * L::kTileBytes + rg * L::kRegionBytes, &p.tm_q,
+                             bar(L::kBarQFull + i), 64 * rg, u.q0 + i * kBlockM, u.bh);
+          ++q_count[i];
         }
+        for (int j = 0; j < u.nmax && ok; ++j) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t, ++it) {   // t = 0: K_j, t = 1: V_j
+            const int s = it % L::kStages;
+            const uint32_t ph = (it / L::kStages) & 1;
+            if (!wait_phase(bar(L::kBarKVEmpty + s), ph ^ 1u, abort_flag, limit, kSiteLoadKV)) {
+              ok = false;
+              break;
+            }
+            if ((p.flags & 1u) && first && j == 0 && t == 1) continue;   // test hook: withhold V_0
+            ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
+#pragma unroll
+            for (int rg = 0; rg < L::kRegions; ++rg)
+              ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + rg * L::kRegionBytes,
+                               t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * rg,
+                               j * kBlockN, u.bh);
+            last_fill[s] = static_cast<int>(it);
+          }
+        }
+        first = false;
       }
       // Drain: every copy this thread started has landed before the CTA may exit.
 #pragma unroll
@@ -369,11 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           drain_phase(bar(L::kBarKVFull + s), (last_fill[s] / L::kStages) & 1, limit);
 #pragma unroll
       for (int i = 0; i < 2; ++i)
-        if (nblk[i] > 0) drain_phase(bar(L::kBarQFull + i), 0, limit);
+        if (q_count[i] > 0) drain_phase(bar(L::kBarQFull + i), (q_count[i] - 1) & 1, limit);
     }
     __syncwarp();
-  } else {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA warp
+    ptx::setmaxnreg_dec<kRegsOther>();
     if (lane == 0) {   // one thread issues every MMA and commit
       constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false);
       constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true);
@@ -399,68 +456,97 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
+      uint32_t q_count[2] = {0, 0};   // units in which tile i was present (q_full / o_empty phase)
+      uint32_t p_base[2] = {0, 0};    // S_i tiles of earlier units (p_full phase)
+      uint32_t it_base = 0;           // K/V ring position of this unit's K_0
       bool ok = true;
+      Unit u;
+      for (int r = 0; ok && unit_of(p, r, u); ++r) {
+        const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
+        const int nblk[2] = {nb0, nb1};
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        if (ok && nblk[i] > 0)
-          ok = wait_phase(bar(L::kBarQFull + i), 0, abort_flag, limit, kSiteMmaQ);
-      if (ok && nmax > 0) ok = wait_phase(bar(L::kBarKVFull + 0), 0, abort_flag, limit, kSiteMmaK);
-      if (ok && nmax > 0) {
+        for (int i = 0; i < 2; ++i)
+          if (ok && nblk[i] > 0)
+            ok = wait_phase(bar(L::kBarQFull + i), q_count[i] & 1, abort_flag, limit, kSiteMmaQ);
+        const int slot_k0 = it_base % L::kStages;
+        if (ok) ok = wait_phase(bar(L::kBarKVFull + slot_k0), (it_base / L::kStages) & 1,
+                                abort_flag, limit, kSiteMmaK);
+        if (!ok) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (nblk[i] > 0) {
-            issue_s(i, 0);
+            issue_s(i, slot_k0);
             ptx::mma_commit(bar(L::kBarSFull + i));
+            if (nblk[i] == 1) ptx::mma_commit(bar(L::kBarQEmpty + i));
           }
         }
-        ptx::mma_commit(bar(L::kBarKVEmpty + 0));
-      }
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int it_v = 2 * j + 1;
-        const int slot_v = it_v % L::kStages;
-        if (!wait_phase(bar(L::kBarKVFull + slot_v), (it_v / L::kStages) & 1, abort_flag, limit,
-                        kSiteMmaV)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const int it_k = 2 * j + 2;
-        const int slot_k = it_k % L::kStages;
-        bool k_ready = false;
+        ptx::mma_commit(bar(L::kBarKVEmpty + slot_k0));
+        // The first P_i V MMA of a unit overwrites O_i: the previous unit's epilogue
+        // must have read it.
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (j >= nblk[i]) continue;
-          if (!wait_phase(bar(L::kBarPFull + i), j & 1, abort_flag, limit, kSiteMmaP)) {
+        for (int i = 0; i < 2; ++i)
+          if (ok && nblk[i] > 0 && q_count[i] > 0)
+            ok = wait_phase(bar(L::kBarOEmpty + i), (q_count[i] - 1) & 1, abort_flag, limit,
+                            kSiteMmaP);
+        for (int j = 0; j < nmax && ok; ++j) {
+          const uint32_t it_v = it_base + 2 * j + 1;
+          const int slot_v = it_v % L::kStages;
+          if (!wait_phase(bar(L::kBarKVFull + slot_v), (it_v / L::kStages) & 1, abort_flag, limit,
+                          kSiteMmaV)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          issue_pv(i, slot_v, j > 0);
-          if (j == nblk[i] - 1) ptx::mma_commit(bar(L::kBarOFull + i));
-          if (j + 1 < nblk[i]) {
-            if (!k_ready) {
-              if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
-                              limit, kSiteMmaK)) {
-                ok = false;
-                break;
-              }
-              ptx::tc_fence_after();
-              k_ready = true;
+          const uint32_t it_k = it_v + 1;
+          const int slot_k = it_k % L::kStages;
+          bool k_ready = false;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (j >= nblk[i]) continue;
+            if (!wait_phase(bar(L::kBarPFull + i), (p_base[i] + j) & 1, abort_flag, limit,
+                            kSiteMmaP)) {
+              ok = false;
+              break;
             }
-            issue_s(i, slot_k);
-            ptx::mma_commit(bar(L::kBarSFull + i));
+            ptx::tc_fence_after();
+            issue_pv(i, slot_v, j > 0);
+            if (j == nblk[i] - 1) {
+              ptx::mma_commit(bar(L::kBarOFull + i));
+              if (nblk[i] > 1) ptx::mma_commit(bar(L::kBarQEmpty + i));   // Q_i no longer read
+            }
+            if (j + 1 < nblk[i]) {
+              if (!k_ready) {
+                if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
+                                limit, kSiteMmaK)) {
+                  ok = false;
+                  break;
+                }
+                ptx::tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(i, slot_k);
+              ptx::mma_commit(bar(L::kBarSFull + i));
+            }
           }
+          if (!ok) break;
+          ptx::mma_commit(bar(L::kBarKVEmpty + slot_v));
+          if (k_ready) ptx::mma_commit(bar(L::kBarKVEmpty + slot_k));
         }
-        if (!ok) break;
-        ptx::mma_commit(bar(L::kBarKVEmpty + slot_v));
-        if (k_ready) ptx::mma_commit(bar(L::kBarKVEmpty + slot_k));
+        it_base += 2 * nmax;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          p_base[i] += nblk[i];
+          if (nblk[i] > 0) ++q_count[i];
+        }
       }
       // Drain: every MMA issued has completed before TMEM is freed.
       ptx::mma_commit(bar(L::kBarDrain));
       drain_phase(bar(L::kBarDrain), 0, limit);
     }
     __syncwarp();
+  } else {
+    ptx::setmaxnreg_dec<kRegsOther>();   // the two spare warps of the load/MMA warpgroup
   }
 
   ptx::tc_fence_before();
@@ -483,6 +569,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
+  int sm_count = 0;
   bool attr64 = false;
   bool attr128 = false;
 };
@@ -498,8 +585,24 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return na && nb && pa < pb + nb && pb < pa + na;
 }
 
+// Shared-memory opt-in for one kernel instance, and a check that the registers it
+// is launched with cover the warpgroups' register split (setmaxnreg.inc would
+// otherwise wait forever for registers that do not exist).
+fa_status configure_kernel(void (*kernel)(Params), int smem_bytes) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return FA_ERR_CUDA;
+  const long long launched = static_cast<long long>(attr.numRegs) * fa::kThreads;
+  const long long split = 256ll * fa::kRegsSoftmax + 128ll * fa::kRegsOther;
+  if (launched < split) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 // Per-device set-up: capability check, kernel attributes, encoder entry point.
-fa_status prepare_device(int dev, int D) {
+// On success *sm_count holds the device's number of SMs.
+fa_status prepare_device(int dev, int D, int* sm_count) {
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo& info = g_devices[dev];
@@ -508,10 +611,13 @@ fa_status prepare_device(int dev, int D) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
     info.supported = (major == 10 && minor == 3);
     info.ready = true;
   }
   if (!info.supported) return FA_ERR_UNSUPPORTED;
+  *sm_count = info.sm_count;
   if (!g_encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -522,15 +628,13 @@ fa_status prepare_device(int dev, int D) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if (D == 64 && !info.attr64) {
-    if (cudaFuncSetAttribute(fa::fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             fa::Layout<64>::kAlloc) != cudaSuccess)
-      return FA_ERR_CUDA;
+    const fa_status st = configure_kernel(fa::fa_fwd_kernel<64>, fa::Layout<64>::kAlloc);
+    if (st != FA_OK) return st;
     info.attr64 = true;
   }
   if (D == 128 && !info.attr128) {
-    if (cudaFuncSetAttribute(fa::fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             fa::Layout<128>::kAlloc) != cudaSuccess)
-      return FA_ERR_CUDA;
+    const fa_status st = configure_kernel(fa::fa_fwd_kernel<128>, fa::Layout<128>::kAlloc);
+    if (st != FA_OK) return st;
     info.attr128 = true;
   }
   return FA_OK;
@@ -579,7 +683,8 @@ extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  const fa_status prep = prepare_device(dev, D);
+  int sm_count = 0;
+  const fa_status prep = prepare_device(dev, D, &sm_count);
   if (prep != FA_OK) return prep;
 
   Params p;
@@ -593,15 +698,18 @@ extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O
   p.Lk = Lk;
   p.causal = causal ? 1 : 0;
   p.n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  if (bh > INT_MAX || static_cast<long long>(p.n_pairs) * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  p.n_units = static_cast<int>(p.n_pairs * bh);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.flags = g_debug_flags.load();
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitNs;
-  if (bh > INT_MAX || static_cast<long long>(p.n_pairs) * bh > INT_MAX) return FA_ERR_INVALID_ARG;
   if (p.flags & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n_pairs * bh));
+  // Persistent launch: one CTA per SM (shared memory allows no more), each
+  // walking its share of the units.
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.blockDim = dim3(fa::kThreads);
   cfg.stream = stream;
   cudaError_t err;
