@@ -150,6 +150,12 @@ def reduce_max(dist, value: float, device=None) -> float:
     return float(t.item())
 
 
+def aggregate_tflops(world: int, flops_per_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step` work;
+    the job took the slowest rank's time."""
+    return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
+
+
 def barrier(dist, device=None):
     if dist is not None:
         if device is not None and device.type == "cuda":
@@ -312,7 +318,7 @@ def run_ours(args, w):
         raise RuntimeError(f"timed region reported {fa.fa_status_string(st)}")
     max_ms = reduce_max(dist, total_ms, dev)
     flops = w.flops()
-    value = world * flops * args.steps / (max_ms / 1e3) / 1e12
+    value = aggregate_tflops(world, flops, args.steps, max_ms)
     ms_per_step = max_ms / args.steps
     kernel_tflops = flops / (statistics.mean(per_launch_ms) / 1e3) / 1e12
 
@@ -345,7 +351,7 @@ def run_ours(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
-        e2e = {"value": world * flops * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+        e2e = {"value": aggregate_tflops(world, flops, e2e_steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "ms_per_step": e2e_ms / e2e_steps}
 

@@ -203,3 +203,26 @@ def test_stream_argument():
     assert st == fa.FA_OK
     assert fa.fa_last_device_status(s) == fa.FA_OK
     assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,D,causal", [
+    (8, 64, 384, 384, 128, True),      # 1024 units: several rounds per CTA, absent tile 1 in every second unit
+    (1, 2, 32768, 32768, 128, True),   # long sequence: 256 key tiles for the last query tiles
+    (1, 4096, 1, 1, 64, False),        # thousands of one-row heads
+    (2, 300, 130, 70, 64, True),       # more units than CTAs, ragged query and key tails
+])
+def test_scheduler_shapes(oracle_mod, B, H, Lq, Lk, causal, D):
+    """Shapes that exercise the persistent unit schedule: many rounds per CTA,
+    very long rows, and many tiny units."""
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed=B * 7 + H + Lq)
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse = o.cpu(), lse.cpu()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    BH = B * H
+    rng = np.random.default_rng(B + H + Lq + Lk)
+    pairs = np.stack([rng.integers(0, BH, 160), rng.integers(0, Lq, 160)], axis=1)
+    edge = np.array([[0, 0], [BH - 1, Lq - 1], [BH // 2, Lq // 2], [BH - 1, 0], [0, Lq - 1]])
+    check_rows(oracle_mod, q, k, v, causal, 1.0 / math.sqrt(D), np.concatenate([pairs, edge]),
+               o, lse)
