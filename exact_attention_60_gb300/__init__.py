@@ -8,7 +8,8 @@ from __future__ import annotations
 import math
 
 from ._native import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
-                      FA_OK, fa_debug_set, fa_fwd, fa_last_device_status, fa_status_string)
+                      FA_OK, fa_debug_set, fa_fwd, fa_fwd_workspace_size, fa_fwd_ws,
+                      fa_last_device_status, fa_status_string)
 
 
 class FaError(RuntimeError):
@@ -17,11 +18,33 @@ class FaError(RuntimeError):
         self.status = status
 
 
+_workspaces = {}
+
+
+def workspace_for(B, H, Lq, Lk, D, causal, device):
+    """A cached device workspace large enough for fa_fwd_ws on this problem (or None)."""
+    import torch
+    st, nbytes = fa_fwd_workspace_size(B, H, Lq, Lk, D, causal)
+    if st != FA_OK:
+        raise FaError(st)
+    if nbytes == 0:
+        return None, 0
+    key = (torch.device(device).index, )
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws, ws.numel()
+
+
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-              stream=None):
+              stream=None, split: bool = True):
     """O, LSE = exact attention of contiguous bf16 CUDA tensors q [B,H,Lq,D], k/v [B,H,Lk,D].
 
-    Allocates ``out`` (bf16 [B,H,Lq,D]) and ``lse`` (fp32 [B,H,Lq]) if not given.
+    Allocates ``out`` (bf16 [B,H,Lq,D]) and ``lse`` (fp32 [B,H,Lq]) if not given.  With
+    ``split`` (default) it calls fa_fwd_ws with a cached workspace, so the library may
+    split key ranges across SMs; ``split=False`` calls fa_fwd.  Calls that share the
+    cached workspace (same device) must be ordered on one stream.
     """
     import torch
     B, H, Lq, D = q.shape
@@ -37,7 +60,11 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
-    st = fa_fwd(q, k, v, out, lse, B, H, Lq, Lk, D, causal, scale, stream)
+    if split:
+        ws, nbytes = workspace_for(B, H, Lq, Lk, D, causal, q.device)
+        st = fa_fwd_ws(q, k, v, out, lse, B, H, Lq, Lk, D, causal, scale, ws, nbytes, stream)
+    else:
+        st = fa_fwd(q, k, v, out, lse, B, H, Lq, Lk, D, causal, scale, stream)
     if st != FA_OK:
         raise FaError(st)
     return out, lse

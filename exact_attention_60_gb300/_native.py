@@ -18,7 +18,8 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 # Every symbol include/fa.h declares.
-EXPORTED = ("fa_fwd", "fa_status_string", "fa_last_device_status", "fa_debug_set")
+EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_status_string",
+            "fa_last_device_status", "fa_debug_set")
 
 _lib = None
 
@@ -36,6 +37,12 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
+    lib.fa_fwd_workspace_size.restype = ctypes.c_int
+    lib.fa_fwd_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_fwd_ws.restype = ctypes.c_int
+    lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp,
+                              ctypes.c_size_t, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_last_device_status.restype = ctypes.c_int
@@ -69,6 +76,22 @@ def fa_fwd(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, stream=None) -> int:
     return load().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
                          int(Lq), int(Lk), int(D), int(bool(causal)), float(scale),
                          _stream(stream))
+
+
+def fa_fwd_workspace_size(B, H, Lq, Lk, D, causal):
+    """C ``fa_fwd_workspace_size``: returns (status, bytes)."""
+    n = ctypes.c_size_t(0)
+    st = load().fa_fwd_workspace_size(int(B), int(H), int(Lq), int(Lk), int(D),
+                                      int(bool(causal)), ctypes.byref(n))
+    return st, int(n.value)
+
+
+def fa_fwd_ws(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, workspace, workspace_bytes,
+              stream=None) -> int:
+    """C ``fa_fwd_ws``; ``workspace`` may be an int, a tensor or None."""
+    return load().fa_fwd_ws(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
+                            int(Lq), int(Lk), int(D), int(bool(causal)), float(scale),
+                            _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_status_string(status: int) -> str:

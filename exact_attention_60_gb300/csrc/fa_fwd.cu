@@ -117,6 +117,11 @@ struct Params {
   int causal;
   int n_pairs;        // ceil(Lq / 256)
   int n_units;        // n_pairs * bh_count
+  int nkv;            // key tiles per unit: ceil(Lk / 128)
+  int split;          // 0: whole units, boustrophedon; 1: split key ranges (stream-K)
+  long long total_steps;   // n_units * nkv (split schedule)
+  float* ws_o;        // split schedule: partial O rows   [2 * grid][2 tiles][128 rows][D] fp32
+  float* ws_ml;       //                 partial (m, l)   [2 * grid][2 tiles][128 rows][2] fp32
   float scale_log2;   // scale * log2(e)
   uint32_t flags;     // test hooks (fa_debug_set)
   unsigned long long wait_limit_ns;
@@ -127,29 +132,75 @@ struct Params {
 // most keys); a CTA takes units in boustrophedon order over the grid (round r:
 // CTA g takes unit r*G + g when r is even, r*G + G-1-g when odd), which keeps
 // the per-CTA totals within a few percent of each other for causal loads.
+//
+// Split schedule (non-causal only, where every unit costs the same): the units'
+// key tiles form one sequence of n_units * nkv steps and CTA g takes the steps
+// [T*g/G, T*(g+1)/G).  A unit cut by a CTA boundary is processed in parts; each
+// part leaves its rows' partial state (unnormalised O, running max m, sum l) in
+// the workspace, and a second kernel on the same stream merges the parts of every
+// split unit into the final O and LSE.  No CTA ever waits for another.
 struct Unit {
   int bh;
   int q0;
-  int nblk[2];   // key tiles of query tile 0 and 1 (0 = tile absent)
+  int kv0;       // first key tile of this (part of a) unit
+  int nblk[2];   // key tiles of query tile 0 and 1 in this part (0 = tile absent)
   int nmax;
+  int partial;   // 1: a part of a unit split across CTAs
+  int slot;      // workspace slot of this part: 2 * CTA + (first part of the CTA ? 0 : 1)
 };
 
+__device__ __forceinline__ long long split_lo(const Params& p, int g) {
+  return p.total_steps * g / static_cast<int>(gridDim.x);
+}
+
+__device__ __forceinline__ void unit_rows(const Params& p, int idx, Unit& u) {
+  if (p.causal) {   // heaviest first: the last query tiles of every head come first
+    const int pair = p.n_pairs - 1 - idx / p.bh_count;
+    u.bh = idx % p.bh_count;
+    u.q0 = pair * 2 * kBlockM;
+  } else {          // equal costs: the units of one head are neighbours, so they run together
+    u.bh = idx / p.n_pairs;
+    u.q0 = (idx % p.n_pairs) * 2 * kBlockM;
+  }
+}
+
+template <bool kSplit>
 __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
   const int G = static_cast<int>(gridDim.x);
   const int g = static_cast<int>(blockIdx.x);
-  const int idx = r * G + ((r & 1) ? (G - 1 - g) : g);
-  if (idx >= p.n_units) return false;
-  const int pair = p.n_pairs - 1 - idx / p.bh_count;
-  u.bh = idx % p.bh_count;
-  u.q0 = pair * 2 * kBlockM;
-  const int nkv = (p.Lk + kBlockN - 1) / kBlockN;
+  if constexpr (!kSplit) {
+    const int idx = r * G + ((r & 1) ? (G - 1 - g) : g);
+    if (idx >= p.n_units) return false;
+    unit_rows(p, idx, u);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int qi = u.q0 + i * kBlockM;
-    u.nblk[i] = (qi >= p.Lq) ? 0 : (p.causal ? min(nkv, qi / kBlockN + 1) : nkv);
+    for (int i = 0; i < 2; ++i) {
+      const int qi = u.q0 + i * kBlockM;
+      u.nblk[i] = (qi >= p.Lq) ? 0 : (p.causal ? min(p.nkv, qi / kBlockN + 1) : p.nkv);
+    }
+    u.nmax = max(u.nblk[0], u.nblk[1]);
+    u.kv0 = 0;
+    u.partial = 0;
+    return true;
+  } else {
+  const long long lo = split_lo(p, g), hi = split_lo(p, g + 1);
+  long long x = lo;
+  for (int k = 0; k < r && x < hi; ++k) {   // skip the first r parts of this CTA's range
+    const long long end = (x / p.nkv + 1) * p.nkv;
+    x = min(end, hi);
   }
-  u.nmax = max(u.nblk[0], u.nblk[1]);
+  if (x >= hi) return false;
+  const int idx = static_cast<int>(x / p.nkv);
+  const int a = static_cast<int>(x - static_cast<long long>(idx) * p.nkv);
+  const int len = static_cast<int>(min(static_cast<long long>(p.nkv - a), hi - x));
+  unit_rows(p, idx, u);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) u.nblk[i] = (u.q0 + i * kBlockM >= p.Lq) ? 0 : len;
+  u.nmax = len;
+  u.kv0 = a;
+  u.partial = (len != p.nkv);
+  if (u.partial) u.slot = 2 * g + (x == lo ? 0 : 1);
   return true;
+  }
 }
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
@@ -205,7 +256,9 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned
   return true;
 }
 
-template <int HD>
+// kSplit selects the schedule at compile time, so the whole-unit kernel carries
+// none of the split schedule's code.
+template <int HD, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -262,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint32_t o_count = 0;   // units finished by this warpgroup (o_full phase)
     bool ok = true;
     Unit u;
-    for (int r = 0; ok && unit_of(p, r, u); ++r) {
+    for (int r = 0; ok && unit_of<kSplit>(p, r, u); ++r) {
       const int n_blocks = wg ? u.nblk[1] : u.nblk[0];
       if (n_blocks == 0) continue;
       const int bh = u.bh;
@@ -282,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j >= first_diag || (j + 1) * kBlockN > p.Lk) {
-          const int lim = key_lim - j * kBlockN;   // columns c < lim are allowed keys
+        const int jb = kSplit ? u.kv0 + j : j;   // key tile index
+        if (jb >= first_diag || (jb + 1) * kBlockN > p.Lk) {
+          const int lim = key_lim - jb * kBlockN;   // columns c < lim are allowed keys
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
         }
@@ -339,6 +393,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (!ok) break;
       ++o_count;
       ptx::tc_fence_after();
+      if (kSplit && u.partial) {
+        // A part of a split unit: park this row's state (unnormalised O, m, l) for
+        // the combine kernel that runs after this one.
+        const size_t rowi = static_cast<size_t>(u.slot * 2 + wg) * kBlockM + row;
+        float* so = p.ws_o + rowi * HD;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld32x32b_x32(t_o + c0, o);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(so + c0)[v] =
+                make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                            __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
+        p.ws_ml[rowi * 2] = m;
+        p.ws_ml[rowi * 2 + 1] = l;
+        continue;
+      }
       // Epilogue: O / l as bf16 rows, LSE = ln2 * (m + log2 l); rows >= Lq are not stored.
       const float inv_l = 1.0f / l;
       const bool store = q < p.Lq;
@@ -381,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       bool ok = true;
       bool first = true;
       Unit u;
-      for (int r = 0; ok && unit_of(p, r, u); ++r) {
+      for (int r = 0; ok && unit_of<kSplit>(p, r, u); ++r) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (u.nblk[i] == 0) continue;
@@ -412,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int rg = 0; rg < L::kRegions; ++rg)
               ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + rg * L::kRegionBytes,
                                t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * rg,
-                               j * kBlockN, u.bh);
+                               (kSplit ? u.kv0 + j : j) * kBlockN, u.bh);
             last_fill[s] = static_cast<int>(it);
           }
         }
@@ -461,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       uint32_t it_base = 0;           // K/V ring position of this unit's K_0
       bool ok = true;
       Unit u;
-      for (int r = 0; ok && unit_of(p, r, u); ++r) {
+      for (int r = 0; ok && unit_of<kSplit>(p, r, u); ++r) {
         const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
         const int nblk[2] = {nb0, nb1};
 #pragma unroll
@@ -557,6 +632,110 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   }
 }
 
+// Parameters of the combine kernel that finishes split units (split schedule).
+struct CombineParams {
+  const float* ws_o;
+  const float* ws_ml;
+  __nv_bfloat16* o;
+  float* lse;
+  long long total_steps;
+  int grid;          // CTAs of the attention kernel that made the parts
+  int nkv;
+  int n_pairs;
+  int bh_count;
+  int Lq;
+};
+
+// One CTA per (CTA boundary of the attention kernel, query tile, group of 16
+// rows).  The boundary that is the first one inside a unit finishes that unit:
+// for each row it merges the unit's parts k in one pass, the same update the
+// online softmax applies per key tile:
+//   m' = max(m, m_k),  l' = l 2^(m - m') + l_k 2^(m_k - m'),
+//   O' = O 2^(m - m') + O_k 2^(m_k - m'),
+// and writes O = O'/l' and LSE = ln2 (m' + log2 l').  Each warp merges 4 rows,
+// interleaved so their loads overlap; its lanes cover the D columns.
+constexpr int kCombineRowsPerWarp = 4;
+constexpr int kCombineRows = 4 * kCombineRowsPerWarp;   // rows per CTA (4 warps)
+constexpr int kCombineMaxParts = 256;                   // parts come from distinct CTAs
+
+template <int HD>
+__global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__ CombineParams c) {
+  __shared__ int s_slot[kCombineMaxParts];
+  __shared__ int s_nparts, s_bh, s_q0;
+  const int b = blockIdx.x + 1;   // boundary between CTA b-1 and CTA b
+  const int tile = blockIdx.y;
+  if (threadIdx.x == 0) {
+    const long long G = c.grid;
+    auto lo = [&](long long g) { return c.total_steps * g / G; };
+    const long long xb = lo(b);
+    const long long u = xb / c.nkv;
+    const long long step0 = u * c.nkv;
+    int n = 0;
+    // nothing to do on a boundary between units, or if an earlier boundary lies in u
+    if (xb != step0 && !(b >= 2 && lo(b - 1) > step0)) {
+      for (long long g = b - 1; g < G && lo(g) <= step0 + c.nkv - 1 && n < kCombineMaxParts; ++g)
+        s_slot[n++] = static_cast<int>(2 * g + (lo(g) >= step0 ? 0 : 1));
+    }
+    s_nparts = n;
+    s_bh = static_cast<int>(u / c.n_pairs);   // non-causal order: a head's pairs are neighbours
+    s_q0 = static_cast<int>(u % c.n_pairs) * 2 * kBlockM + tile * kBlockM;
+  }
+  __syncthreads();
+  const int nparts = s_nparts;
+  if (nparts == 0 || s_q0 >= c.Lq) return;
+  constexpr int kPerLane = HD / 32;   // 4 (D = 128) or 2 (D = 64) columns per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.z * kCombineRows + warp * kCombineRowsPerWarp;
+  float m[kCombineRowsPerWarp], l[kCombineRowsPerWarp], acc[kCombineRowsPerWarp][kPerLane];
+#pragma unroll
+  for (int rr = 0; rr < kCombineRowsPerWarp; ++rr) {
+    m[rr] = -INFINITY;
+    l[rr] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kPerLane; ++e) acc[rr][e] = 0.0f;
+  }
+  for (int k = 0; k < nparts; ++k) {
+    const size_t base = static_cast<size_t>(s_slot[k] * 2 + tile) * kBlockM + r0;
+#pragma unroll
+    for (int rr = 0; rr < kCombineRowsPerWarp; ++rr) {
+      const size_t row = base + rr;
+      const float2 ml = __ldg(reinterpret_cast<const float2*>(c.ws_ml) + row);
+      const float* src = c.ws_o + row * HD + lane * kPerLane;
+      float x[kPerLane];
+      if constexpr (kPerLane == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+      } else {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+        x[0] = v.x; x[1] = v.y;
+      }
+      const float m_new = fmaxf(m[rr], ml.x);
+      const float a = ptx::ex2_approx(m[rr] - m_new);   // 0 on the first part (m = -inf)
+      const float w = ptx::ex2_approx(ml.x - m_new);
+      l[rr] = l[rr] * a + ml.y * w;
+#pragma unroll
+      for (int e = 0; e < kPerLane; ++e) acc[rr][e] = acc[rr][e] * a + x[e] * w;
+      m[rr] = m_new;
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < kCombineRowsPerWarp; ++rr) {
+    const int q = s_q0 + r0 + rr;
+    if (q >= c.Lq) continue;
+    const float inv_l = 1.0f / l[rr];
+    __nv_bfloat16* dst = c.o + (static_cast<size_t>(s_bh) * c.Lq + q) * HD + lane * kPerLane;
+    if constexpr (kPerLane == 4) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(ptx::pack_bf16x2(acc[rr][0] * inv_l, acc[rr][1] * inv_l),
+                     ptx::pack_bf16x2(acc[rr][2] * inv_l, acc[rr][3] * inv_l));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = ptx::pack_bf16x2(acc[rr][0] * inv_l, acc[rr][1] * inv_l);
+    }
+    if (lane == 0)
+      c.lse[static_cast<size_t>(s_bh) * c.Lq + q] = (m[rr] + log2f(l[rr])) * 0.69314718055994531f;
+  }
+}
+
 }  // namespace fa
 
 // ============================================================================ host side
@@ -570,8 +749,7 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
-  bool attr64 = false;
-  bool attr128 = false;
+  bool attr[2][2] = {{false, false}, {false, false}};   // [D == 128][split]
 };
 
 std::mutex g_mutex;
@@ -588,7 +766,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // Shared-memory opt-in for one kernel instance, and a check that the registers it
 // is launched with cover the warpgroups' register split (setmaxnreg.inc would
 // otherwise wait forever for registers that do not exist).
-fa_status configure_kernel(void (*kernel)(Params), int smem_bytes) {
+fa_status configure_kernel(void (*kernel)(const Params), int smem_bytes) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
       cudaSuccess)
     return FA_ERR_CUDA;
@@ -627,15 +805,18 @@ fa_status prepare_device(int dev, int D, int* sm_count) {
       return FA_ERR_CUDA;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  if (D == 64 && !info.attr64) {
-    const fa_status st = configure_kernel(fa::fa_fwd_kernel<64>, fa::Layout<64>::kAlloc);
+  const int di = (D == 128) ? 1 : 0;
+  for (int sp = 0; sp < 2; ++sp) {
+    if (info.attr[di][sp]) continue;
+    fa_status st;
+    if (D == 64)
+      st = sp ? configure_kernel(fa::fa_fwd_kernel<64, true>, fa::Layout<64>::kAlloc)
+              : configure_kernel(fa::fa_fwd_kernel<64, false>, fa::Layout<64>::kAlloc);
+    else
+      st = sp ? configure_kernel(fa::fa_fwd_kernel<128, true>, fa::Layout<128>::kAlloc)
+              : configure_kernel(fa::fa_fwd_kernel<128, false>, fa::Layout<128>::kAlloc);
     if (st != FA_OK) return st;
-    info.attr64 = true;
-  }
-  if (D == 128 && !info.attr128) {
-    const fa_status st = configure_kernel(fa::fa_fwd_kernel<128>, fa::Layout<128>::kAlloc);
-    if (st != FA_OK) return st;
-    info.attr128 = true;
+    info.attr[di][sp] = true;
   }
   return FA_OK;
 }
@@ -656,14 +837,35 @@ bool encode_map(CUtensorMap* map, const void* base, long long BH, long long L, i
 
 }  // namespace
 
-extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                            int B, int H, int Lq, int Lk, int D, int causal, float scale,
-                            cudaStream_t stream) {
+namespace {
+
+// A validated problem (argument checks shared by every entry point).
+struct Problem {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  float* LSE;
+  int Lq, Lk, D, causal;
+  float scale;
+  long long bh;
+  int n_pairs, n_units, nkv;
+  size_t bytes_q, bytes_k, bytes_lse;
+};
+
+// FA_OK with *empty = true means there is nothing to compute (no launch).
+fa_status check_problem(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                        int H, int Lq, int Lk, int D, int causal, float scale, Problem* pr,
+                        bool* empty) {
+  *empty = false;
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long rows_q = bh * Lq;
-  if (rows_q == 0) return FA_OK;
+  if (rows_q == 0) {
+    *empty = true;
+    return FA_OK;
+  }
   if (Lk < 1) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
@@ -680,47 +882,194 @@ extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O
       overlaps(LSE, bytes_lse, Q, bytes_q) || overlaps(LSE, bytes_lse, K, bytes_k) ||
       overlaps(LSE, bytes_lse, V, bytes_k))
     return FA_ERR_INVALID_ARG;
+  const long long n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  if (bh > INT_MAX || n_pairs * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  *pr = Problem{Q, K, V, O, LSE, Lq, Lk, D, causal ? 1 : 0, scale, bh,
+                static_cast<int>(n_pairs), static_cast<int>(n_pairs * bh),
+                (Lk + fa::kBlockN - 1) / fa::kBlockN, bytes_q, bytes_k, bytes_lse};
+  return FA_OK;
+}
 
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  int sm_count = 0;
-  const fa_status prep = prepare_device(dev, D, &sm_count);
-  if (prep != FA_OK) return prep;
+// Schedule choice.  Causal units have different costs and are balanced by the
+// heaviest-first boustrophedon order.  Non-causal units all cost the same; when
+// whole units would keep at most half of the SM-rounds busy (a quarter for D = 64,
+// whose parts are cheaper to compute and so relatively dearer to merge) and a unit
+// has at least two key tiles, the key ranges are split across CTAs (needs a
+// workspace).  The thresholds come from measurements: splitting paid 3.1-3.6x at
+// 21 % fill and 61 % at 42 % fill (D = 128), and lost 9-36 % at 84 % fill.
+struct Plan {
+  bool split;
+  int grid;
+  size_t off_ml, ws_bytes;
+};
 
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Plan plan_schedule(const Problem& pr, int sm_count) {
+  Plan pl{};
+  const long long rounds = (pr.n_units + sm_count - 1) / sm_count;
+  const double fill = static_cast<double>(pr.n_units) / (static_cast<double>(rounds) * sm_count);
+  pl.split = !pr.causal && pr.nkv >= 2 && fill <= (pr.D == 128 ? 0.5 : 0.25);
+  if (!pl.split) {
+    pl.grid = std::min(pr.n_units, sm_count);
+    return pl;
+  }
+  const long long steps = static_cast<long long>(pr.n_units) * pr.nkv;
+  pl.grid = static_cast<int>(std::min<long long>(steps, sm_count));
+  const size_t rows = static_cast<size_t>(pl.grid) * 2 * 2 * fa::kBlockM;   // 2 slots x 2 tiles
+  pl.off_ml = round256(rows * pr.D * sizeof(float));
+  pl.ws_bytes = pl.off_ml + round256(rows * 2 * sizeof(float));
+  return pl;
+}
+
+fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cudaStream_t stream) {
   Params p;
-  if (!encode_map(&p.tm_q, Q, bh, Lq, D) || !encode_map(&p.tm_k, K, bh, Lk, D) ||
-      !encode_map(&p.tm_v, V, bh, Lk, D))
+  if (!encode_map(&p.tm_q, pr.Q, pr.bh, pr.Lq, pr.D) ||
+      !encode_map(&p.tm_k, pr.K, pr.bh, pr.Lk, pr.D) ||
+      !encode_map(&p.tm_v, pr.V, pr.bh, pr.Lk, pr.D))
     return FA_ERR_CUDA;
-  p.o = static_cast<__nv_bfloat16*>(O);
-  p.lse = LSE;
-  p.bh_count = static_cast<int>(bh);
-  p.Lq = Lq;
-  p.Lk = Lk;
-  p.causal = causal ? 1 : 0;
-  p.n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-  if (bh > INT_MAX || static_cast<long long>(p.n_pairs) * bh > INT_MAX) return FA_ERR_INVALID_ARG;
-  p.n_units = static_cast<int>(p.n_pairs * bh);
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.o = static_cast<__nv_bfloat16*>(pr.O);
+  p.lse = pr.LSE;
+  p.bh_count = static_cast<int>(pr.bh);
+  p.Lq = pr.Lq;
+  p.Lk = pr.Lk;
+  p.causal = pr.causal;
+  p.n_pairs = pr.n_pairs;
+  p.n_units = pr.n_units;
+  p.nkv = pr.nkv;
+  p.split = pl.split ? 1 : 0;
+  p.total_steps = static_cast<long long>(pr.n_units) * pr.nkv;
+  p.ws_o = nullptr;
+  p.ws_ml = nullptr;
+  if (pl.split) {
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    p.ws_o = reinterpret_cast<float*>(base);
+    p.ws_ml = reinterpret_cast<float*>(base + pl.off_ml);
+  }
+  p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.flags = g_debug_flags.load();
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitNs;
   if (p.flags & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
+  (void)sm_count;
 
   cudaLaunchConfig_t cfg = {};
   // Persistent launch: one CTA per SM (shared memory allows no more), each
-  // walking its share of the units.
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
+  // walking its share of the work.
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
   cfg.blockDim = dim3(fa::kThreads);
   cfg.stream = stream;
   cudaError_t err;
-  if (D == 64) {
+  if (pr.D == 64) {
     cfg.dynamicSmemBytes = fa::Layout<64>::kAlloc;
-    err = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<64>, p);
+    err = pl.split ? cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<64, true>, p)
+                   : cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<64, false>, p);
   } else {
     cfg.dynamicSmemBytes = fa::Layout<128>::kAlloc;
-    err = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<128>, p);
+    err = pl.split ? cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<128, true>, p)
+                   : cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<128, false>, p);
   }
-  return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (err != cudaSuccess) return FA_ERR_CUDA;
+  if (pl.split && pl.grid > 1) {
+    // Merge the parts of every split unit (same stream: runs after the parts exist).
+    fa::CombineParams c;
+    c.ws_o = p.ws_o;
+    c.ws_ml = p.ws_ml;
+    c.o = p.o;
+    c.lse = p.lse;
+    c.total_steps = p.total_steps;
+    c.grid = pl.grid;
+    c.nkv = pr.nkv;
+    c.n_pairs = pr.n_pairs;
+    c.bh_count = static_cast<int>(pr.bh);
+    c.Lq = pr.Lq;
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(static_cast<unsigned>(pl.grid - 1), 2, fa::kBlockM / fa::kCombineRows);
+    cc.blockDim = dim3(128);
+    cc.stream = stream;
+    err = (pr.D == 64) ? cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<64>, c)
+                       : cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<128>, c);
+    if (err != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+fa_status current_device(int D, int* sm_count) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  return prepare_device(dev, D, sm_count);
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int B, int H, int Lq, int Lk, int D, int causal, float scale,
+                            cudaStream_t stream) {
+  Problem pr;
+  bool empty = false;
+  const fa_status st = check_problem(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, &pr, &empty);
+  if (st != FA_OK || empty) return st;
+  int sm_count = 0;
+  const fa_status prep = current_device(D, &sm_count);
+  if (prep != FA_OK) return prep;
+  Plan pl = plan_schedule(pr, sm_count);
+  if (pl.split) {   // no workspace here: whole units only
+    pl.split = false;
+    pl.grid = std::min(pr.n_units, sm_count);
+  }
+  return launch(pr, sm_count, pl, nullptr, stream);
+}
+
+extern "C" fa_status fa_fwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
+                                           size_t* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * Lq == 0) return FA_OK;
+  if (Lk < 1) return FA_ERR_INVALID_ARG;
+  const long long n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  if (bh > INT_MAX || n_pairs * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  int sm_count = 0;
+  const fa_status prep = current_device(D, &sm_count);
+  if (prep != FA_OK) return prep;
+  Problem pr{};
+  pr.Lq = Lq;
+  pr.Lk = Lk;
+  pr.D = D;
+  pr.causal = causal ? 1 : 0;
+  pr.bh = bh;
+  pr.n_pairs = static_cast<int>(n_pairs);
+  pr.n_units = static_cast<int>(n_pairs * bh);
+  pr.nkv = (Lk + fa::kBlockN - 1) / fa::kBlockN;
+  const Plan pl = plan_schedule(pr, sm_count);
+  *bytes = pl.split ? pl.ws_bytes : 0;
+  return FA_OK;
+}
+
+extern "C" fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int Lq, int Lk, int D, int causal, float scale,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Problem pr;
+  bool empty = false;
+  const fa_status st = check_problem(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, &pr, &empty);
+  if (st != FA_OK || empty) return st;
+  int sm_count = 0;
+  const fa_status prep = current_device(D, &sm_count);
+  if (prep != FA_OK) return prep;
+  const Plan pl = plan_schedule(pr, sm_count);
+  if (pl.split) {
+    if (!workspace || workspace_bytes < pl.ws_bytes) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID_ARG;
+    if (overlaps(workspace, pl.ws_bytes, Q, pr.bytes_q) ||
+        overlaps(workspace, pl.ws_bytes, K, pr.bytes_k) ||
+        overlaps(workspace, pl.ws_bytes, V, pr.bytes_k) ||
+        overlaps(workspace, pl.ws_bytes, O, pr.bytes_q) ||
+        overlaps(workspace, pl.ws_bytes, LSE, pr.bytes_lse))
+      return FA_ERR_INVALID_ARG;
+  }
+  return launch(pr, sm_count, pl, workspace, stream);
 }
 
 extern "C" const char* fa_status_string(fa_status s) {

@@ -78,6 +78,43 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
                  int B, int H, int Lq, int Lk, int D, int causal, float scale,
                  cudaStream_t stream);
 
+/*
+ * fa_fwd_workspace_size -- device workspace that fa_fwd_ws needs for this problem
+ * on the current device, in *bytes (0: none).
+ *
+ * Same operation as fa_fwd, scheduled differently when few query tiles face long
+ * key ranges.  Work is handed out in units of two 128-row query tiles of one head.
+ * Causal units differ in cost and are balanced by ordering them heaviest first.
+ * Non-causal units all cost the same; when whole units would keep at most half of
+ * the SMs busy per round (a quarter for D = 64) and each unit has at least two
+ * 128-key tiles, the key range of each unit is cut into consecutive pieces (the
+ * FA-2 post's loop over K/V blocks, split between CTAs so every SM gets the same
+ * number of key tiles).  Each piece leaves its rows' partial online-softmax state
+ * (unnormalised O, running max m, exp-sum l -- the three per-row quantities of the
+ * post's online-softmax section) in the workspace, and a second kernel on the same
+ * stream merges them per row with the online-softmax update:
+ *   m = max_k m_k,  O = sum_k 2^(m_k - m) O_k / sum_k 2^(m_k - m) l_k.
+ * The workspace holds 2 x grid x 2 x 128 rows of (D + 2) floats (about 40 MB for
+ * D = 128 on 152 SMs).
+ * Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED for arguments fa_fwd rejects on
+ * sizes alone (and for bytes == NULL), FA_ERR_CUDA if the device cannot be queried.
+ */
+fa_status fa_fwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal, size_t* bytes);
+
+/*
+ * fa_fwd_ws -- fa_fwd with a caller-owned device workspace, which lets the
+ * library use the split-key schedule above.  `workspace` must be 256-byte
+ * aligned, hold at least the size fa_fwd_workspace_size reports and overlap no
+ * other argument; it may be NULL when that size is 0.  Its contents on entry do
+ * not matter; after the call it holds scratch.  Two calls that share a workspace
+ * must not run concurrently.  When the split schedule is used, two kernels are
+ * queued on `stream`.  Otherwise identical to fa_fwd (arguments, errors, results
+ * up to the summation order of the merged rows).
+ */
+fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    int B, int H, int Lq, int Lk, int D, int causal, float scale,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -106,3 +106,22 @@ def test_missing_library_fails_loudly(tmp_path):
             _native.load(missing)
     finally:
         _native._lib = saved
+
+
+def test_workspace_size_rejects_bad_arguments(lib):
+    assert fa.fa_fwd_workspace_size(1, 1, 16, 16, 96, 0)[0] == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_workspace_size(-1, 1, 16, 16, 64, 0)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_workspace_size(1, 1, 16, 0, 64, 0)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_workspace_size(0, 1, 16, 16, 64, 0) == (fa.FA_OK, 0)
+    assert lib.fa_fwd_workspace_size(1, 1, 16, 16, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,expect", [(dict(D=96), fa.FA_ERR_UNSUPPORTED), (dict(Lk=0), fa.FA_ERR_INVALID_ARG),
+                                       (dict(Q=0), fa.FA_ERR_INVALID_ARG), (dict(scale=0.0), fa.FA_ERR_INVALID_ARG)])
+def test_fwd_ws_rejects_bad_arguments_before_any_cuda_call(lib, kw, expect):
+    args = dict(Q=ALIGNED, K=2 * ALIGNED, V=3 * ALIGNED, O=4 * ALIGNED, LSE=5 * ALIGNED, B=1, H=1,
+                Lq=16, Lk=16, D=64, causal=0, scale=0.125)
+    args.update(kw)
+    assert fa.fa_fwd_ws(args["Q"], args["K"], args["V"], args["O"], args["LSE"], args["B"],
+                        args["H"], args["Lq"], args["Lk"], args["D"], args["causal"],
+                        args["scale"], None, 0, 0) == expect

@@ -194,7 +194,7 @@ def test_stream_argument():
     """fa_fwd runs on the stream it is given."""
     dev = torch.device("cuda:0")
     q, k, v = (t.to(dev) for t in make_qkv(1, 2, 256, 256, 64, seed=13))
-    ref_o, ref_l = fa.attention(q, k, v)
+    ref_o, ref_l = fa.attention(q, k, v, split=False)
     s = torch.cuda.Stream()
     o = torch.empty_like(q)
     lse = torch.empty(1, 2, 256, device=dev)
@@ -226,3 +226,60 @@ def test_scheduler_shapes(oracle_mod, B, H, Lq, Lk, causal, D):
     edge = np.array([[0, 0], [BH - 1, Lq - 1], [BH // 2, Lq // 2], [BH - 1, 0], [0, Lq - 1]])
     check_rows(oracle_mod, q, k, v, causal, 1.0 / math.sqrt(D), np.concatenate([pairs, edge]),
                o, lse)
+
+
+# non-causal shapes with few units (query-tile pairs) per SM: the split-key schedule
+SPLIT_SHAPES = [(1, 4, 2048, 32768, 128), (1, 8, 2048, 16384, 128), (1, 4, 2048, 32768, 64),
+                (1, 2, 256, 256, 64), (3, 5, 700, 1300, 128), (1, 1, 128, 40000, 128),
+                (2, 3, 500, 8191, 64)]
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,D", SPLIT_SHAPES)
+def test_split_schedule_matches(oracle_mod, B, H, Lq, Lk, D):
+    """Non-causal shapes that take the split-key schedule: the merged result agrees
+    with the whole-unit schedule (fa_fwd) and with the oracle on sampled rows."""
+    st, nbytes = fa.fa_fwd_workspace_size(B, H, Lq, Lk, D, False)
+    assert st == fa.FA_OK and nbytes > 0
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed=B + H + Lq + Lk, sigma_qk=2.0)
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o1, l1 = fa.attention(qd, kd, vd, split=False)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev)   # arbitrary contents
+    o2 = torch.empty_like(qd)
+    l2 = torch.empty(B, H, Lq, device=dev)
+    for _ in range(2):   # the workspace is reused as left by the previous call
+        st = fa.fa_fwd_ws(qd, kd, vd, o2, l2, B, H, Lq, Lk, D, 0, 1.0 / math.sqrt(D), ws, nbytes)
+        assert st == fa.FA_OK
+        assert fa.fa_last_device_status() == fa.FA_OK
+        assert (o2.float() - o1.float()).abs().max().item() <= TOL_O
+        assert (l2 - l1).abs().max().item() <= TOL_LSE
+    rng = np.random.default_rng(Lk)
+    pairs = np.stack([rng.integers(0, B * H, 64), rng.integers(0, Lq, 64)], axis=1)
+    pairs = np.concatenate([pairs, [[0, 0], [B * H - 1, Lq - 1]]])
+    check_rows(oracle_mod, q, k, v, False, 1.0 / math.sqrt(D), pairs, o2.cpu(), l2.cpu())
+
+
+def test_no_split_for_causal_or_full_rounds():
+    assert fa.fa_fwd_workspace_size(2, 32, 4096, 4096, 128, True) == (fa.FA_OK, 0)
+    assert fa.fa_fwd_workspace_size(1, 16, 16384, 16384, 128, True) == (fa.FA_OK, 0)
+    assert fa.fa_fwd_workspace_size(1, 2, 128, 128, 64, False) == (fa.FA_OK, 0)   # one key tile
+    assert fa.fa_fwd_workspace_size(8, 16, 500, 8191, 128, False) == (fa.FA_OK, 0)  # 84 % fill
+    assert fa.fa_fwd_workspace_size(0, 2, 128, 512, 64, False) == (fa.FA_OK, 0)   # empty
+
+
+def test_workspace_argument_errors():
+    dev = torch.device("cuda:0")
+    B, H, Lq, Lk, D = 2, 4, 300, 1000, 128
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, Lq, Lk, D, seed=31))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Lq, device=dev)
+    st, nbytes = fa.fa_fwd_workspace_size(B, H, Lq, Lk, D, False)
+    assert st == fa.FA_OK and nbytes > 0
+    ws = torch.empty(nbytes + 512, dtype=torch.uint8, device=dev)
+    call = lambda w, n: fa.fa_fwd_ws(q, k, v, o, lse, B, H, Lq, Lk, D, 0, 0.1, w, n)
+    assert call(None, 0) == fa.FA_ERR_INVALID_ARG                   # needed but missing
+    assert call(ws, nbytes - 1) == fa.FA_ERR_INVALID_ARG            # too small
+    assert call(ws.data_ptr() + 16, nbytes) == fa.FA_ERR_INVALID_ARG   # not 256-aligned
+    assert call(o.data_ptr(), nbytes) == fa.FA_ERR_INVALID_ARG      # overlaps O
+    assert call(ws, nbytes) == fa.FA_OK
+    assert fa.fa_last_device_status() == fa.FA_OK
