@@ -8,8 +8,8 @@ from __future__ import annotations
 import math
 
 from ._native import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
-                      FA_OK, fa_debug_set, fa_fwd, fa_fwd_workspace_size, fa_fwd_ws,
-                      fa_last_device_status, fa_status_string)
+                      FA_OK, fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_workspace_size,
+                      fa_fwd_ws, fa_last_device_status, fa_status_string)
 
 
 class FaError(RuntimeError):

@@ -1072,6 +1072,55 @@ extern "C" fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void
   return launch(pr, sm_count, pl, workspace, stream);
 }
 
+// ---------------------------------------------------------------- no-allocation entry point
+// Scratch for fa_fwd_noalloc: the split schedule's workspace, held in device
+// memory that the CUDA runtime reserves when this library's module is loaded on a
+// GPU, so the call itself never allocates.  42 MiB covers the split schedule at
+// D = 128 on up to 165 SMs (GB300 has 152) and at D = 64 on up to 326 SMs.
+constexpr size_t kNoAllocScratchBytes = 42ull << 20;
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_fa_noalloc_scratch on device `dev` (which must be current).
+// The name g_fa_noalloc_scratch in host code only stands in for the symbol; the
+// address comes from cudaGetSymbolAddress, once per device.
+fa_status scratch_address(int dev, void** addr) {
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_fa_noalloc_scratch) != cudaSuccess || !a) return FA_ERR_CUDA;
+    g_scratch_addr[dev] = a;
+  }
+  *addr = g_scratch_addr[dev];
+  return FA_OK;
+}
+}  // namespace
+
+extern "C" fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O,
+                                    float* LSE, int B, int H, int Lq, int Lk, int D, int causal,
+                                    float scale, cudaStream_t stream) {
+  Problem pr;
+  bool empty = false;
+  const fa_status st = check_problem(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, &pr, &empty);
+  if (st != FA_OK || empty) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int sm_count = 0;
+  const fa_status prep = prepare_device(dev, D, &sm_count);
+  if (prep != FA_OK) return prep;
+  const Plan pl = plan_schedule(pr, sm_count);
+  if (!pl.split) return launch(pr, sm_count, pl, nullptr, stream);
+  if (pl.ws_bytes > kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const fa_status sa = scratch_address(dev, &scratch);
+  if (sa != FA_OK) return sa;
+  return launch(pr, sm_count, pl, scratch, stream);
+}
+
 extern "C" const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK";

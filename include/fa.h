@@ -115,6 +115,33 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
                     int B, int H, int Lq, int Lk, int D, int causal, float scale,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * fa_fwd_noalloc -- fa_fwd_ws without a workspace argument, for callers that
+ * cannot allocate device memory: code that only receives the input and output
+ * pointers through a fixed interface with no allocator to ask, and code that
+ * must not call cudaMalloc on its hot path because the call can synchronize the
+ * device and take unbounded time.  The pages have no counterpart; this is a
+ * packaging of the same computation.
+ *
+ * The split schedule's workspace lives in a 42 MiB device array inside this
+ * library, reserved on every GPU that loads the library and held until the
+ * process exits.  That covers the split schedule at D = 128 on GPUs with up to
+ * 165 SMs (D = 64: 326 SMs); on larger GPUs a problem that would need more
+ * returns FA_ERR_UNSUPPORTED before anything is launched.  Problems that run on
+ * whole units (all causal ones, and non-causal ones that keep the SMs busy) use
+ * no scratch at all.  Nothing is allocated by the call itself.
+ *
+ * The first call on each device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.  Every
+ * call shares the one array and leaves scratch in it (it needs no clearing):
+ * calls whose kernels can overlap on the GPU -- on different streams, or from
+ * different host threads -- race on it and must be ordered by the caller.
+ * Arguments, errors and results are otherwise those of fa_fwd_ws.
+ */
+fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         int B, int H, int Lq, int Lk, int D, int causal, float scale,
+                         cudaStream_t stream);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(fa_status s);
 
