@@ -68,3 +68,73 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     if st != FA_OK:
         raise FaError(st)
     return out, lse
+
+
+def attention_from_host(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                        lse=None, chunks: int | None = None, device=None):
+    """Exact attention of host tensors: copies in, computes, copies out, overlapped.
+
+    ``q`` [B,H,Lq,D], ``k``/``v`` [B,H,Lk,D] are contiguous bf16 CPU tensors (pinned for
+    the copies to overlap).  The (batch, head) slices are cut into ``chunks`` groups;
+    group i+1 travels to the GPU while group i is computed and group i-1 travels back,
+    on three streams ordered by events.  Returns host ``out`` (bf16) and ``lse`` (fp32),
+    allocated pinned if not given.  Device buffers are allocated per call.
+    """
+    import torch
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    BH = B * H
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32).pin_memory()
+    if chunks is None:
+        chunks = default_chunks(BH, Lq, Lk, causal)
+    chunks = max(1, min(int(chunks), BH))
+    dq = torch.empty((BH, Lq, D), dtype=torch.bfloat16, device=dev)
+    dk = torch.empty((BH, Lk, D), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty((BH, Lk, D), dtype=torch.bfloat16, device=dev)
+    do = torch.empty((BH, Lq, D), dtype=torch.bfloat16, device=dev)
+    dl = torch.empty((BH, Lq), dtype=torch.float32, device=dev)
+    hq, hk, hv = q.reshape(BH, Lq, D), k.reshape(BH, Lk, D), v.reshape(BH, Lk, D)
+    ho, hl = out.view(BH, Lq, D), lse.view(BH, Lq)
+    main = torch.cuda.current_stream(dev)
+    # uploads on one stream (parallel upload streams measured slower: they make the
+    # first chunk's tensors arrive later), kernels on a second, downloads on a third
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    for s in (s_in, s_cmp, s_out):
+        s.wait_stream(main)
+    bounds = [(BH * i // chunks, BH * (i + 1) // chunks) for i in range(chunks)]
+    for a, b in bounds:
+        if a == b:
+            continue
+        with torch.cuda.stream(s_in):
+            dq[a:b].copy_(hq[a:b], non_blocking=True)
+            dk[a:b].copy_(hk[a:b], non_blocking=True)
+            dv[a:b].copy_(hv[a:b], non_blocking=True)
+        s_cmp.wait_stream(s_in)
+        with torch.cuda.stream(s_cmp):
+            n = b - a
+            attention(dq[a:b].view(1, n, Lq, D), dk[a:b].view(1, n, Lk, D), dv[a:b].view(1, n, Lk, D),
+                      causal=causal, scale=scale, out=do[a:b].view(1, n, Lq, D),
+                      lse=dl[a:b].view(1, n, Lq), stream=s_cmp)
+        s_out.wait_stream(s_cmp)
+        with torch.cuda.stream(s_out):
+            ho[a:b].copy_(do[a:b], non_blocking=True)
+            hl[a:b].copy_(dl[a:b], non_blocking=True)
+    main.wait_stream(s_out)
+    for t in (dq, dk, dv, do, dl):
+        for s in (s_in, s_cmp, s_out):
+            t.record_stream(s)
+    return out, lse
+
+
+def default_chunks(BH: int, Lq: int, Lk: int, causal: bool) -> int:
+    """Chunks for attention_from_host: enough to overlap the copies with the kernels,
+    few enough that each kernel still spreads over the GPU (at least 256 query-tile
+    pairs per chunk, at most 8 chunks)."""
+    units = BH * ((Lq + 255) // 256)
+    return max(1, min(8, units // 256, BH))
