@@ -154,6 +154,69 @@ int oracle_attn_full(const double *Q, const double *K, const double *V,
     return ORACLE_OK;
 }
 
+
+/*
+ * Local (sliding-window) attention for one (batch, head) slice: query row i may
+ * attend to key j iff  i - left <= j <= i + right  and 0 <= j < Lk, where left or
+ * right = -1 means unbounded on that side ("FlashAttention-2 forward in Triton",
+ * wsisp.com: local / sliding-window attention, whose queries do not attend to all
+ * tokens).  Rows and keys are aligned at index 0 as in the causal case, which is
+ * left = -1, right = 0.  The allowed keys of a row form one contiguous range, so
+ * each row is the definition above applied to that range of K and V rows.
+ * A row with no allowed key is an argument error (ORACLE_BAD_ARG).
+ * Arguments as oracle_attn_head; P (if given) is zero outside the range.
+ */
+int oracle_attn_head_window(const double *Q, const double *K, const double *V,
+                            long Lq, long Lk, long D, long left, long right, double scale,
+                            const long *rows, long nrows,
+                            double *O, double *LSE, double *P, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE) return ORACLE_BAD_ARG;
+    if (Lq < 0 || Lk < 1 || D < 1 || nrows < 0 || left < -1 || right < -1) return ORACLE_BAD_ARG;
+    if (!rows && nrows != Lq) return ORACLE_BAD_ARG;
+    for (long r = 0; r < nrows; ++r) {
+        const long i = rows ? rows[r] : r;
+        if (i < 0 || i >= Lq) return ORACLE_BAD_ARG;
+        const long lo = (left < 0 || i - left < 0) ? 0 : i - left;
+        const long hi = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;
+        if (lo > hi) return ORACLE_BAD_ARG;
+    }
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *S = (double *)malloc(sizeof(double) * (size_t)Lk);
+        double *Pr = (double *)malloc(sizeof(double) * (size_t)Lk);
+        if (!S || !Pr) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = ORACLE_NO_MEMORY;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+            for (long r = 0; r < nrows; ++r) {
+                const long i = rows ? rows[r] : r;
+                const long lo = (left < 0 || i - left < 0) ? 0 : i - left;
+                const long hi = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;
+                double *p_row = P ? P + r * Lk : NULL;
+                attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo + 1, D, hi - lo + 1, scale,
+                           S, Pr, O + r * D, LSE + r, p_row ? p_row + lo : NULL);
+                if (p_row)
+                    for (long j = 0; j < lo; ++j) p_row[j] = 0.0;
+                if (p_row)
+                    for (long j = hi + 1; j < Lk; ++j) p_row[j] = 0.0;
+            }
+        }
+        free(S);
+        free(Pr);
+    }
+    return status;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int oracle_max_threads(void)
 {

@@ -191,6 +191,95 @@ PINS = [pin_rows_sum_to_one, pin_single_key, pin_constant_v, pin_causal_row0,
         pin_online_recurrence, pin_golden, pin_row_subset]
 
 
+# --------------------------------------------------------------------------
+# Local (sliding-window) attention: key j allowed for row i iff
+# i - left <= j <= i + right (-1 = unbounded).
+# --------------------------------------------------------------------------
+
+def _window(i, Lk, left, right):
+    lo = 0 if left < 0 else max(0, i - left)
+    hi = Lk - 1 if right < 0 else min(Lk - 1, i + right)
+    return lo, hi
+
+
+WINDOW_CASES = [(9, 9, 3, 0), (12, 9, 4, 2), (6, 15, 2, 5), (10, 10, -1, 1), (8, 20, 0, -1),
+                (5, 5, 1, 1)]
+
+
+def pin_window_torch_f64(lib):
+    """Brute force with torch fp64 and an explicit window mask."""
+    for (Lq, Lk, left, right) in WINDOW_CASES:
+        g = torch.Generator().manual_seed(Lq * 31 + Lk + left)
+        q = torch.randn(Lq, 8, generator=g, dtype=torch.float64)
+        k = torch.randn(Lk, 8, generator=g, dtype=torch.float64)
+        v = torch.randn(Lk, 8, generator=g, dtype=torch.float64)
+        i = torch.arange(Lq)[:, None]
+        j = torch.arange(Lk)[None, :]
+        keep = torch.ones(Lq, Lk, dtype=torch.bool)
+        if left >= 0:
+            keep &= j >= i - left
+        if right >= 0:
+            keep &= j <= i + right
+        s = (q @ k.T * 0.4).masked_fill(~keep, float("-inf"))
+        O, L = lib.attn_head_window(q.numpy(), k.numpy(), v.numpy(), left, right, 0.4)
+        np.testing.assert_allclose(O, (torch.softmax(s, -1) @ v).numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_window_uniform(lib):
+    """Q = 0: each row averages exactly the value rows in its window, LSE = ln(width)."""
+    for (Lq, Lk, left, right) in WINDOW_CASES:
+        q, k, v = np.zeros((Lq, 4)), _rand((Lk, 4), 50), _rand((Lk, 4), 51)
+        O, L = lib.attn_head_window(q, k, v, left, right, 1.0)
+        for i in range(Lq):
+            lo, hi = _window(i, Lk, left, right)
+            np.testing.assert_allclose(O[i], v[lo:hi + 1].mean(axis=0), rtol=0, atol=1e-12)
+            assert abs(L[i] - math.log(hi - lo + 1)) < 1e-12
+
+
+def pin_window_single_key(lib):
+    """left = right = 0: row i sees only key i: O_i = V_i, LSE_i = scale q_i . k_i."""
+    q, k, v = _rand((6, 8), 52), _rand((9, 8), 53), _rand((9, 8), 54)
+    O, L = lib.attn_head_window(q, k, v, 0, 0, 0.7)
+    np.testing.assert_allclose(O, v[:6], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L, 0.7 * np.einsum("id,id->i", q, k[:6]), rtol=0, atol=1e-12)
+
+
+def pin_window_rows(lib):
+    """Probability rows sum to 1, are positive inside the window and 0 outside."""
+    for (Lq, Lk, left, right) in WINDOW_CASES:
+        q, k, v = _rand((Lq, 8), 55), _rand((Lk, 8), 56), _rand((Lk, 8), 57)
+        _, _, P = lib.attn_head_window(q, k, v, left, right, 0.5, want_p=True)
+        for i in range(Lq):
+            lo, hi = _window(i, Lk, left, right)
+            assert abs(P[i].sum() - 1.0) < 1e-12
+            assert np.all(P[i, lo:hi + 1] > 0) and np.all(P[i, :lo] == 0) and np.all(P[i, hi + 1:] == 0)
+
+
+def pin_window_online(lib):
+    """The online recurrence over the window's keys, for every block size."""
+    q, k, v = _rand((7, 8), 58, 2.0), _rand((12, 8), 59, 2.0), _rand((12, 8), 60)
+    left, right = 3, 2
+    O, L = lib.attn_head_window(q, k, v, left, right, 0.6)
+    for block in range(1, 8):
+        for i in range(7):
+            lo, hi = _window(i, 12, left, right)
+            o2, l2 = _online(q[i:i + 1], k[lo:hi + 1], v[lo:hi + 1], False, 0.6, block)
+            np.testing.assert_allclose(O[i], o2[0], rtol=0, atol=1e-12)
+            assert abs(L[i] - l2[0]) < 1e-12
+
+
+WINDOW_PINS = [pin_window_torch_f64, pin_window_uniform, pin_window_single_key, pin_window_rows,
+               pin_window_online]
+PINS.extend(WINDOW_PINS)
+
+
+def test_window_rejects_empty_rows(oracle_mod):
+    q, k, v = _rand((5, 4), 1), _rand((3, 4), 2), _rand((3, 4), 3)
+    with pytest.raises(ValueError):   # row 4 would need key 4 >= Lk
+        oracle_mod.attn_head_window(q, k, v, 0, 0, 1.0)
+
+
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
 def test_oracle_pin(oracle_mod, pin):
     pin(oracle_mod._get())
@@ -218,6 +307,9 @@ MUTATIONS = {
     "lse_missing_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "no_normalisation": ("for (long j = 0; j < n_allowed; ++j) P[j] /= l;", ";"),
     "causal_ignored": ("if (!causal) return Lk;", "return Lk;"),
+    "window_drops_last_key": ("attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo + 1, D, hi - lo + 1, scale,",
+                              "attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo, D, hi - lo, scale,"),
+    "window_shifted_values": ("attend_row(Q + i * D, K + lo * D, V + lo * D,", "attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
 }
 
 
