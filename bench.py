@@ -190,9 +190,12 @@ def measured_traffic(workload: str):
 
 # ----------------------------------------------------------------------------- CPU oracle legs
 def row_flops(w, rows) -> int:
-    if w.causal:
-        return int(sum(4 * w.D * min(int(i) + 1, w.Lk) for i in rows))
-    return 4 * w.D * w.Lk * len(rows)
+    """4 D flops per allowed (row, key) pair of the sampled rows."""
+    total = 0
+    for i in rows:
+        lo, hi = w.key_range(int(i))
+        total += hi - lo + 1
+    return 4 * w.D * total
 
 
 def time_oracle(w, q, k, v, budget_s: float, heads: int = 2, rows_per_call: int = 64, seed: int = 0):
@@ -214,7 +217,10 @@ def time_oracle(w, q, k, v, budget_s: float, heads: int = 2, rows_per_call: int 
         qq, kk, vv = per_head[it % len(per_head)]
         rows = rng.integers(0, w.Lq, size=rows_per_call)
         t0 = time.perf_counter()
-        oracle.attn_head(qq, kk, vv, w.causal, w.scale, rows=rows)
+        if w.window is not None:
+            oracle.attn_head_window(qq, kk, vv, w.window[0], w.window[1], w.scale, rows=rows)
+        else:
+            oracle.attn_head(qq, kk, vv, w.causal, w.scale, rows=rows)
         spent += time.perf_counter() - t0
         flops += row_flops(w, rows)
         nrows += rows_per_call
@@ -286,15 +292,23 @@ def run_ours(args, w):
 
     # Workspace for the split-key schedule, allocated once outside the timed region
     # (zero bytes, and plain fa_fwd semantics, for causal workloads).
-    st, ws_bytes = fa.fa_fwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
-    if st != fa.FA_OK:
-        raise RuntimeError(fa.fa_status_string(st))
+    # Local-window workloads run fa_fwd_window (whole units, no workspace).
+    if w.window is None:
+        st, ws_bytes = fa.fa_fwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
+        if st != fa.FA_OK:
+            raise RuntimeError(fa.fa_status_string(st))
+    else:
+        ws_bytes = 0
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
 
     def launch(i):
         q, k, v, o, lse = bufs[i % n_copies]
-        st = fa.fa_fwd_ws(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.causal, w.scale, ws,
-                          ws_bytes, stream)
+        if w.window is not None:
+            st = fa.fa_fwd_window(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.window[0],
+                                  w.window[1], w.scale, stream)
+        else:
+            st = fa.fa_fwd_ws(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.causal, w.scale, ws,
+                              ws_bytes, stream)
         if st != fa.FA_OK:
             raise RuntimeError(fa.fa_status_string(st))
 
@@ -341,7 +355,7 @@ def run_ours(args, w):
         def e2e_step():
             # the public host-buffer call: uploads, kernels and downloads overlapped by chunk
             fa.attention_from_host(q_p, k_p, v_p, causal=w.causal, scale=w.scale, out=o_p,
-                                   lse=l_p, device=dev)
+                                   lse=l_p, device=dev, window=w.window)
 
         e2e_steps = max(1, min(args.steps, 10))
         for _ in range(2):
@@ -384,7 +398,8 @@ def run_ours(args, w):
                        "l2": f"inputs rotate over {n_copies} copies "
                              f"({n_copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
                        "parallelism": f"replica per GPU x{world}",
-                       "schedule": "split key ranges" if ws_bytes else "whole units",
+                       "schedule": ("local-window band" if w.window is not None else
+                                    "split key ranges" if ws_bytes else "whole units"),
                        "workspace_bytes": ws_bytes},
             "pct_of_peak": 100.0 * kernel_tflops / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,

@@ -8,8 +8,8 @@ from __future__ import annotations
 import math
 
 from ._native import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
-                      FA_OK, fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_workspace_size,
-                      fa_fwd_ws, fa_last_device_status, fa_status_string)
+                      FA_OK, fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_window,
+                      fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status, fa_status_string)
 
 
 class FaError(RuntimeError):
@@ -38,13 +38,17 @@ def workspace_for(B, H, Lq, Lk, D, causal, device):
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-              stream=None, split: bool = True):
+              stream=None, split: bool = True, window=None):
     """O, LSE = exact attention of contiguous bf16 CUDA tensors q [B,H,Lq,D], k/v [B,H,Lk,D].
 
     Allocates ``out`` (bf16 [B,H,Lq,D]) and ``lse`` (fp32 [B,H,Lq]) if not given.  With
     ``split`` (default) it calls fa_fwd_ws with a cached workspace, so the library may
     split key ranges across SMs; ``split=False`` calls fa_fwd.  Calls that share the
     cached workspace (same device) must be ordered on one stream.
+
+    ``window=(left, right)`` restricts row i to keys i - left <= j <= i + right (-1:
+    unbounded side) and calls fa_fwd_window; with ``causal`` the band is cut at the
+    diagonal (right = 0).
     """
     import torch
     B, H, Lq, D = q.shape
@@ -60,7 +64,12 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
-    if split:
+    if window is not None:
+        left, right = (int(x) for x in window)
+        if causal:
+            right = 0
+        st = fa_fwd_window(q, k, v, out, lse, B, H, Lq, Lk, D, left, right, scale, stream)
+    elif split:
         ws, nbytes = workspace_for(B, H, Lq, Lk, D, causal, q.device)
         st = fa_fwd_ws(q, k, v, out, lse, B, H, Lq, Lk, D, causal, scale, ws, nbytes, stream)
     else:
@@ -71,14 +80,15 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
 
 
 def attention_from_host(q, k, v, causal: bool = False, scale: float | None = None, out=None,
-                        lse=None, chunks: int | None = None, device=None):
+                        lse=None, chunks: int | None = None, device=None, window=None):
     """Exact attention of host tensors: copies in, computes, copies out, overlapped.
 
     ``q`` [B,H,Lq,D], ``k``/``v`` [B,H,Lk,D] are contiguous bf16 CPU tensors (pinned for
     the copies to overlap).  The (batch, head) slices are cut into ``chunks`` groups;
     group i+1 travels to the GPU while group i is computed and group i-1 travels back,
     on three streams ordered by events.  Returns host ``out`` (bf16) and ``lse`` (fp32),
-    allocated pinned if not given.  Device buffers are allocated per call.
+    allocated pinned if not given.  Device buffers are allocated per call.  ``window``
+    as for ``attention``.
     """
     import torch
     B, H, Lq, D = q.shape
@@ -120,7 +130,7 @@ def attention_from_host(q, k, v, causal: bool = False, scale: float | None = Non
             n = b - a
             attention(dq[a:b].view(1, n, Lq, D), dk[a:b].view(1, n, Lk, D), dv[a:b].view(1, n, Lk, D),
                       causal=causal, scale=scale, out=do[a:b].view(1, n, Lq, D),
-                      lse=dl[a:b].view(1, n, Lq), stream=s_cmp)
+                      lse=dl[a:b].view(1, n, Lq), stream=s_cmp, window=window)
         s_out.wait_stream(s_cmp)
         with torch.cuda.stream(s_out):
             ho[a:b].copy_(do[a:b], non_blocking=True)

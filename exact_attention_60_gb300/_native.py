@@ -18,7 +18,7 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 # Every symbol include/fa.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_noalloc",
+EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_noalloc",
             "fa_status_string", "fa_last_device_status", "fa_debug_set")
 
 _lib = None
@@ -43,6 +43,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp,
                               ctypes.c_size_t, vp]
+    lib.fa_fwd_window.restype = ctypes.c_int
+    lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 7 + [ctypes.c_float, vp]
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
@@ -95,6 +97,14 @@ def fa_fwd_ws(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, workspace, worksp
     return load().fa_fwd_ws(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
                             int(Lq), int(Lk), int(D), int(bool(causal)), float(scale),
                             _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_window(Q, K, V, O, LSE, B, H, Lq, Lk, D, window_left, window_right, scale,
+                  stream=None) -> int:
+    """C ``fa_fwd_window``: keys i - window_left <= j <= i + window_right (-1: unbounded)."""
+    return load().fa_fwd_window(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
+                                int(Lq), int(Lk), int(D), int(window_left), int(window_right),
+                                float(scale), _stream(stream))
 
 
 def fa_fwd_noalloc(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, stream=None) -> int:

@@ -69,6 +69,13 @@ constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold on the running max (log2 units)
 constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // one second per wait
 
+// Work schedules, one kernel instantiation each (template parameter kS).
+//   kSchedWhole: whole units, every query tile starts at key tile 0 (full or causal mask).
+//   kSchedSplit: non-causal key ranges cut across CTAs, merged by fa_combine_kernel.
+//   kSchedBand : local (sliding-window) attention; each query tile covers its own band
+//                of key tiles, and only tiles cut by the band's edges are masked.
+enum Sched : int { kSchedWhole = 0, kSchedSplit = 1, kSchedBand = 2 };
+
 enum WaitSite : uint32_t {
   kSiteLoadKV = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteSoftS, kSiteSoftO
 };
@@ -122,6 +129,9 @@ struct Params {
   long long total_steps;   // n_units * nkv (split schedule)
   float* ws_o;        // split schedule: partial O rows   [2 * grid][2 tiles][128 rows][D] fp32
   float* ws_ml;       //                 partial (m, l)   [2 * grid][2 tiles][128 rows][2] fp32
+  int win_left;       // band schedule: key j allowed for row i iff i - win_left <= j <= i + win_right,
+  int win_right;      //   -1 = unbounded on that side; both are below Lq / Lk
+  int band_desc;      // band schedule: 1 = units in descending query order (heavier last tiles)
   float scale_log2;   // scale * log2(e)
   uint32_t flags;     // test hooks (fa_debug_set)
   unsigned long long wait_limit_ns;
@@ -144,7 +154,8 @@ struct Unit {
   int q0;
   int kv0;       // first key tile of this (part of a) unit
   int nblk[2];   // key tiles of query tile 0 and 1 in this part (0 = tile absent)
-  int nmax;
+  int first[2];  // band schedule: key tile (relative to kv0) where query tile i starts
+  int nmax;      // key tiles loaded for the unit: the union of the tiles' ranges
   int partial;   // 1: a part of a unit split across CTAs
   int slot;      // workspace slot of this part: 2 * CTA + (first part of the CTA ? 0 : 1)
 };
@@ -164,11 +175,58 @@ __device__ __forceinline__ void unit_rows(const Params& p, int idx, Unit& u) {
   }
 }
 
-template <bool kSplit>
+// Band schedule: allowed keys of row q are [band_lo(q), band_lim(q)).
+__device__ __forceinline__ int band_lo(const Params& p, int q) {
+  return p.win_left < 0 ? 0 : max(0, q - p.win_left);
+}
+__device__ __forceinline__ int band_lim(const Params& p, int q) {
+  return p.win_right < 0
+             ? p.Lk
+             : static_cast<int>(min(static_cast<long long>(p.Lk),
+                                    static_cast<long long>(q) + p.win_right + 1));
+}
+
+template <int kS>
 __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
   const int G = static_cast<int>(gridDim.x);
   const int g = static_cast<int>(blockIdx.x);
-  if constexpr (!kSplit) {
+  if constexpr (kS == kSchedBand) {
+    // Units in the order that puts the heaviest first: descending query order
+    // when the band is bounded on the right or open on the left (the last tiles
+    // see the most keys), ascending when only the left side is bounded.
+    const int idx = r * G + ((r & 1) ? (G - 1 - g) : g);
+    if (idx >= p.n_units) return false;
+    const int pi = idx / p.bh_count;
+    const int pair = p.band_desc ? p.n_pairs - 1 - pi : pi;
+    u.bh = idx % p.bh_count;
+    u.q0 = pair * 2 * kBlockM;
+    // Tile i covers key tiles a[i]..b[i]: from the band's left edge at its first
+    // row to its right edge at its last stored row (the band only moves right as
+    // the row grows, and every row's band is non-empty).  The two ranges overlap or
+    // touch, so the unit loads one contiguous run of key tiles.
+    int a[2], b[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int qt = u.q0 + i * kBlockM;
+      if (qt >= p.Lq) {   // tile 1 absent (tile 0 never is)
+        a[i] = a[0];
+        b[i] = a[0] - 1;
+        continue;
+      }
+      const int last = min(qt + kBlockM, p.Lq) - 1;   // last row that is stored
+      a[i] = band_lo(p, qt) / kBlockN;
+      b[i] = (band_lim(p, last) - 1) / kBlockN;
+    }
+    u.kv0 = a[0];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      u.first[i] = a[i] - a[0];
+      u.nblk[i] = b[i] - a[i] + 1;   // 0 when the tile is absent
+    }
+    u.nmax = max(u.nblk[0], u.first[1] + u.nblk[1]);
+    u.partial = 0;
+    return true;
+  } else if constexpr (kS == kSchedWhole) {
     const int idx = r * G + ((r & 1) ? (G - 1 - g) : g);
     if (idx >= p.n_units) return false;
     unit_rows(p, idx, u);
@@ -179,6 +237,7 @@ __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
     }
     u.nmax = max(u.nblk[0], u.nblk[1]);
     u.kv0 = 0;
+    u.first[0] = u.first[1] = 0;
     u.partial = 0;
     return true;
   } else {
@@ -197,6 +256,7 @@ __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
   for (int i = 0; i < 2; ++i) u.nblk[i] = (u.q0 + i * kBlockM >= p.Lq) ? 0 : len;
   u.nmax = len;
   u.kv0 = a;
+  u.first[0] = u.first[1] = 0;
   u.partial = (len != p.nkv);
   if (u.partial) u.slot = 2 * g + (x == lo ? 0 : 1);
   return true;
@@ -256,11 +316,13 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned
   return true;
 }
 
-// kSplit selects the schedule at compile time, so the whole-unit kernel carries
-// none of the split schedule's code.
-template <int HD, bool kSplit>
+// kS selects the schedule at compile time, so the whole-unit kernel carries none
+// of the other schedules' code.
+template <int HD, int kS>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<HD>;
+  constexpr bool kSplit = kS == kSchedSplit;
+  constexpr bool kBand = kS == kSchedBand;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -315,14 +377,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint32_t o_count = 0;   // units finished by this warpgroup (o_full phase)
     bool ok = true;
     Unit u;
-    for (int r = 0; ok && unit_of<kSplit>(p, r, u); ++r) {
+    for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
       const int n_blocks = wg ? u.nblk[1] : u.nblk[0];
       if (n_blocks == 0) continue;
       const int bh = u.bh;
       const int qt = u.q0 + wg * kBlockM;
       const int q = qt + row;
-      const int key_lim = p.causal ? min(p.Lk, q + 1) : p.Lk;
+      const int key_lim = kBand ? band_lim(p, q) : (p.causal ? min(p.Lk, q + 1) : p.Lk);
       const int first_diag = p.causal ? qt / kBlockN : INT_MAX;
+      // Band: row q keeps keys [key_lo, key_lim); a key tile needs masking when the
+      // band's left edge (of the tile's last row) or right edge (of its first row) cuts it.
+      const int key_lo = kBand ? band_lo(p, q) : 0;
+      const int lo_last = kBand ? band_lo(p, qt + kBlockM - 1) : 0;
+      const int lim_first = kBand ? band_lim(p, qt) : 0;
+      const int jb0 = kBand ? u.kv0 + (wg ? u.first[1] : u.first[0]) : (kSplit ? u.kv0 : 0);
       float m = -INFINITY;   // running max of scaled scores, log2 units (possibly stale by < 8)
       float l = 0.0f;        // running sum of exp2(s*sl2 - m)
       for (int j = 0; j < n_blocks; ++j) {
@@ -335,8 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        const int jb = kSplit ? u.kv0 + j : j;   // key tile index
-        if (jb >= first_diag || (jb + 1) * kBlockN > p.Lk) {
+        const int jb = jb0 + j;   // key tile index
+        if constexpr (kBand) {
+          if (jb * kBlockN < lo_last || (jb + 1) * kBlockN > lim_first) {
+            const int lo = key_lo - jb * kBlockN;    // columns lo <= c < lim are allowed keys
+            const int lim = key_lim - jb * kBlockN;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = (c >= lo && c < lim) ? s[c] : -INFINITY;
+          }
+        } else if (jb >= first_diag || (jb + 1) * kBlockN > p.Lk) {
           const int lim = key_lim - jb * kBlockN;   // columns c < lim are allowed keys
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
@@ -456,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       bool ok = true;
       bool first = true;
       Unit u;
-      for (int r = 0; ok && unit_of<kSplit>(p, r, u); ++r) {
+      for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (u.nblk[i] == 0) continue;
@@ -487,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int rg = 0; rg < L::kRegions; ++rg)
               ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + rg * L::kRegionBytes,
                                t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * rg,
-                               (kSplit ? u.kv0 + j : j) * kBlockN, u.bh);
+                               (kS != kSchedWhole ? u.kv0 + j : j) * kBlockN, u.bh);
             last_fill[s] = static_cast<int>(it);
           }
         }
@@ -536,9 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       uint32_t it_base = 0;           // K/V ring position of this unit's K_0
       bool ok = true;
       Unit u;
-      for (int r = 0; ok && unit_of<kSplit>(p, r, u); ++r) {
+      for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
         const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
         const int nblk[2] = {nb0, nb1};
+        // Step j of the unit (key tile kv0 + j) is step j - fst[i] of query tile i.
+        const int fst[2] = {0, kBand ? u.first[1] : 0};
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (ok && nblk[i] > 0)
@@ -550,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         ptx::tc_fence_after();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          if (nblk[i] > 0) {
+          if (nblk[i] > 0 && fst[i] == 0) {
             issue_s(i, slot_k0);
             ptx::mma_commit(bar(L::kBarSFull + i));
             if (nblk[i] == 1) ptx::mma_commit(bar(L::kBarQEmpty + i));
@@ -578,19 +655,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           bool k_ready = false;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            if (j >= nblk[i]) continue;
-            if (!wait_phase(bar(L::kBarPFull + i), (p_base[i] + j) & 1, abort_flag, limit,
+            const int jl = j - fst[i];
+            if (jl < 0 || jl >= nblk[i]) continue;
+            if (!wait_phase(bar(L::kBarPFull + i), (p_base[i] + jl) & 1, abort_flag, limit,
                             kSiteMmaP)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            issue_pv(i, slot_v, j > 0);
-            if (j == nblk[i] - 1) {
+            issue_pv(i, slot_v, jl > 0);
+            if (jl == nblk[i] - 1) {
               ptx::mma_commit(bar(L::kBarOFull + i));
               if (nblk[i] > 1) ptx::mma_commit(bar(L::kBarQEmpty + i));   // Q_i no longer read
             }
-            if (j + 1 < nblk[i]) {
+            if (jl + 1 < nblk[i]) {
               if (!k_ready) {
                 if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
                                 limit, kSiteMmaK)) {
@@ -602,6 +680,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               }
               issue_s(i, slot_k);
               ptx::mma_commit(bar(L::kBarSFull + i));
+            }
+          }
+          if constexpr (kBand) {
+            // A query tile whose band starts at the next key tile: its first S GEMM.
+            if (ok && nblk[1] > 0 && fst[1] == j + 1) {
+              if (!k_ready) {
+                if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
+                                limit, kSiteMmaK)) {
+                  ok = false;
+                } else {
+                  ptx::tc_fence_after();
+                  k_ready = true;
+                }
+              }
+              if (ok) {
+                issue_s(1, slot_k);
+                ptx::mma_commit(bar(L::kBarSFull + 1));
+                if (nblk[1] == 1) ptx::mma_commit(bar(L::kBarQEmpty + 1));
+              }
             }
           }
           if (!ok) break;
@@ -749,7 +846,7 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
-  bool attr[2][2] = {{false, false}, {false, false}};   // [D == 128][split]
+  bool attr[2][3] = {};   // [D == 128][schedule]: shared-memory opt-in done
 };
 
 std::mutex g_mutex;
@@ -761,6 +858,18 @@ std::atomic<unsigned long long> g_wait_limit_ns{0};
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
   return na && nb && pa < pb + nb && pb < pa + na;
+}
+
+// The attention kernel instance for head dimension D and schedule `sched` (fa::Sched).
+using KernelFn = void (*)(const Params);
+KernelFn attention_kernel(int D, int sched) {
+  if (D == 64)
+    return sched == fa::kSchedBand    ? fa::fa_fwd_kernel<64, fa::kSchedBand>
+           : sched == fa::kSchedSplit ? fa::fa_fwd_kernel<64, fa::kSchedSplit>
+                                      : fa::fa_fwd_kernel<64, fa::kSchedWhole>;
+  return sched == fa::kSchedBand    ? fa::fa_fwd_kernel<128, fa::kSchedBand>
+         : sched == fa::kSchedSplit ? fa::fa_fwd_kernel<128, fa::kSchedSplit>
+                                    : fa::fa_fwd_kernel<128, fa::kSchedWhole>;
 }
 
 // Shared-memory opt-in for one kernel instance, and a check that the registers it
@@ -806,17 +915,12 @@ fa_status prepare_device(int dev, int D, int* sm_count) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   const int di = (D == 128) ? 1 : 0;
-  for (int sp = 0; sp < 2; ++sp) {
-    if (info.attr[di][sp]) continue;
-    fa_status st;
-    if (D == 64)
-      st = sp ? configure_kernel(fa::fa_fwd_kernel<64, true>, fa::Layout<64>::kAlloc)
-              : configure_kernel(fa::fa_fwd_kernel<64, false>, fa::Layout<64>::kAlloc);
-    else
-      st = sp ? configure_kernel(fa::fa_fwd_kernel<128, true>, fa::Layout<128>::kAlloc)
-              : configure_kernel(fa::fa_fwd_kernel<128, false>, fa::Layout<128>::kAlloc);
+  for (int sc = 0; sc < 3; ++sc) {
+    if (info.attr[di][sc]) continue;
+    const fa_status st = configure_kernel(attention_kernel(D, sc),
+                                          D == 64 ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc);
     if (st != FA_OK) return st;
-    info.attr[di][sp] = true;
+    info.attr[di][sc] = true;
   }
   return FA_OK;
 }
@@ -851,6 +955,9 @@ struct Problem {
   long long bh;
   int n_pairs, n_units, nkv;
   size_t bytes_q, bytes_k, bytes_lse;
+  bool band = false;     // local attention over the band below (fa_fwd_window)
+  int win_left = -1;     // key j allowed for row i iff i - win_left <= j <= i + win_right
+  int win_right = -1;    //   (-1: unbounded side)
 };
 
 // FA_OK with *empty = true means there is nothing to compute (no launch).
@@ -899,6 +1006,7 @@ fa_status check_problem(const void* Q, const void* K, const void* V, void* O, fl
 // 21 % fill and 61 % at 42 % fill (D = 128), and lost 9-36 % at 84 % fill.
 struct Plan {
   bool split;
+  bool band;
   int grid;
   size_t off_ml, ws_bytes;
 };
@@ -938,6 +1046,10 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   p.n_units = pr.n_units;
   p.nkv = pr.nkv;
   p.split = pl.split ? 1 : 0;
+  p.win_left = pr.win_left;
+  p.win_right = pr.win_right;
+  // Heaviest units first: the last query tiles unless only the left side is bounded.
+  p.band_desc = (pr.win_left >= 0 && pr.win_right < 0) ? 0 : 1;
   p.total_steps = static_cast<long long>(pr.n_units) * pr.nkv;
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
@@ -959,16 +1071,9 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
   cfg.blockDim = dim3(fa::kThreads);
   cfg.stream = stream;
-  cudaError_t err;
-  if (pr.D == 64) {
-    cfg.dynamicSmemBytes = fa::Layout<64>::kAlloc;
-    err = pl.split ? cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<64, true>, p)
-                   : cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<64, false>, p);
-  } else {
-    cfg.dynamicSmemBytes = fa::Layout<128>::kAlloc;
-    err = pl.split ? cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<128, true>, p)
-                   : cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<128, false>, p);
-  }
+  cfg.dynamicSmemBytes = (pr.D == 64) ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc;
+  const int sched = pl.band ? fa::kSchedBand : pl.split ? fa::kSchedSplit : fa::kSchedWhole;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched), p);
   if (err != cudaSuccess) return FA_ERR_CUDA;
   if (pl.split && pl.grid > 1) {
     // Merge the parts of every split unit (same stream: runs after the parts exist).
@@ -1070,6 +1175,38 @@ extern "C" fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void
       return FA_ERR_INVALID_ARG;
   }
   return launch(pr, sm_count, pl, workspace, stream);
+}
+
+extern "C" fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O,
+                                   float* LSE, int B, int H, int Lq, int Lk, int D,
+                                   int window_left, int window_right, float scale,
+                                   cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  Problem pr;
+  bool empty = false;
+  const fa_status st = check_problem(Q, K, V, O, LSE, B, H, Lq, Lk, D, 0, scale, &pr, &empty);
+  if (st != FA_OK || empty) return st;
+  // A side of the band that reaches past every row's first or last key is unbounded.
+  int left = window_left, right = window_right;
+  if (left >= Lq - 1) left = -1;
+  if (right >= Lk - 1) right = -1;
+  // Every row needs an allowed key: the last row's band starts at Lq - 1 - left.
+  if (left >= 0 && Lq - 1 - left > Lk - 1) return FA_ERR_INVALID_ARG;
+  int sm_count = 0;
+  const fa_status prep = current_device(D, &sm_count);
+  if (prep != FA_OK) return prep;
+  const bool force_band = (g_debug_flags.load() & 4u) != 0;
+  if (!force_band && left < 0 && (right < 0 || right == 0)) {
+    pr.causal = (right == 0) ? 1 : 0;   // the full or the causal mask: whole units
+  } else {
+    pr.band = true;
+    pr.win_left = left;
+    pr.win_right = right;
+  }
+  Plan pl{};
+  pl.band = pr.band;
+  pl.grid = std::min(pr.n_units, sm_count);
+  return launch(pr, sm_count, pl, nullptr, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation entry point

@@ -4,11 +4,13 @@ This module holds no attention arithmetic.  It is the one module that both the
 CUDA path (tests, benchmark) and the fp64 oracle's callers draw inputs from, so
 the two sides always see the same bits.
 
-The five workloads are the ones the method is measured on: a tiny head pair,
-a 1K-token D=64 batch (non-causal and causal), a 4K-token and a 16K-token
+The first five workloads are the ones the method is measured on: a tiny head
+pair, a 1K-token D=64 batch (non-causal and causal), a 4K-token and a 16K-token
 causal D=128 batch, and a ragged cross-attention case whose query/key
-logits are scaled up (standard deviation 3) to stress the softmax.  Inputs are
-i.i.d. normal draws rounded to bf16, contiguous ``[B, H, L, D]``.
+logits are scaled up (standard deviation 3) to stress the softmax.  Two more
+exercise local (sliding-window) attention: 16K tokens with a causal window of
+4096 keys, and 4K tokens with a symmetric band of 256 keys on each side.  Inputs
+are i.i.d. normal draws rounded to bf16, contiguous ``[B, H, L, D]``.
 """
 from __future__ import annotations
 
@@ -31,6 +33,7 @@ class Workload:
     sigma_qk: float = 1.0   # standard deviation of Q and K draws
     sigma_v: float = 1.0    # standard deviation of V draws
     index: int = 0          # position in the workload list (fixes the seed)
+    window: tuple | None = None   # (left, right): keys i-left <= j <= i+right (-1: unbounded)
 
     @property
     def scale(self) -> float:
@@ -41,8 +44,23 @@ class Workload:
     def seed(self) -> int:
         return 1234 + self.index
 
+    def key_range(self, i: int):
+        """First and last allowed key of query row i."""
+        if self.window is not None:
+            left, right = self.window
+            lo = 0 if left < 0 else max(0, i - left)
+            hi = self.Lk - 1 if right < 0 else min(self.Lk - 1, i + right)
+            return lo, hi
+        return 0, (min(i, self.Lk - 1) if self.causal else self.Lk - 1)
+
     def pairs_per_head(self) -> int:
         """Unmasked (query, key) pairs of one head."""
+        if self.window is not None:
+            i = np.arange(self.Lq, dtype=np.int64)
+            left, right = self.window
+            lo = np.zeros_like(i) if left < 0 else np.maximum(0, i - left)
+            hi = np.full_like(i, self.Lk - 1) if right < 0 else np.minimum(self.Lk - 1, i + right)
+            return int(np.sum(hi - lo + 1))
         if not self.causal:
             return self.Lq * self.Lk
         # top-left aligned causal: row i keeps keys 0..min(i, Lk-1)
@@ -61,6 +79,8 @@ class Workload:
 
     def describe(self) -> str:
         kind = "causal" if self.causal else "non-causal"
+        if self.window is not None:
+            kind = f"window=({self.window[0]},{self.window[1]})"
         return (f"B={self.B},H={self.H},Lq={self.Lq},Lk={self.Lk},D={self.D},{kind},"
                 f"sigma_qk={self.sigma_qk:g},sigma_v={self.sigma_v:g}")
 
@@ -73,6 +93,10 @@ WORKLOADS = {
     "seq16k_d128_causal": Workload("seq16k_d128_causal", 1, 16, 16384, 16384, 128, True, index=3),
     "cross_q500_k8191_d128": Workload("cross_q500_k8191_d128", 8, 16, 500, 8191, 128, False,
                                       sigma_qk=3.0, sigma_v=1.0, index=4),
+    "seq16k_d128_window4k": Workload("seq16k_d128_window4k", 1, 16, 16384, 16384, 128, False,
+                                     index=5, window=(4095, 0)),
+    "seq4k_d64_local256": Workload("seq4k_d64_local256", 2, 16, 4096, 4096, 64, False,
+                                   index=6, window=(256, 256)),
 }
 
 

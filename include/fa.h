@@ -116,6 +116,31 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_fwd_window -- local (sliding-window) attention: the operation of fa_fwd with
+ * the allowed keys of row i restricted to a band around it,
+ *     i - window_left <= j <= i + window_right   (and 0 <= j < Lk),
+ * where -1 leaves that side unbounded.  Rows and keys are aligned at index 0 as
+ * for the causal mask, which is the band (-1, 0); (-1, -1) is the full softmax.
+ * The variant is the local / sliding-window attention that the wsisp.com post
+ * "FlashAttention-2 forward in Triton" names among the masks FA-2 supports
+ * (queries attend to a window of keys, not to all of them).  Key tiles outside
+ * a query tile's band are skipped; only tiles the band's edges cut are masked.
+ *
+ *   window_left, window_right : >= -1.  A side at least Lq - 1 (left) or Lk - 1
+ *     (right) keys wide covers every key on that side and counts as unbounded.
+ *   Other arguments, layout, ownership and execution: as fa_fwd (whole units, no
+ *   workspace; the bands (-1, 0) and (-1, -1) run fa_fwd's causal and full
+ *   kernels).  LSE is taken over each row's band.
+ *
+ * Returns FA_ERR_INVALID_ARG for a side below -1, and when some row would have no
+ * allowed key (window_left >= 0 and Lq - 1 - window_left > Lk - 1: the band of
+ * the last row starts past the last key); otherwise as fa_fwd.
+ */
+fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        int B, int H, int Lq, int Lk, int D, int window_left, int window_right,
+                        float scale, cudaStream_t stream);
+
+/*
  * fa_fwd_noalloc -- fa_fwd_ws without a workspace argument, for callers that
  * cannot allocate device memory: code that only receives the input and output
  * pointers through a fixed interface with no allocator to ask, and code that
@@ -159,8 +184,11 @@ fa_status fa_last_device_status(cudaStream_t stream);
  * pipeline wait inside the kernels (0 restores the default of one second).
  * `flags` bit 0 makes the load warp withhold the first value-tile load, so
  * that the consumers' waits run out and the kernel reports FA_ERR_TIMEOUT
- * through fa_last_device_status() instead of completing.  Not for production
- * use; returns FA_OK.
+ * through fa_last_device_status() instead of completing.  Bit 1 makes every
+ * launch fail with FA_ERR_CUDA before anything is queued.  Bit 2 makes
+ * fa_fwd_window run its band kernel also for the bands (-1, 0) and (-1, -1), so
+ * that it can be compared with fa_fwd's kernels.  Not for production use;
+ * returns FA_OK.
  */
 fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns);
 

@@ -125,3 +125,31 @@ def test_fwd_ws_rejects_bad_arguments_before_any_cuda_call(lib, kw, expect):
     assert fa.fa_fwd_ws(args["Q"], args["K"], args["V"], args["O"], args["LSE"], args["B"],
                         args["H"], args["Lq"], args["Lk"], args["D"], args["causal"],
                         args["scale"], None, 0, 0) == expect
+
+
+def call_window(left, right, Lq=16, Lk=16, **kw):
+    args = dict(Q=ALIGNED, K=2 * ALIGNED, V=3 * ALIGNED, O=4 * ALIGNED, LSE=5 * ALIGNED, B=1, H=1,
+                D=64, scale=0.125)
+    args.update(kw)
+    return fa.fa_fwd_window(args["Q"], args["K"], args["V"], args["O"], args["LSE"], args["B"],
+                            args["H"], Lq, Lk, args["D"], left, right, args["scale"], 0)
+
+
+@pytest.mark.parametrize("left,right,Lq,Lk,kw,expect", [
+    (-2, 0, 16, 16, {}, fa.FA_ERR_INVALID_ARG),          # a side below -1
+    (3, -5, 16, 16, {}, fa.FA_ERR_INVALID_ARG),
+    (0, 0, 17, 16, {}, fa.FA_ERR_INVALID_ARG),           # row 16 would need key 16
+    (3, -1, 300, 200, {}, fa.FA_ERR_INVALID_ARG),        # rows 204.. start past the last key
+    (4, 4, 16, 16, dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (4, 4, 16, 0, {}, fa.FA_ERR_INVALID_ARG),
+    (4, 4, 16, 16, dict(Q=0), fa.FA_ERR_INVALID_ARG),
+    (4, 4, 16, 16, dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (4, 4, 16, 16, dict(O=ALIGNED), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_window_rejects_bad_arguments_before_any_cuda_call(lib, left, right, Lq, Lk, kw, expect):
+    assert call_window(left, right, Lq, Lk, **kw) == expect
+
+
+def test_fwd_window_empty_problem_is_ok_without_launch(lib):
+    assert call_window(2, 2, Lq=0, Lk=16) == fa.FA_OK
+    assert call_window(2, 2, B=0, Q=0, K=0, V=0, O=0, LSE=0) == fa.FA_OK
