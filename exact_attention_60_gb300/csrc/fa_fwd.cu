@@ -77,7 +77,8 @@ constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // one second per 
 enum Sched : int { kSchedWhole = 0, kSchedSplit = 1, kSchedBand = 2 };
 
 enum WaitSite : uint32_t {
-  kSiteLoadKV = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteSoftS, kSiteSoftO
+  kSiteLoadKV = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteSoftS, kSiteSoftO,
+  kSiteMmaSFree, kSiteSoftPV
 };
 
 template <int HD>
@@ -98,16 +99,28 @@ struct Layout {
   static constexpr int kBarOFull = kBarPFull + 2;           // [2] last P_i V MMA of a unit done
   static constexpr int kBarOEmpty = kBarOFull + 2;          // [2] epilogue has read O_i
   static constexpr int kBarDrain = kBarOEmpty + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  // Decoupled pipeline only (kDecoupled): S_i read out of TMEM into registers, and
+  // the last P_i V MMA issued so far done (P_i columns free, O_i stable).
+  static constexpr int kBarSFree = kBarDrain + 1;           // [2]
+  static constexpr int kBarPVDone = kBarSFree + 2;          // [2]
+  static constexpr int kNumBars = kBarPVDone + 2;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kAlloc = kBytes + 1024;           // slack to align the base to 1 KB
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: S_0 | S_1 | O_0 | O_1.  P_i (bf16 pairs) overwrites the first 64 columns of S_i.
+  // TMEM columns: S_0 | S_1 | O_0 | O_1.  At D = 128 P_i (bf16 pairs) overwrites the
+  // first 64 columns of S_i, so S_i(j+1) can only be computed after P_i(j) V.  At D = 64
+  // the 128 columns left over hold P_0 | P_1 (kDecoupled): S_i(j+1) is computed as
+  // soon as the softmax has read S_i(j), while it still works on that tile.
+  static constexpr bool kDecoupled = (HD == 64);
   __host__ __device__ static constexpr uint32_t col_s(int i) { return 128u * i; }
   __host__ __device__ static constexpr uint32_t col_o(int i) { return 256u + HD * i; }
+  __host__ __device__ static constexpr uint32_t col_p(int i) {
+    return kDecoupled ? 256u + 2u * HD + 64u * i : 128u * i;
+  }
 };
+static_assert(256 + 2 * 64 + 2 * 64 <= 512, "D = 64 TMEM budget: S, O and P of two tiles");
 
 static_assert(Layout<128>::kAlloc <= 232448, "shared memory budget (D=128)");
 static_assert(Layout<64>::kAlloc <= 232448, "shared memory budget (D=64)");
@@ -306,6 +319,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
+// wait_phase for a whole warp that must stay converged: true only if every lane's
+// wait succeeded.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns, uint32_t site) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, limit_ns, site));
+}
+
 // Bounded wait used while draining: ignores the abort flag (the copy or MMA being
 // waited for completes on its own), still limited in time.
 __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
@@ -350,6 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       ptx::mbar_init(bar(L::kBarKVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kBarDrain), 1);
+    if constexpr (L::kDecoupled) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(bar(L::kBarSFree + i), 4 * 32);
+        ptx::mbar_init(bar(L::kBarPVDone + i), 1);
+      }
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -372,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t lane_off = static_cast<uint32_t>(rw * 32) << 16;
     const uint32_t t_s = tmem + lane_off + L::col_s(wg);
     const uint32_t t_o = tmem + lane_off + L::col_o(wg);
+    const uint32_t t_p = tmem + lane_off + L::col_p(wg);
     const float sl2 = p.scale_log2;
     uint32_t s_base = 0;    // S_i tiles consumed in earlier units (s_full / p_full phase)
     uint32_t o_count = 0;   // units finished by this warpgroup (o_full phase)
@@ -400,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         ptx::tc_fence_after();
         uint32_t sr[128];
         ptx::tmem_ld32x32b_x128(t_s, sr);
+        if constexpr (L::kDecoupled) {   // S_i is in registers: the MMA may overwrite it
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::kBarSFree + wg));
+        }
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -436,25 +468,60 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const uint64_t k2 = ptx::pack_f32x2(sl2, sl2);
         const uint64_t c2 = ptx::pack_f32x2(neg_m, neg_m);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        if constexpr (L::kDecoupled) {
+          // P_i(j) may only be stored once P_i(j-1) V has been computed (P_i columns
+          // free, O_i no longer being accumulated): the first half of the row is
+          // exponentiated before that wait, the second half while the first is stored.
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            pk[c] = ptx::exp2_pair_bf16(s[64 * h + 2 * c], s[64 * h + 2 * c + 1], k2, c2, acc[c & 3]);
-          ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
-        }
-        float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
-        float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
-        l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
-        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+            pk[c] = ptx::exp2_pair_bf16(s[2 * c], s[2 * c + 1], k2, c2, acc[c & 3]);
+          if (j > 0) {
+            ok = wait_phase(bar(L::kBarPVDone + wg), (s_base + j - 1) & 1, abort_flag, limit,
+                            kSiteSoftPV);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int c0 = 0; c0 < HD; c0 += 32) {
-            uint32_t o[32];
-            ptx::tmem_ld32x32b_x32(t_o + c0, o);
+              for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t o[32];
+                ptx::tmem_ld32x32b_x32(t_o + c0, o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            ptx::tmem_st32x32b_x32(t_o + c0, o);
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                ptx::tmem_st32x32b_x32(t_o + c0, o);
+              }
+            }
+          }
+          ptx::tmem_st32x32b_x32(t_p, pk);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            pk[c] = ptx::exp2_pair_bf16(s[64 + 2 * c], s[64 + 2 * c + 1], k2, c2, acc[c & 3]);
+          ptx::tmem_st32x32b_x32(t_p + 32, pk);
+          float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
+          float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
+          l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              pk[c] = ptx::exp2_pair_bf16(s[64 * h + 2 * c], s[64 * h + 2 * c + 1], k2, c2, acc[c & 3]);
+            ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
+          }
+          float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
+          float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
+          l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+              uint32_t o[32];
+              ptx::tmem_ld32x32b_x32(t_o + c0, o);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              ptx::tmem_st32x32b_x32(t_o + c0, o);
+            }
           }
         }
         ptx::tmem_st_wait();
@@ -581,7 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA warp
     ptx::setmaxnreg_dec<kRegsOther>();
-    if (lane == 0) {   // one thread issues every MMA and commit
+    {   // The whole warp runs the loop, so its state stays warp-uniform; one elected
+        // lane issues every MMA and commit.
       constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false);
       constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true);
       // Descriptors of the first operand blocks; later blocks differ only in the
@@ -595,14 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kRegionBytes + (kk & 3) * 32) >> 4;
-          ptx::mma_ss(tmem + L::col_s(i), a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
+          ptx::mma_ss_warp(tmem + L::col_s(i), a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int i, int slot, bool accumulate) {
         const uint64_t b = desc_v0 + ((slot * L::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          ptx::mma_ts(tmem + L::col_o(i), tmem + L::col_s(i) + kk * 8, b + ((kk * 16 * 128) >> 4),
+          ptx::mma_ts_warp(tmem + L::col_o(i), tmem + L::col_p(i) + kk * 8, b + ((kk * 16 * 128) >> 4),
                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
@@ -611,7 +679,105 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       uint32_t it_base = 0;           // K/V ring position of this unit's K_0
       bool ok = true;
       Unit u;
-      for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+      if constexpr (L::kDecoupled) {
+        // Per key tile j: first the S GEMMs of key tile j+1 (each as soon as the
+        // softmax has read the tile's previous S), then the P V GEMMs of key tile j.
+        uint32_t s_iss[2] = {0, 0};   // S_i GEMMs issued so far (s_free phase)
+        for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+          const int nblk[2] = {u.nblk[0], u.nblk[1]};
+          const int nmax = u.nmax;
+          const int fst[2] = {0, kBand ? u.first[1] : 0};
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            if (ok && nblk[i] > 0)
+              ok = wait_warp(bar(L::kBarQFull + i), q_count[i] & 1, abort_flag, limit, kSiteMmaQ);
+          const int slot_k0 = it_base % L::kStages;
+          if (ok) ok = wait_warp(bar(L::kBarKVFull + slot_k0), (it_base / L::kStages) & 1,
+                                  abort_flag, limit, kSiteMmaK);
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (nblk[i] > 0 && fst[i] == 0) {   // S_i of the unit's first key tile
+              issue_s(i, slot_k0);
+              ptx::mma_commit_warp(bar(L::kBarSFull + i));
+              ++s_iss[i];
+              if (nblk[i] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));
+            }
+          }
+          ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k0));
+          for (int j = 0; j < nmax && ok; ++j) {
+            const uint32_t it_v = it_base + 2 * j + 1;
+            const int slot_v = it_v % L::kStages;
+            const uint32_t it_k = it_v + 1;
+            const int slot_k = it_k % L::kStages;
+            bool k_ready = false;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int t = j + 1 - fst[i];   // tile i's step that key tile j+1 is
+              if (t < 0 || t >= nblk[i]) continue;
+              if (t > 0) {   // S_i(t-1) must have left TMEM
+                if (!wait_warp(bar(L::kBarSFree + i), (s_iss[i] - 1) & 1, abort_flag, limit,
+                                kSiteMmaSFree)) {
+                  ok = false;
+                  break;
+                }
+              }
+              if (!k_ready) {
+                if (!wait_warp(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
+                                limit, kSiteMmaK)) {
+                  ok = false;
+                  break;
+                }
+                k_ready = true;
+              }
+              ptx::tc_fence_after();
+              issue_s(i, slot_k);
+              ptx::mma_commit_warp(bar(L::kBarSFull + i));
+              ++s_iss[i];
+              if (t == nblk[i] - 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));   // Q_i read for the last time
+            }
+            if (!ok) break;
+            if (k_ready) ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k));
+            if (!wait_warp(bar(L::kBarKVFull + slot_v), (it_v / L::kStages) & 1, abort_flag, limit,
+                            kSiteMmaV)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int jl = j - fst[i];
+              if (jl < 0 || jl >= nblk[i]) continue;
+              // The first P_i V MMA of a unit overwrites O_i: the previous epilogue must
+              // have read it.
+              if (jl == 0 && q_count[i] > 0 &&
+                  !wait_warp(bar(L::kBarOEmpty + i), (q_count[i] - 1) & 1, abort_flag, limit,
+                              kSiteMmaP)) {
+                ok = false;
+                break;
+              }
+              if (!wait_warp(bar(L::kBarPFull + i), (p_base[i] + jl) & 1, abort_flag, limit,
+                              kSiteMmaP)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              issue_pv(i, slot_v, jl > 0);
+              ptx::mma_commit_warp(bar(L::kBarPVDone + i));
+              if (jl == nblk[i] - 1) ptx::mma_commit_warp(bar(L::kBarOFull + i));
+            }
+            if (!ok) break;
+            ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_v));
+          }
+          it_base += 2 * nmax;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            p_base[i] += nblk[i];
+            if (nblk[i] > 0) ++q_count[i];
+          }
+        }
+      }
+      for (int r = 0; !L::kDecoupled && ok && unit_of<kS>(p, r, u); ++r) {
         const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
         const int nblk[2] = {nb0, nb1};
         // Step j of the unit (key tile kv0 + j) is step j - fst[i] of query tile i.
@@ -619,9 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (ok && nblk[i] > 0)
-            ok = wait_phase(bar(L::kBarQFull + i), q_count[i] & 1, abort_flag, limit, kSiteMmaQ);
+            ok = wait_warp(bar(L::kBarQFull + i), q_count[i] & 1, abort_flag, limit, kSiteMmaQ);
         const int slot_k0 = it_base % L::kStages;
-        if (ok) ok = wait_phase(bar(L::kBarKVFull + slot_k0), (it_base / L::kStages) & 1,
+        if (ok) ok = wait_warp(bar(L::kBarKVFull + slot_k0), (it_base / L::kStages) & 1,
                                 abort_flag, limit, kSiteMmaK);
         if (!ok) break;
         ptx::tc_fence_after();
@@ -629,22 +795,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         for (int i = 0; i < 2; ++i) {
           if (nblk[i] > 0 && fst[i] == 0) {
             issue_s(i, slot_k0);
-            ptx::mma_commit(bar(L::kBarSFull + i));
-            if (nblk[i] == 1) ptx::mma_commit(bar(L::kBarQEmpty + i));
+            ptx::mma_commit_warp(bar(L::kBarSFull + i));
+            if (nblk[i] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));
           }
         }
-        ptx::mma_commit(bar(L::kBarKVEmpty + slot_k0));
+        ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k0));
         // The first P_i V MMA of a unit overwrites O_i: the previous unit's epilogue
         // must have read it.
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (ok && nblk[i] > 0 && q_count[i] > 0)
-            ok = wait_phase(bar(L::kBarOEmpty + i), (q_count[i] - 1) & 1, abort_flag, limit,
+            ok = wait_warp(bar(L::kBarOEmpty + i), (q_count[i] - 1) & 1, abort_flag, limit,
                             kSiteMmaP);
         for (int j = 0; j < nmax && ok; ++j) {
           const uint32_t it_v = it_base + 2 * j + 1;
           const int slot_v = it_v % L::kStages;
-          if (!wait_phase(bar(L::kBarKVFull + slot_v), (it_v / L::kStages) & 1, abort_flag, limit,
+          if (!wait_warp(bar(L::kBarKVFull + slot_v), (it_v / L::kStages) & 1, abort_flag, limit,
                           kSiteMmaV)) {
             ok = false;
             break;
@@ -657,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           for (int i = 0; i < 2; ++i) {
             const int jl = j - fst[i];
             if (jl < 0 || jl >= nblk[i]) continue;
-            if (!wait_phase(bar(L::kBarPFull + i), (p_base[i] + jl) & 1, abort_flag, limit,
+            if (!wait_warp(bar(L::kBarPFull + i), (p_base[i] + jl) & 1, abort_flag, limit,
                             kSiteMmaP)) {
               ok = false;
               break;
@@ -665,12 +831,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             ptx::tc_fence_after();
             issue_pv(i, slot_v, jl > 0);
             if (jl == nblk[i] - 1) {
-              ptx::mma_commit(bar(L::kBarOFull + i));
-              if (nblk[i] > 1) ptx::mma_commit(bar(L::kBarQEmpty + i));   // Q_i no longer read
+              ptx::mma_commit_warp(bar(L::kBarOFull + i));
+              if (nblk[i] > 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));   // Q_i no longer read
             }
             if (jl + 1 < nblk[i]) {
               if (!k_ready) {
-                if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
+                if (!wait_warp(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
                                 limit, kSiteMmaK)) {
                   ok = false;
                   break;
@@ -679,14 +845,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 k_ready = true;
               }
               issue_s(i, slot_k);
-              ptx::mma_commit(bar(L::kBarSFull + i));
+              ptx::mma_commit_warp(bar(L::kBarSFull + i));
             }
           }
           if constexpr (kBand) {
             // A query tile whose band starts at the next key tile: its first S GEMM.
             if (ok && nblk[1] > 0 && fst[1] == j + 1) {
               if (!k_ready) {
-                if (!wait_phase(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
+                if (!wait_warp(bar(L::kBarKVFull + slot_k), (it_k / L::kStages) & 1, abort_flag,
                                 limit, kSiteMmaK)) {
                   ok = false;
                 } else {
@@ -696,14 +862,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               }
               if (ok) {
                 issue_s(1, slot_k);
-                ptx::mma_commit(bar(L::kBarSFull + 1));
-                if (nblk[1] == 1) ptx::mma_commit(bar(L::kBarQEmpty + 1));
+                ptx::mma_commit_warp(bar(L::kBarSFull + 1));
+                if (nblk[1] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + 1));
               }
             }
           }
           if (!ok) break;
-          ptx::mma_commit(bar(L::kBarKVEmpty + slot_v));
-          if (k_ready) ptx::mma_commit(bar(L::kBarKVEmpty + slot_k));
+          ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_v));
+          if (k_ready) ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k));
         }
         it_base += 2 * nmax;
 #pragma unroll
@@ -713,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
       }
       // Drain: every MMA issued has completed before TMEM is freed.
-      ptx::mma_commit(bar(L::kBarDrain));
+      ptx::mma_commit_warp(bar(L::kBarDrain));
       drain_phase(bar(L::kBarDrain), 0, limit);
     }
     __syncwarp();
