@@ -74,6 +74,10 @@ class OracleLib:
                                                 ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                                 ctypes.c_double, lp, ctypes.c_long, dp, dp, dp,
                                                 ctypes.c_int]
+        lib.oracle_attn_bwd_head.restype = ctypes.c_int
+        lib.oracle_attn_bwd_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                             ctypes.c_long, ctypes.c_int, ctypes.c_double,
+                                             dp, dp, dp, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self.lib = lib
@@ -147,6 +151,34 @@ class OracleLib:
                                                          scale, nthreads=nthreads)
         return O, L
 
+    def attn_bwd_head(self, q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
+        """Gradients (dQ, dK, dV) of one (batch, head) slice given dO = dLoss/dO."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        Lq, D = q.shape
+        Lk = k.shape[0]
+        if k.shape != (Lk, D) or v.shape != (Lk, D) or do.shape != (Lq, D):
+            raise ValueError("k, v must be [Lk, D] and do [Lq, D] with the same D as q")
+        dq = np.empty((Lq, D))
+        dk = np.empty((Lk, D))
+        dv = np.empty((Lk, D))
+        rc = self.lib.oracle_attn_bwd_head(_dptr(q), _dptr(k), _dptr(v), _dptr(do), Lq, Lk, D,
+                                           int(bool(causal)), float(scale), _dptr(dq), _dptr(dk),
+                                           _dptr(dv), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_head failed with code {rc}")
+        return dq, dk, dv
+
+    def attn_bwd_full(self, q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
+        """Gradients over contiguous [B, H, L, D] tensors: returns (dQ, dK, dV)."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        B, H = q.shape[:2]
+        dq, dk, dv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+        for b in range(B):
+            for h in range(H):
+                dq[b, h], dk[b, h], dv[b, h] = self.attn_bwd_head(q[b, h], k[b, h], v[b, h],
+                                                                  do[b, h], causal, scale, nthreads)
+        return dq, dk, dv
+
     def attn_full(self, q, k, v, causal: bool, scale: float, want_p: bool = False,
                   nthreads: int = 0):
         """Attention over contiguous [B, H, L, D] tensors: returns (O, LSE[, P])."""
@@ -194,3 +226,11 @@ def attn_head_window(*args, **kwargs):
 
 def attn_full_window(*args, **kwargs):
     return _get().attn_full_window(*args, **kwargs)
+
+
+def attn_bwd_head(*args, **kwargs):
+    return _get().attn_bwd_head(*args, **kwargs)
+
+
+def attn_bwd_full(*args, **kwargs):
+    return _get().attn_bwd_full(*args, **kwargs)

@@ -217,6 +217,93 @@ int oracle_attn_head_window(const double *Q, const double *K, const double *V,
     return status;
 }
 
+/*
+ * Gradients of the attention of one (batch, head) slice -- the backward pass that
+ * the "FlashAttention-2 forward in Triton" post (wsisp.com) leaves to later work
+ * and whose principle it states: recompute the probabilities rather than store
+ * them.  With the loss's gradient dO with respect to O given, the chain rule
+ * through O = P V, P = softmax_rows(S), S = scale Q K^T gives, per row i over its
+ * allowed keys j (the same keys as oracle_attn_head):
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)      (the softmax Jacobian)
+ *   dQ_i  = scale sum_j dS_ij K_j
+ *   dK_j  = scale sum_i dS_ij Q_i
+ * and 0 for every masked pair.  P and dS are materialised as [Lq, Lk] matrices
+ * in double precision; dQ is formed per row, dV and dK per key row.
+ *   Q, dO: [Lq, D]; K, V: [Lk, D]; dQ: [Lq, D]; dK, dV: [Lk, D] (all written).
+ * Returns ORACLE_OK, ORACLE_BAD_ARG or ORACLE_NO_MEMORY.
+ */
+int oracle_attn_bwd_head(const double *Q, const double *K, const double *V, const double *dO,
+                         long Lq, long Lk, long D, int causal, double scale,
+                         double *dQ, double *dK, double *dV, int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return ORACLE_BAD_ARG;
+    if (Lq < 0 || Lk < 1 || D < 1) return ORACLE_BAD_ARG;
+    double *P = (double *)malloc(sizeof(double) * (size_t)(Lq > 0 ? Lq : 1) * (size_t)Lk);
+    double *dS = (double *)malloc(sizeof(double) * (size_t)(Lq > 0 ? Lq : 1) * (size_t)Lk);
+    if (!P || !dS) {
+        free(P);
+        free(dS);
+        return ORACLE_NO_MEMORY;
+    }
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (long i = 0; i < Lq; ++i) {
+        const long n = allowed_keys(i, Lk, causal);
+        double *p = P + i * Lk, *ds = dS + i * Lk;
+        /* forward probabilities of row i, straight from the definition */
+        double m = -INFINITY;
+        for (long j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d) dot += Q[i * D + d] * K[j * D + d];
+            p[j] = scale * dot;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (long j = 0; j < n; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        for (long j = 0; j < n; ++j) p[j] /= l;
+        for (long j = n; j < Lk; ++j) p[j] = 0.0;
+        /* dP_ij = dO_i . V_j, and the row's sum of P dP */
+        double pdp = 0.0;
+        for (long j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d) dot += dO[i * D + d] * V[j * D + d];
+            ds[j] = dot;
+            pdp += p[j] * dot;
+        }
+        for (long j = 0; j < n; ++j) ds[j] = p[j] * (ds[j] - pdp);
+        for (long j = n; j < Lk; ++j) ds[j] = 0.0;
+        for (long d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (long j = 0; j < n; ++j) acc += ds[j] * K[j * D + d];
+            dQ[i * D + d] = scale * acc;
+        }
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (long j = 0; j < Lk; ++j) {
+        for (long d = 0; d < D; ++d) {
+            double av = 0.0, ak = 0.0;
+            for (long i = 0; i < Lq; ++i) {
+                av += P[i * Lk + j] * dO[i * D + d];
+                ak += dS[i * Lk + j] * Q[i * D + d];
+            }
+            dV[j * D + d] = av;
+            dK[j * D + d] = scale * ak;
+        }
+    }
+    free(P);
+    free(dS);
+    return ORACLE_OK;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int oracle_max_threads(void)
 {

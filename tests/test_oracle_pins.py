@@ -274,6 +274,68 @@ WINDOW_PINS = [pin_window_torch_f64, pin_window_uniform, pin_window_single_key, 
 PINS.extend(WINDOW_PINS)
 
 
+# --------------------------------------------------------------------------
+# Backward pass (gradients): pinned by central finite differences of the forward
+# oracle, which shares no arithmetic with the gradient formulas.
+# --------------------------------------------------------------------------
+
+def _fd_grads(lib, q, k, v, g, causal, scale, eps=1e-6):
+    def loss(**kw):
+        a = dict(q=q, k=k, v=v)
+        a.update(kw)
+        return float((lib.attn_head(a["q"], a["k"], a["v"], causal, scale)[0] * g).sum())
+    out = []
+    for name, x in (("q", q), ("k", k), ("v", v)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            fd[idx] = (loss(**{name: xp}) - loss(**{name: xm})) / (2 * eps)
+        out.append(fd)
+    return out
+
+
+def pin_bwd_finite_differences(lib):
+    """dQ, dK, dV equal the central differences of sum(G * O) to 1e-7."""
+    for (Lq, Lk, D, causal) in [(5, 6, 3, False), (5, 6, 3, True), (7, 4, 2, True), (3, 8, 4, False)]:
+        q, k, v = _rand((Lq, D), 70 + Lq, 1.5), _rand((Lk, D), 71 + Lk, 1.5), _rand((Lk, D), 72)
+        g = _rand((Lq, D), 73)
+        dq, dk, dv = lib.attn_bwd_head(q, k, v, g, causal, 0.7)
+        for got, fd in zip((dq, dk, dv), _fd_grads(lib, q, k, v, g, causal, 0.7)):
+            np.testing.assert_allclose(got, fd, rtol=0, atol=1e-7)
+
+
+def pin_bwd_constant_v(lib):
+    """Every value row equal: O does not depend on Q or K, so dQ = dK = 0."""
+    q, k = _rand((6, 4), 74), _rand((9, 4), 75)
+    v = np.tile(_rand((1, 4), 76), (9, 1))
+    for causal in (False, True):
+        dq, dk, _ = lib.attn_bwd_head(q, k, v, _rand((6, 4), 77), causal, 0.5)
+        assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
+
+
+def pin_bwd_sums(lib):
+    """Rows of P sum to 1 and rows of dS to 0: sum_j dV_j = sum_i dO_i, sum_j dK_j = 0."""
+    q, k, v, g = _rand((8, 5), 78), _rand((11, 5), 79), _rand((11, 5), 80), _rand((8, 5), 81)
+    for causal in (False, True):
+        dq, dk, dv = lib.attn_bwd_head(q, k, v, g, causal, 0.9)
+        np.testing.assert_allclose(dv.sum(axis=0), g.sum(axis=0), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dk.sum(axis=0), 0.0, rtol=0, atol=1e-12)
+
+
+def pin_bwd_single_key(lib):
+    """Lk = 1: P = 1, so dV_0 = sum_i dO_i and dQ = dK = 0."""
+    q, k, v, g = _rand((5, 3), 82), _rand((1, 3), 83), _rand((1, 3), 84), _rand((5, 3), 85)
+    dq, dk, dv = lib.attn_bwd_head(q, k, v, g, False, 1.0)
+    np.testing.assert_allclose(dv[0], g.sum(axis=0), rtol=0, atol=1e-12)
+    assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_constant_v, pin_bwd_sums, pin_bwd_single_key]
+PINS.extend(BWD_PINS)
+
+
 def test_window_rejects_empty_rows(oracle_mod):
     q, k, v = _rand((5, 4), 1), _rand((3, 4), 2), _rand((3, 4), 3)
     with pytest.raises(ValueError):   # row 4 would need key 4 >= Lk
@@ -309,6 +371,9 @@ MUTATIONS = {
     "causal_ignored": ("if (!causal) return Lk;", "return Lk;"),
     "window_drops_last_key": ("attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo + 1, D, hi - lo + 1, scale,",
                               "attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo, D, hi - lo, scale,"),
+    "bwd_softmax_jacobian_without_row_term": ("ds[j] = p[j] * (ds[j] - pdp);", "ds[j] = p[j] * ds[j];"),
+    "bwd_dk_missing_scale": ("dK[j * D + d] = scale * ak;", "dK[j * D + d] = ak;"),
+    "bwd_dv_from_queries": ("av += P[i * Lk + j] * dO[i * D + d];", "av += P[i * Lk + j] * Q[i * D + d];"),
     "window_shifted_values": ("attend_row(Q + i * D, K + lo * D, V + lo * D,", "attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
 }
 
