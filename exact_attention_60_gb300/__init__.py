@@ -8,8 +8,9 @@ from __future__ import annotations
 import math
 
 from ._native import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
-                      FA_OK, fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_window,
-                      fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status, fa_status_string)
+                      FA_OK, fa_bwd, fa_bwd_workspace_size, fa_debug_set, fa_fwd, fa_fwd_noalloc,
+                      fa_fwd_window, fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status,
+                      fa_status_string)
 
 
 class FaError(RuntimeError):
@@ -77,6 +78,63 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     if st != FA_OK:
         raise FaError(st)
     return out, lse
+
+
+_bwd_workspaces = {}
+
+
+def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+                       dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of ``attention`` given its inputs, its outputs ``o``/``lse`` and
+    ``do`` = dLoss/dO (contiguous bf16 / fp32 CUDA tensors of the forward's shapes).
+    Allocates the gradients if not given; uses a cached per-device workspace, so calls
+    on one device must be ordered on one stream."""
+    import torch
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    for t in (q, k, v, o, do):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st, nbytes = fa_bwd_workspace_size(B, H, Lq, Lk, D, causal)
+    if st != FA_OK:
+        raise FaError(st)
+    key = (torch.device(q.device).index, )
+    ws = _bwd_workspaces.get(key)
+    if ws is None or ws.numel() < max(nbytes, 256):
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+        _bwd_workspaces[key] = ws
+    st = fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Lq, Lk, D, causal, scale, ws, ws.numel(),
+                stream)
+    if st != FA_OK:
+        raise FaError(st)
+    return dq, dk, dv
+
+
+def flash_attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """Differentiable exact attention: ``attention`` forward, ``attention_backward``
+    for the gradients (torch.autograd glue only)."""
+    import torch
+
+    class _Fn(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v):
+            o, lse = attention(q, k, v, causal=causal, scale=scale)
+            ctx.save_for_backward(q, k, v, o, lse)
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            return attention_backward(q, k, v, o, lse, do.contiguous(), causal=causal, scale=scale)
+
+    return _Fn.apply(q, k, v)
 
 
 def attention_from_host(q, k, v, causal: bool = False, scale: float | None = None, out=None,

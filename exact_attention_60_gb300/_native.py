@@ -19,7 +19,8 @@ FA_ERR_TIMEOUT = 4
 
 # Every symbol include/fa.h declares.
 EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_noalloc",
-            "fa_status_string", "fa_last_device_status", "fa_debug_set")
+            "fa_bwd_workspace_size", "fa_bwd", "fa_status_string", "fa_last_device_status",
+            "fa_debug_set")
 
 _lib = None
 
@@ -48,6 +49,10 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_int
+    lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = [vp] * 9 + [ctypes.c_int] * 6 + [ctypes.c_float, vp, ctypes.c_size_t, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_last_device_status.restype = ctypes.c_int
@@ -113,6 +118,23 @@ def fa_fwd_noalloc(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, stream=None)
     return load().fa_fwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
                                  int(Lq), int(Lk), int(D), int(bool(causal)), float(scale),
                                  _stream(stream))
+
+
+def fa_bwd_workspace_size(B, H, Lq, Lk, D, causal):
+    """C ``fa_bwd_workspace_size``: returns (status, bytes)."""
+    n = ctypes.c_size_t(0)
+    st = load().fa_bwd_workspace_size(int(B), int(H), int(Lq), int(Lk), int(D),
+                                      int(bool(causal)), ctypes.byref(n))
+    return st, int(n.value)
+
+
+def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Lq, Lk, D, causal, scale, workspace,
+           workspace_bytes, stream=None) -> int:
+    """C ``fa_bwd``: gradients dQ, dK, dV of the forward attention given dO."""
+    return load().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                         _ptr(dK), _ptr(dV), int(B), int(H), int(Lq), int(Lk), int(D),
+                         int(bool(causal)), float(scale), _ptr(workspace), int(workspace_bytes),
+                         _stream(stream))
 
 
 def fa_status_string(status: int) -> str:

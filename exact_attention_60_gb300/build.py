@@ -1,8 +1,8 @@
 """Build step for the CUDA library ``libfa.so`` (nvcc, sm_103a only).
 
 The library is built in-tree next to this file so the tests and the benchmark
-load the copy compiled from this checkout.  One translation unit, one
-``-gencode``: a build takes a few seconds.
+load the copy compiled from this checkout.  Two translation units (forward and
+backward), one ``-gencode``: a build takes a few seconds.
 """
 from __future__ import annotations
 
@@ -14,8 +14,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = [os.path.join(CSRC, "fa_fwd.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "sm103_ptx.cuh"), os.path.join(INCLUDE, "fa.h")]
+SOURCES = [os.path.join(CSRC, "fa_fwd.cu"), os.path.join(CSRC, "fa_bwd.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "sm103_ptx.cuh"), os.path.join(CSRC, "fa_internal.h"),
+                  os.path.join(INCLUDE, "fa.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -1,0 +1,1024 @@
+// fa_bwd.cu -- FlashAttention-2 backward for GB300 (sm_103a), and its C ABI.
+//
+// What is computed (per batch b, head h), given Q, K, V, the forward output O, its
+// row statistic LSE and the loss gradient dO:
+//   P_ij  = exp(scale * Q_i.K_j - LSE_i)          (recomputed, never stored)
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = dO_i . V_j
+//   dS_ij = P_ij (dP_ij - Delta_i),  Delta_i = dO_i . O_i  (= sum_j P_ij dP_ij)
+//   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
+// over the allowed pairs (all j < Lk, or j <= i when causal).  The principle --
+// keep the per-row statistic from the forward pass and recompute P from it
+// instead of storing the score matrix -- is the one the wsisp.com post
+// "FlashAttention-2 forward in Triton" states for the backward pass, which it
+// leaves to later work; the formulas are the chain rule through O = P V, the row
+// softmax and S = scale Q K^T.
+//
+// Three kernels on one stream:
+//   fa_bwd_delta_kernel : Delta = rowsum(dO * O), fp32, memory-bound.
+//   fa_bwd_dkdv_kernel  : one unit = one 128-key tile of one head; streams the
+//                         query tiles that see it.  TMEM: S^T | dP^T | dV | dK.
+//                           S^T  = K Q^T,  dP^T = V dO^T        (A, B in smem)
+//                           dV  += P^T dO, dK  += dS^T Q        (A = P^T / dS^T in TMEM)
+//                         One warpgroup (thread = key row) turns S^T into P^T
+//                         (bf16, over S^T) and dP^T into dS^T (bf16, over dP^T).
+//   fa_bwd_dq_kernel    : one unit = one 128-query tile; streams its key tiles.
+//                         TMEM: S | dP | dQ.  S = Q K^T, dP = dO V^T, dQ += dS K.
+// Splitting dQ from dK/dV costs two extra GEMMs per tile pair but needs no
+// atomics and no dQ accumulator in global memory.  Roles per CTA (192 threads):
+// warps 0-3 compute warpgroup, warp 4 TMA loads, warp 5 MMA issue (the whole warp
+// runs the loop; one elected lane issues each tcgen05.mma / commit).  Every wait
+// is bounded in time; a wait that runs out records FA_ERR_TIMEOUT in this file's
+// status word (read by fa_last_device_status) and every role drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fab {
+
+namespace ptx = fa::ptx;
+
+__device__ unsigned int g_bwd_status;
+
+constexpr int kBlk = 128;          // rows per tile (queries or keys), one M=128 MMA
+constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Site : uint32_t { kSiteLoad = 1, kSiteMma = 2, kSiteCompute = 3, kSiteEpilogue = 4 };
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned long long limit_ns, uint32_t site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicCAS(&g_bwd_status, 0u, static_cast<unsigned>(FA_ERR_TIMEOUT) | (site << 8));
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns, uint32_t site) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, limit_ns, site));
+}
+
+__device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major or (b_mn_major) MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Shared-memory descriptor of a 128B-swizzled operand (see the forward kernel).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+struct BwdParams {
+  CUtensorMap tm_q;    // 3-D views [B*H][L][D], box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const float* lse;    // [B*H][Lq] natural log
+  const float* delta;  // [B*H][Lq] rowsum(dO * O)
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int bh_count;
+  int Lq;
+  int Lk;
+  int causal;
+  int nq;              // query tiles: ceil(Lq / 128)
+  int nk;              // key tiles:   ceil(Lk / 128)
+  int n_units;
+  float scale;
+  float scale_log2;    // scale * log2(e)
+  unsigned long long wait_limit_ns;
+};
+
+template <int HD>
+struct Tiles {
+  static constexpr int kTileBytes = kBlk * HD * 2;   // one 128 x HD bf16 tile
+  static constexpr int kRegionBytes = kBlk * 128;    // 128 rows x 64 bf16: one swizzle column
+  static constexpr int kRegions = HD / 64;
+};
+
+// Row tiles a unit streams: dK/dV units (key tile kt) see query tiles [q_first, nq);
+// dQ units (query tile qt) see key tiles [0, k_count).
+__device__ __forceinline__ int dkdv_first_q(const BwdParams& p, int kt) {
+  return p.causal ? kt : 0;   // causal: query q >= key k, so query tiles from the key tile's index
+}
+__device__ __forceinline__ int dq_key_tiles(const BwdParams& p, int qt) {
+  return p.causal ? min(p.nk, qt + 1) : p.nk;
+}
+
+// Unit r of this CTA (boustrophedon over the grid), heaviest first.
+__device__ __forceinline__ bool unit_index(const BwdParams& p, int r, int& idx) {
+  const int G = static_cast<int>(gridDim.x), g = static_cast<int>(blockIdx.x);
+  idx = r * G + ((r & 1) ? (G - 1 - g) : g);
+  return idx < p.n_units;
+}
+__device__ __forceinline__ void dkdv_unit(const BwdParams& p, int idx, int& bh, int& kt) {
+  if (p.causal) {   // the first key tiles are seen by the most query tiles
+    kt = idx / p.bh_count;
+    bh = idx % p.bh_count;
+  } else {          // a head's tiles run together and share its query tiles in L2
+    bh = idx / p.nk;
+    kt = idx % p.nk;
+  }
+}
+__device__ __forceinline__ void dq_unit(const BwdParams& p, int idx, int& bh, int& qt) {
+  if (p.causal) {   // the last query tiles see the most key tiles
+    qt = p.nq - 1 - idx / p.bh_count;
+    bh = idx % p.bh_count;
+  } else {
+    bh = idx / p.nq;
+    qt = idx % p.nq;
+  }
+}
+
+// ------------------------------------------------------------------ Delta = rowsum(dO * O)
+template <int HD>
+__global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __nv_bfloat16* __restrict__ O,
+                                                           const __nv_bfloat16* __restrict__ dO,
+                                                           float* __restrict__ delta,
+                                                           long long rows) {
+  constexpr int kT = HD / 8;   // threads per row, 8 elements (16 bytes) each
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = tid / kT;
+  const int part = static_cast<int>(tid % kT);
+  float acc = 0.0f;
+  if (row < rows) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + row * HD) + part);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + row * HD) + part);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = ptx::unpack_bf16x2(av[e]), y = ptx::unpack_bf16x2(bv[e]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = kT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (part == 0 && row < rows) delta[row] = acc;
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int HD>
+struct DkdvLayout {
+  using T = Tiles<HD>;
+  static constexpr int kStages = (HD == 128) ? 2 : 4;           // (Q, dO, LSE, Delta) ring
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = T::kTileBytes;
+  static constexpr int kOffStage = 2 * T::kTileBytes;
+  static constexpr int kStageBytes = 2 * T::kTileBytes + 1024;   // Q | dO | lse2[128] | delta[128]
+  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  static constexpr int kBarKvFull = 0, kBarKvEmpty = 1;
+  static constexpr int kBarQdFull = 2;                          // [kStages]
+  static constexpr int kBarQdEmpty = kBarQdFull + kStages;      // [kStages]
+  static constexpr int kBarSFull = kBarQdEmpty + kStages;
+  static constexpr int kBarDpFull = kBarSFull + 1;
+  static constexpr int kBarPFull = kBarDpFull + 1;              // count 128
+  static constexpr int kBarDsFull = kBarPFull + 1;              // count 128
+  static constexpr int kBarAccFull = kBarDsFull + 1;
+  static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 128
+  static constexpr int kBarDrain = kBarAccEmpty + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffAbort = kOffBar + kNumBars * 8;
+  static constexpr int kOffTmemSlot = kOffAbort + 4;
+  static constexpr int kBytes = kOffTmemSlot + 4;
+  static constexpr int kAlloc = kBytes + 1024;
+  // TMEM columns: S^T | dP^T | dV | dK (P^T and dS^T as bf16 over the first 64 columns of S^T / dP^T)
+  static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 256 + HD;
+  static constexpr uint32_t kTmemCols = 512;
+};
+static_assert(DkdvLayout<128>::kAlloc <= 232448, "dK/dV shared memory (D=128)");
+static_assert(DkdvLayout<64>::kAlloc <= 232448, "dK/dV shared memory (D=64)");
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using L = DkdvLayout<HD>;
+  using T = Tiles<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_addr(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
+  auto stage_off = [&](int s) -> uint32_t { return L::kOffStage + s * L::kStageBytes; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(L::kBarKvFull), 1);
+    ptx::mbar_init(bar(L::kBarKvEmpty), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(L::kBarQdFull + s), 1 + 32);   // the TMA arrive + every load lane
+      ptx::mbar_init(bar(L::kBarQdEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(L::kBarSFull), 1);
+    ptx::mbar_init(bar(L::kBarDpFull), 1);
+    ptx::mbar_init(bar(L::kBarPFull), 128);
+    ptx::mbar_init(bar(L::kBarDsFull), 128);
+    ptx::mbar_init(bar(L::kBarAccFull), 1);
+    ptx::mbar_init(bar(L::kBarAccEmpty), 128);
+    ptx::mbar_init(bar(L::kBarDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const unsigned long long limit = p.wait_limit_ns;
+
+  if (warp < 4) {
+    // ------------------------------------------------ compute warpgroup: thread = key row
+    const int row = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::kColS;
+    const uint32_t t_dp = tmem + lane_off + L::kColDp;
+    const float sl2 = p.scale_log2;
+    uint32_t it = 0;          // query tiles processed (s_full, dp_full phases; ring position)
+    uint32_t acc_count = 0;   // units whose accumulators were read
+    bool ok = true;
+    int idx;
+    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+      int bh, kt;
+      dkdv_unit(p, idx, bh, kt);
+      const int q_first = dkdv_first_q(p, kt);
+      const int n = max(0, p.nq - q_first);
+      const int k = kt * kBlk + row;   // this thread's key
+      const size_t orow = (static_cast<size_t>(bh) * p.Lk + (k < p.Lk ? k : 0)) * HD;
+      if (n == 0) {   // no query sees these keys: their gradients are zero
+        if (k < p.Lk) {
+          for (int c = 0; c < HD; c += 8) {
+            *reinterpret_cast<uint4*>(p.dv + orow + c) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(p.dk + orow + c) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      for (int t = 0; t < n; ++t, ++it) {
+        const int qt = q_first + t;
+        const int s = static_cast<int>(it % L::kStages);
+        const float* lse2 = reinterpret_cast<const float*>(smem + stage_off(s) + 2 * T::kTileBytes);
+        const float* dlt = lse2 + kBlk;
+        // the stage's LSE and Delta were written by the load warp's lanes: wait for them
+        // directly (and for S^T, which the MMA warp commits)
+        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarQdFull + s), (it / L::kStages) & 1, abort_flag,
+                                                limit, kSiteCompute) &&
+                                         wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[128];
+        ptx::tmem_ld32x32b_x128(t_s, sr);
+        // P^T_kq = exp2(sl2 * S - lse_q * log2e); padded queries carry lse2 = +inf (P = 0)
+        float pr[128];
+        const bool diag = p.causal && qt == kt;   // causal: query q >= key k
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2[c]));
+          pr[c] = (diag && c < row) ? 0.0f : x;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(pr[64 * h + 2 * c], pr[64 * h + 2 * c + 1]);
+          ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarPFull));
+        // dS^T_kq = P^T_kq (dP^T_kq - Delta_q), in four 32-column chunks; each chunk's bf16
+        // result lands in columns already read.
+        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t d[32];
+          ptx::tmem_ld32x32b_x32(t_dp + c0, d);
+          uint32_t q16[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float a = pr[c0 + 2 * c] * (__uint_as_float(d[2 * c]) - dlt[c0 + 2 * c]);
+            const float b = pr[c0 + 2 * c + 1] * (__uint_as_float(d[2 * c + 1]) - dlt[c0 + 2 * c + 1]);
+            q16[c] = ptx::pack_bf16x2(a, b);
+          }
+          ptx::tmem_st32x32b_x16(t_dp + c0 / 2, q16);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarDsFull));
+      }
+      if (!ok) break;
+      // Epilogue: dV and scale * dK of this thread's key row.
+      ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarAccFull), acc_count & 1, abort_flag, limit, kSiteEpilogue));
+      if (!ok) break;
+      ++acc_count;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t t_acc = tmem + lane_off + (which ? L::kColDk : L::kColDv);
+        const float mul = which ? p.scale : 1.0f;
+        __nv_bfloat16* dst = (which ? p.dk : p.dv) + orow;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t a[32];
+          ptx::tmem_ld32x32b_x32(t_acc + c0, a);
+          uint32_t pk16[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk16[c] = ptx::pack_bf16x2(__uint_as_float(a[2 * c]) * mul, __uint_as_float(a[2 * c + 1]) * mul);
+          if (k < p.Lk) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(dst + c0)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::kBarAccEmpty));
+    }
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------ load warp
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&p.tm_q);
+      ptx::prefetch_tensormap(&p.tm_k);
+      ptx::prefetch_tensormap(&p.tm_v);
+      ptx::prefetch_tensormap(&p.tm_do);
+    }
+    uint32_t it = 0, units = 0;
+    int last_fill[L::kStages];
+    for (int s = 0; s < L::kStages; ++s) last_fill[s] = -1;
+    bool ok = true;
+    int idx;
+    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+      int bh, kt;
+      dkdv_unit(p, idx, bh, kt);
+      const int q_first = dkdv_first_q(p, kt);
+      const int n = max(0, p.nq - q_first);
+      if (units > 0) {
+        ok = wait_warp(bar(L::kBarKvEmpty), (units - 1) & 1, abort_flag, limit, kSiteLoad);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(L::kBarKvFull), 2 * T::kTileBytes);
+        for (int rg = 0; rg < T::kRegions; ++rg) {
+          ptx::tma_load_3d(sbase + L::kOffK + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
+          ptx::tma_load_3d(sbase + L::kOffV + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
+        }
+      }
+      ++units;
+      for (int t = 0; t < n; ++t, ++it) {
+        const int qt = q_first + t;
+        const int s = static_cast<int>(it % L::kStages);
+        ok = wait_warp(bar(L::kBarQdEmpty + s), ((it / L::kStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
+        if (!ok) break;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(bar(L::kBarQdFull + s), 2 * T::kTileBytes);
+          for (int rg = 0; rg < T::kRegions; ++rg) {
+            ptx::tma_load_3d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, bar(L::kBarQdFull + s), 64 * rg, qt * kBlk, bh);
+            ptx::tma_load_3d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, bar(L::kBarQdFull + s), 64 * rg, qt * kBlk, bh);
+          }
+        }
+        last_fill[s] = static_cast<int>(it);
+        float* lse2 = reinterpret_cast<float*>(smem + stage_off(s) + 2 * T::kTileBytes);
+        float* dlt = lse2 + kBlk;
+        for (int c = lane; c < kBlk; c += 32) {
+          const int q = qt * kBlk + c;
+          const size_t gi = static_cast<size_t>(bh) * p.Lq + q;
+          lse2[c] = (q < p.Lq) ? p.lse[gi] * kLog2e : INFINITY;
+          dlt[c] = (q < p.Lq) ? p.delta[gi] : 0.0f;
+        }
+        ptx::mbar_arrive(bar(L::kBarQdFull + s));
+      }
+    }
+    // Drain: every copy this warp started has landed before the CTA exits.
+    if (units > 0) drain_phase(bar(L::kBarKvFull), (units - 1) & 1, limit);
+    for (int s = 0; s < L::kStages; ++s)
+      if (last_fill[s] >= 0) drain_phase(bar(L::kBarQdFull + s), (last_fill[s] / L::kStages) & 1, limit);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------ MMA warp (warp-uniform, elected issue)
+    constexpr uint32_t kIdescS = make_idesc(kBlk, kBlk, false);   // S^T, dP^T: 128 x 128, K = HD
+    constexpr uint32_t kIdescAcc = make_idesc(kBlk, HD, true);    // dV, dK: 128 x HD, K = 128 queries
+    const uint64_t desc_k = sw128_desc(sbase + L::kOffK, 16, 1024);
+    const uint64_t desc_v = sw128_desc(sbase + L::kOffV, 16, 1024);
+    auto kmaj = [&](uint32_t off) { return sw128_desc(sbase + off, 16, 1024); };
+    auto mnmaj = [&](uint32_t off) { return sw128_desc(sbase + off, T::kRegionBytes, 1024); };
+    // X^T = A B^T with A (keys) and B (queries) both K-major over HD.
+    auto issue_rows = [&](uint32_t d_col, uint64_t a, uint64_t b) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * T::kRegionBytes + (kk & 3) * 32) >> 4;
+        ptx::mma_ss_warp(tmem + d_col, a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    // acc (+)= X^T B, X^T (bf16) in TMEM columns a_col, B MN-major [128 queries x HD].
+    auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint64_t b, bool accumulate) {
+#pragma unroll
+      for (int kk = 0; kk < kBlk / 16; ++kk)
+        ptx::mma_ts_warp(tmem + d_col, tmem + a_col + kk * 8, b + ((kk * 16 * 128) >> 4), kIdescAcc,
+                         (accumulate || kk > 0) ? 1u : 0u);
+    };
+    uint32_t it = 0, units = 0, acc_units = 0;
+    bool ok = true;
+    int idx;
+    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+      int bh, kt;
+      dkdv_unit(p, idx, bh, kt);
+      const int n = max(0, p.nq - dkdv_first_q(p, kt));
+      ok = wait_warp(bar(L::kBarKvFull), units & 1, abort_flag, limit, kSiteMma);
+      if (!ok) break;
+      ++units;
+      if (n == 0) {   // nothing reads K, V: release them
+        ptx::mma_commit_warp(bar(L::kBarKvEmpty));
+        continue;
+      }
+      ptx::tc_fence_after();
+      {
+        const int s0 = static_cast<int>(it % L::kStages);
+        ok = wait_warp(bar(L::kBarQdFull + s0), (it / L::kStages) & 1, abort_flag, limit, kSiteMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_rows(L::kColS, desc_k, kmaj(stage_off(s0)));
+        ptx::mma_commit_warp(bar(L::kBarSFull));
+        issue_rows(L::kColDp, desc_v, kmaj(stage_off(s0) + T::kTileBytes));
+        ptx::mma_commit_warp(bar(L::kBarDpFull));
+      }
+      for (int t = 0; t < n && ok; ++t, ++it) {
+        const int s = static_cast<int>(it % L::kStages);
+        const int s1 = static_cast<int>((it + 1) % L::kStages);
+        if (t == 0 && acc_units > 0) {   // the previous unit's epilogue has read dV, dK
+          ok = wait_warp(bar(L::kBarAccEmpty), (acc_units - 1) & 1, abort_flag, limit, kSiteMma);
+          if (!ok) break;
+        }
+        ok = wait_warp(bar(L::kBarPFull), it & 1, abort_flag, limit, kSiteMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_acc(L::kColDv, L::kColS, mnmaj(stage_off(s) + T::kTileBytes), t > 0);   // dV += P^T dO
+        if (t + 1 < n) {   // next S^T overwrites P^T: issued after the MMA that reads it
+          ok = wait_warp(bar(L::kBarQdFull + s1), ((it + 1) / L::kStages) & 1, abort_flag, limit, kSiteMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_rows(L::kColS, desc_k, kmaj(stage_off(s1)));
+          ptx::mma_commit_warp(bar(L::kBarSFull));
+        }
+        ok = wait_warp(bar(L::kBarDsFull), it & 1, abort_flag, limit, kSiteMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_acc(L::kColDk, L::kColDp, mnmaj(stage_off(s)), t > 0);                   // dK += dS^T Q
+        ptx::mma_commit_warp(bar(L::kBarQdEmpty + s));   // Q, dO (and LSE, Delta) of stage s read
+        if (t + 1 < n) {
+          issue_rows(L::kColDp, desc_v, kmaj(stage_off(s1) + T::kTileBytes));
+          ptx::mma_commit_warp(bar(L::kBarDpFull));
+        }
+      }
+      if (!ok) break;
+      ptx::mma_commit_warp(bar(L::kBarAccFull));
+      ptx::mma_commit_warp(bar(L::kBarKvEmpty));
+      ++acc_units;
+    }
+    ptx::mma_commit_warp(bar(L::kBarDrain));
+    drain_phase(bar(L::kBarDrain), 0, limit);
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int HD>
+struct DqLayout {
+  using T = Tiles<HD>;
+  static constexpr int kStages = (HD == 128) ? 2 : 4;           // (K, V) ring
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDo = T::kTileBytes;
+  static constexpr int kOffStage = 2 * T::kTileBytes;
+  static constexpr int kStageBytes = 2 * T::kTileBytes;          // K | V
+  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  static constexpr int kBarQdFull = 0, kBarQdEmpty = 1;
+  static constexpr int kBarKvFull = 2;                          // [kStages]
+  static constexpr int kBarKvEmpty = kBarKvFull + kStages;      // [kStages]
+  static constexpr int kBarSFull = kBarKvEmpty + kStages;
+  static constexpr int kBarSFree = kBarSFull + 1;               // count 128
+  static constexpr int kBarDpFull = kBarSFree + 1;
+  static constexpr int kBarDsFull = kBarDpFull + 1;             // count 128
+  static constexpr int kBarAccFull = kBarDsFull + 1;
+  static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 128
+  static constexpr int kBarDrain = kBarAccEmpty + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffAbort = kOffBar + kNumBars * 8;
+  static constexpr int kOffTmemSlot = kOffAbort + 4;
+  static constexpr int kBytes = kOffTmemSlot + 4;
+  static constexpr int kAlloc = kBytes + 1024;
+  // TMEM columns: S | dP | dQ (dS as bf16 over the first 64 columns of dP)
+  static constexpr uint32_t kColS = 0, kColDp = 128, kColDq = 256;
+  static constexpr uint32_t kTmemCols = 512;
+};
+static_assert(DqLayout<128>::kAlloc <= 232448, "dQ shared memory (D=128)");
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using L = DqLayout<HD>;
+  using T = Tiles<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_addr(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
+  auto stage_off = [&](int s) -> uint32_t { return L::kOffStage + s * L::kStageBytes; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(L::kBarQdFull), 1);
+    ptx::mbar_init(bar(L::kBarQdEmpty), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(L::kBarKvFull + s), 1);
+      ptx::mbar_init(bar(L::kBarKvEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(L::kBarSFull), 1);
+    ptx::mbar_init(bar(L::kBarSFree), 128);
+    ptx::mbar_init(bar(L::kBarDpFull), 1);
+    ptx::mbar_init(bar(L::kBarDsFull), 128);
+    ptx::mbar_init(bar(L::kBarAccFull), 1);
+    ptx::mbar_init(bar(L::kBarAccEmpty), 128);
+    ptx::mbar_init(bar(L::kBarDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const unsigned long long limit = p.wait_limit_ns;
+
+  if (warp < 4) {
+    // ------------------------------------------------ compute warpgroup: thread = query row
+    const int row = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::kColS;
+    const uint32_t t_dp = tmem + lane_off + L::kColDp;
+    const float sl2 = p.scale_log2;
+    uint32_t it = 0, acc_count = 0;
+    bool ok = true;
+    int idx;
+    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+      int bh, qt;
+      dq_unit(p, idx, bh, qt);
+      const int n = dq_key_tiles(p, qt);
+      const int q = qt * kBlk + row;   // this thread's query
+      const bool valid = q < p.Lq;
+      const size_t gi = static_cast<size_t>(bh) * p.Lq + (valid ? q : 0);
+      const float lse2 = valid ? p.lse[gi] * kLog2e : 0.0f;
+      const float dlt = valid ? p.delta[gi] : 0.0f;
+      // keys k allowed for this row: k < key_lim
+      const int key_lim = p.causal ? min(p.Lk, q + 1) : p.Lk;
+      for (int t = 0; t < n; ++t, ++it) {
+        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[128];
+        ptx::tmem_ld32x32b_x128(t_s, sr);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarSFree));   // S is in registers: the next S may overwrite it
+        const int lim = key_lim - t * kBlk;    // columns c < lim are allowed keys
+        float pr[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+          pr[c] = (c < lim) ? x : 0.0f;
+        }
+        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t d[32];
+          ptx::tmem_ld32x32b_x32(t_dp + c0, d);
+          uint32_t q16[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            q16[c] = ptx::pack_bf16x2(pr[c0 + 2 * c] * (__uint_as_float(d[2 * c]) - dlt),
+                                      pr[c0 + 2 * c + 1] * (__uint_as_float(d[2 * c + 1]) - dlt));
+          ptx::tmem_st32x32b_x16(t_dp + c0 / 2, q16);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarDsFull));
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarAccFull), acc_count & 1, abort_flag, limit, kSiteEpilogue));
+      if (!ok) break;
+      ++acc_count;
+      ptx::tc_fence_after();
+      __nv_bfloat16* dst = p.dq + gi * HD;
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t a[32];
+        ptx::tmem_ld32x32b_x32(tmem + lane_off + L::kColDq + c0, a);
+        uint32_t pk16[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk16[c] = ptx::pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale, __uint_as_float(a[2 * c + 1]) * p.scale);
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            reinterpret_cast<uint4*>(dst + c0)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::kBarAccEmpty));
+    }
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------ load warp
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&p.tm_q);
+      ptx::prefetch_tensormap(&p.tm_k);
+      ptx::prefetch_tensormap(&p.tm_v);
+      ptx::prefetch_tensormap(&p.tm_do);
+    }
+    uint32_t it = 0, units = 0;
+    int last_fill[L::kStages];
+    for (int s = 0; s < L::kStages; ++s) last_fill[s] = -1;
+    bool ok = true;
+    int idx;
+    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+      int bh, qt;
+      dq_unit(p, idx, bh, qt);
+      const int n = dq_key_tiles(p, qt);
+      if (units > 0) {
+        ok = wait_warp(bar(L::kBarQdEmpty), (units - 1) & 1, abort_flag, limit, kSiteLoad);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(L::kBarQdFull), 2 * T::kTileBytes);
+        for (int rg = 0; rg < T::kRegions; ++rg) {
+          ptx::tma_load_3d(sbase + L::kOffQ + rg * T::kRegionBytes, &p.tm_q, bar(L::kBarQdFull), 64 * rg, qt * kBlk, bh);
+          ptx::tma_load_3d(sbase + L::kOffDo + rg * T::kRegionBytes, &p.tm_do, bar(L::kBarQdFull), 64 * rg, qt * kBlk, bh);
+        }
+      }
+      ++units;
+      for (int t = 0; t < n; ++t, ++it) {
+        const int s = static_cast<int>(it % L::kStages);
+        ok = wait_warp(bar(L::kBarKvEmpty + s), ((it / L::kStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
+        if (!ok) break;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(bar(L::kBarKvFull + s), 2 * T::kTileBytes);
+          for (int rg = 0; rg < T::kRegions; ++rg) {
+            ptx::tma_load_3d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKvFull + s), 64 * rg, t * kBlk, bh);
+            ptx::tma_load_3d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull + s), 64 * rg, t * kBlk, bh);
+          }
+        }
+        last_fill[s] = static_cast<int>(it);
+      }
+    }
+    if (lane == 0) {
+      if (units > 0) drain_phase(bar(L::kBarQdFull), (units - 1) & 1, limit);
+      for (int s = 0; s < L::kStages; ++s)
+        if (last_fill[s] >= 0) drain_phase(bar(L::kBarKvFull + s), (last_fill[s] / L::kStages) & 1, limit);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------ MMA warp (warp-uniform, elected issue)
+    constexpr uint32_t kIdescS = make_idesc(kBlk, kBlk, false);
+    constexpr uint32_t kIdescAcc = make_idesc(kBlk, HD, true);
+    const uint64_t desc_q = sw128_desc(sbase + L::kOffQ, 16, 1024);
+    const uint64_t desc_do = sw128_desc(sbase + L::kOffDo, 16, 1024);
+    auto kmaj = [&](uint32_t off) { return sw128_desc(sbase + off, 16, 1024); };
+    auto mnmaj = [&](uint32_t off) { return sw128_desc(sbase + off, T::kRegionBytes, 1024); };
+    auto issue_rows = [&](uint32_t d_col, uint64_t a, uint64_t b) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * T::kRegionBytes + (kk & 3) * 32) >> 4;
+        ptx::mma_ss_warp(tmem + d_col, a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_acc = [&](uint64_t b, bool accumulate) {   // dQ (+)= dS K
+#pragma unroll
+      for (int kk = 0; kk < kBlk / 16; ++kk)
+        ptx::mma_ts_warp(tmem + L::kColDq, tmem + L::kColDp + kk * 8, b + ((kk * 16 * 128) >> 4), kIdescAcc,
+                         (accumulate || kk > 0) ? 1u : 0u);
+    };
+    uint32_t it = 0, units = 0, acc_units = 0;
+    bool ok = true;
+    int idx;
+    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+      int bh, qt;
+      dq_unit(p, idx, bh, qt);
+      const int n = dq_key_tiles(p, qt);
+      ok = wait_warp(bar(L::kBarQdFull), units & 1, abort_flag, limit, kSiteMma);
+      if (!ok) break;
+      ++units;
+      {
+        const int s0 = static_cast<int>(it % L::kStages);
+        ok = wait_warp(bar(L::kBarKvFull + s0), (it / L::kStages) & 1, abort_flag, limit, kSiteMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_rows(L::kColS, desc_q, kmaj(stage_off(s0)));
+        ptx::mma_commit_warp(bar(L::kBarSFull));
+        issue_rows(L::kColDp, desc_do, kmaj(stage_off(s0) + T::kTileBytes));
+        ptx::mma_commit_warp(bar(L::kBarDpFull));
+      }
+      for (int t = 0; t < n && ok; ++t, ++it) {
+        const int s = static_cast<int>(it % L::kStages);
+        const int s1 = static_cast<int>((it + 1) % L::kStages);
+        if (t + 1 < n) {   // next S as soon as this S has left TMEM
+          ok = wait_warp(bar(L::kBarSFree), it & 1, abort_flag, limit, kSiteMma);
+          if (ok) ok = wait_warp(bar(L::kBarKvFull + s1), ((it + 1) / L::kStages) & 1, abort_flag, limit, kSiteMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_rows(L::kColS, desc_q, kmaj(stage_off(s1)));
+          ptx::mma_commit_warp(bar(L::kBarSFull));
+        }
+        if (t == 0 && acc_units > 0) {
+          ok = wait_warp(bar(L::kBarAccEmpty), (acc_units - 1) & 1, abort_flag, limit, kSiteMma);
+          if (!ok) break;
+        }
+        ok = wait_warp(bar(L::kBarDsFull), it & 1, abort_flag, limit, kSiteMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_acc(mnmaj(stage_off(s)), t > 0);
+        ptx::mma_commit_warp(bar(L::kBarKvEmpty + s));   // K, V of stage s read for the last time
+        if (t + 1 < n) {   // next dP overwrites dS: issued after the MMA that reads it
+          issue_rows(L::kColDp, desc_do, kmaj(stage_off(s1) + T::kTileBytes));
+          ptx::mma_commit_warp(bar(L::kBarDpFull));
+        }
+      }
+      if (!ok) break;
+      ptx::mma_commit_warp(bar(L::kBarAccFull));
+      ptx::mma_commit_warp(bar(L::kBarQdEmpty));
+      ++acc_units;
+    }
+    ptx::mma_commit_warp(bar(L::kBarDrain));
+    drain_phase(bar(L::kBarDrain), 0, limit);
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+}  // namespace fab
+
+// ============================================================================ host side
+namespace {
+
+using fab::BwdParams;
+
+std::mutex g_bwd_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
+bool g_bwd_ready[64][2] = {};
+
+bool bwd_overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return na && nb && pa < pb + nb && pb < pa + na;
+}
+
+size_t bwd_round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+fa_status bwd_prepare(int D, int* sm_count) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  // Make the device's primary context current on this thread: a thread that has only
+  // selected the device (a worker thread, autograd's backward thread) has none yet, and
+  // tensor-map encoding needs one.
+  if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_bwd_mutex);
+  if (!g_bwd_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return FA_ERR_CUDA;
+    g_bwd_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const int di = (D == 128) ? 1 : 0;
+  if (!g_bwd_ready[dev][di]) {
+    cudaError_t e1, e2;
+    if (D == 128) {
+      e1 = cudaFuncSetAttribute(fab::fa_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fab::DkdvLayout<128>::kAlloc);
+      e2 = cudaFuncSetAttribute(fab::fa_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fab::DqLayout<128>::kAlloc);
+    } else {
+      e1 = cudaFuncSetAttribute(fab::fa_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fab::DkdvLayout<64>::kAlloc);
+      e2 = cudaFuncSetAttribute(fab::fa_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fab::DqLayout<64>::kAlloc);
+    }
+    if (e1 != cudaSuccess || e2 != cudaSuccess) return FA_ERR_CUDA;
+    g_bwd_ready[dev][di] = true;
+  }
+  return FA_OK;
+}
+
+bool bwd_encode_map(CUtensorMap* map, const void* base, long long BH, long long L, int D) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L) * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estrides[3] = {1, 1, 1};
+  return g_bwd_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                      estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Size checks shared by fa_bwd and fa_bwd_workspace_size; *rows = B*H*Lq.
+fa_status bwd_check_sizes(int B, int H, int Lq, int Lk, int D, long long* rows, long long* bh) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  *bh = static_cast<long long>(B) * H;
+  *rows = *bh * Lq;
+  if (*rows == 0) return FA_OK;
+  if (Lk < 1) return FA_ERR_INVALID_ARG;
+  if (*rows * D > (1ll << 40) || *bh * Lk * D > (1ll << 40)) return FA_ERR_INVALID_ARG;
+  const long long nq = (Lq + 127) / 128, nk = (Lk + 127) / 128;
+  if (*bh > INT_MAX || *bh * nq > INT_MAX || *bh * nk > INT_MAX) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+
+unsigned fa_bwd_take_device_status() {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, fab::g_bwd_status, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(fab::g_bwd_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return v;
+}
+
+extern "C" fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal, size_t* bytes) {
+  (void)causal;
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  long long rows = 0, bh = 0;
+  const fa_status st = bwd_check_sizes(B, H, Lq, Lk, D, &rows, &bh);
+  if (st != FA_OK) return st;
+  *bytes = bwd_round256(static_cast<size_t>(rows) * sizeof(float));
+  return FA_OK;
+}
+
+extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Lq, int Lk,
+                            int D, int causal, float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  long long rows = 0, bh = 0;
+  fa_status st = bwd_check_sizes(B, H, Lq, Lk, D, &rows, &bh);
+  if (st != FA_OK) return st;
+  const size_t bytes_k = static_cast<size_t>(bh) * Lk * D * 2;
+  if (rows == 0) {   // no query rows: every key gradient is zero
+    if (bytes_k == 0) return FA_OK;
+    if (!dK || !dV || (reinterpret_cast<uintptr_t>(dK) | reinterpret_cast<uintptr_t>(dV)) & 15u)
+      return FA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(dK, 0, bytes_k, stream) != cudaSuccess ||
+        cudaMemsetAsync(dV, 0, bytes_k, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
+  if (!(scale > 0.0f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  const void* in[6] = {Q, K, V, O, dO, LSE};
+  void* out[3] = {dQ, dK, dV};
+  uintptr_t bits = reinterpret_cast<uintptr_t>(workspace);
+  for (const void* x : in) {
+    if (!x) return FA_ERR_INVALID_ARG;
+    bits |= reinterpret_cast<uintptr_t>(x);
+  }
+  for (void* x : out) {
+    if (!x) return FA_ERR_INVALID_ARG;
+    bits |= reinterpret_cast<uintptr_t>(x);
+  }
+  if (bits & 15u) return FA_ERR_INVALID_ARG;
+  const size_t bytes_q = static_cast<size_t>(rows) * D * 2, bytes_l = static_cast<size_t>(rows) * 4;
+  const size_t need_ws = bwd_round256(bytes_l);
+  if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_INVALID_ARG;
+  const size_t in_bytes[6] = {bytes_q, bytes_k, bytes_k, bytes_q, bytes_q, bytes_l};
+  const size_t out_bytes[4] = {bytes_q, bytes_k, bytes_k, need_ws};
+  void* outs[4] = {dQ, dK, dV, workspace};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (bwd_overlaps(outs[a], out_bytes[a], in[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (bwd_overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_INVALID_ARG;
+  }
+  int sm_count = 0;
+  st = bwd_prepare(D, &sm_count);
+  if (st != FA_OK) return st;
+
+  BwdParams p;
+  if (!bwd_encode_map(&p.tm_q, Q, bh, Lq, D) || !bwd_encode_map(&p.tm_k, K, bh, Lk, D) ||
+      !bwd_encode_map(&p.tm_v, V, bh, Lk, D) || !bwd_encode_map(&p.tm_do, dO, bh, Lq, D))
+    return FA_ERR_CUDA;
+  float* delta = static_cast<float*>(workspace);
+  p.lse = LSE;
+  p.delta = delta;
+  p.dq = static_cast<__nv_bfloat16*>(dQ);
+  p.dk = static_cast<__nv_bfloat16*>(dK);
+  p.dv = static_cast<__nv_bfloat16*>(dV);
+  p.bh_count = static_cast<int>(bh);
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.causal = causal ? 1 : 0;
+  p.nq = (Lq + 127) / 128;
+  p.nk = (Lk + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const unsigned long long lim = fa_internal_wait_limit_ns();
+  p.wait_limit_ns = lim ? lim : fab::kDefaultWaitNs;
+
+  // 1. Delta = rowsum(dO * O).  Launch errors come from the launch call itself (not
+  // cudaGetLastError, which would also report an earlier error of the calling thread).
+  {
+    const long long threads = rows * (D / 8);
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+    dc.blockDim = dim3(256);
+    dc.stream = stream;
+    const __nv_bfloat16* o_in = static_cast<const __nv_bfloat16*>(O);
+    const __nv_bfloat16* do_in = static_cast<const __nv_bfloat16*>(dO);
+    const cudaError_t e = (D == 128) ? cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<128>, o_in, do_in, delta, rows)
+                                     : cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<64>, o_in, do_in, delta, rows);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+  }
+  // 2. dK, dV (one unit per key tile) and 3. dQ (one unit per query tile)
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(fab::kThreads);
+  cfg.stream = stream;
+  p.n_units = static_cast<int>(bh * p.nk);
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
+  cfg.dynamicSmemBytes = (D == 128) ? fab::DkdvLayout<128>::kAlloc : fab::DkdvLayout<64>::kAlloc;
+  cudaError_t err = (D == 128) ? cudaLaunchKernelEx(&cfg, fab::fa_bwd_dkdv_kernel<128>, p)
+                               : cudaLaunchKernelEx(&cfg, fab::fa_bwd_dkdv_kernel<64>, p);
+  if (err != cudaSuccess) return FA_ERR_CUDA;
+  p.n_units = static_cast<int>(bh * p.nq);
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
+  cfg.dynamicSmemBytes = (D == 128) ? fab::DqLayout<128>::kAlloc : fab::DqLayout<64>::kAlloc;
+  err = (D == 128) ? cudaLaunchKernelEx(&cfg, fab::fa_bwd_dq_kernel<128>, p)
+                   : cudaLaunchKernelEx(&cfg, fab::fa_bwd_dq_kernel<64>, p);
+  if (err != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}

@@ -49,6 +49,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -1268,6 +1269,9 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
 fa_status current_device(int D, int* sm_count) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  // Make the device's primary context current on this thread (a thread that has only
+  // selected the device has none yet, and tensor-map encoding needs one).
+  if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
   return prepare_device(dev, D, sm_count);
 }
 
@@ -1412,6 +1416,7 @@ extern "C" fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V,
   if (st != FA_OK || empty) return st;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;   // primary context current here
   int sm_count = 0;
   const fa_status prep = prepare_device(dev, D, &sm_count);
   if (prep != FA_OK) return prep;
@@ -1443,8 +1448,12 @@ extern "C" fa_status fa_last_device_status(cudaStream_t stream) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(fa::g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
+  const unsigned vb = fa_bwd_take_device_status();   // the backward kernels' word
+  if (!v) v = vb;
   return static_cast<fa_status>(v & 0xffu);
 }
+
+unsigned long long fa_internal_wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 extern "C" fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns) {
   g_debug_flags.store(flags);

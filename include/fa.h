@@ -167,12 +167,51 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, f
                          int B, int H, int Lq, int Lk, int D, int causal, float scale,
                          cudaStream_t stream);
 
+/*
+ * fa_bwd_workspace_size -- device workspace fa_bwd needs, in *bytes: one fp32 per
+ * query row (B*H*Lq), rounded up to 256 bytes.  Argument errors as fa_bwd's
+ * size checks (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED; bytes == NULL is invalid).
+ */
+fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal, size_t* bytes);
+
+/*
+ * fa_bwd -- gradients of the attention of fa_fwd (the backward pass).
+ *
+ * Given the forward's inputs Q, K, V, its outputs O and LSE, and dO = dLoss/dO,
+ * writes dQ, dK, dV = dLoss/dQ, dLoss/dK, dLoss/dV:
+ *   P_ij  = exp(scale * Q_i.K_j - LSE_i)        (recomputed from LSE, not stored)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dS_ij = P_ij (dO_i.V_j - Delta_i),  Delta_i = dO_i.O_i
+ *   dQ_i  = scale sum_j dS_ij K_j,      dK_j = scale sum_i dS_ij Q_i
+ * over the allowed pairs of the same mask as fa_fwd (causal: j <= i, top-left).
+ * The wsisp.com post "FlashAttention-2 forward in Triton" states the principle
+ * (recompute the probabilities from the saved row statistic instead of storing
+ * them) and leaves the backward pass to later work; the formulas are the chain
+ * rule through the forward definition.
+ *
+ *   Q, dO, O : const bf16 [B,H,Lq,D];  K, V : const bf16 [B,H,Lk,D];
+ *   LSE      : const fp32 [B,H,Lq] as written by fa_fwd for the same arguments;
+ *   dQ       : bf16 [B,H,Lq,D], written;  dK, dV : bf16 [B,H,Lk,D], written;
+ *   workspace: device memory of at least fa_bwd_workspace_size bytes, 256-byte
+ *              aligned, contents ignored and left as scratch (it holds Delta);
+ *   B, H, Lq, Lk, D, causal, scale, stream: as fa_fwd.
+ * All pointers are device pointers, 16-byte aligned; dQ, dK, dV and the workspace
+ * must not overlap each other or any input.  Three kernels are queued on `stream`
+ * (Delta, then dK/dV, then dQ).  B*H*Lq == 0 with B*H*Lk > 0 zero-fills dK and dV;
+ * B*H*Lk == 0 returns FA_OK with nothing queued.  Errors as fa_fwd; a pipeline
+ * wait that runs out is reported by fa_last_device_status().
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Lq, int Lk,
+                 int D, int causal, float scale, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(fa_status s);
 
 /*
  * fa_last_device_status -- synchronise `stream`, then read and clear the
- * library's device status word on the current device.  Returns FA_OK if no
+ * library's device status words (forward and backward kernels) on the current device.  Returns FA_OK if no
  * kernel launched since the last read reported a problem, FA_ERR_TIMEOUT if a
  * pipeline wait inside a kernel gave up (the kernel then stops early and its
  * outputs are undefined), or FA_ERR_CUDA if the synchronisation failed.

@@ -93,8 +93,9 @@ def test_binding_is_argument_marshalling_only():
     """The binding module holds no attention arithmetic and imports no oracle."""
     src = open(_native.__file__).read() + open(fa.__file__).read()
     assert "oracle" not in src
+    code = "\n".join(line for line in src.splitlines() if not line.strip().startswith("@"))  # decorators
     for word in ("softmax", "exp(", "exp2", "matmul", "einsum", "@"):
-        assert word not in src.replace("@property", ""), word
+        assert word not in code, word
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -153,3 +154,31 @@ def test_fwd_window_rejects_bad_arguments_before_any_cuda_call(lib, left, right,
 def test_fwd_window_empty_problem_is_ok_without_launch(lib):
     assert call_window(2, 2, Lq=0, Lk=16) == fa.FA_OK
     assert call_window(2, 2, B=0, Q=0, K=0, V=0, O=0, LSE=0) == fa.FA_OK
+
+
+def test_bwd_rejects_bad_arguments_before_any_cuda_call(lib):
+    A = ALIGNED
+    def call(**kw):
+        a = dict(Q=A, K=2 * A, V=3 * A, O=4 * A, dO=5 * A, LSE=6 * A, dQ=7 * A, dK=8 * A, dV=9 * A,
+                 B=1, H=1, Lq=16, Lk=16, D=64, causal=0, scale=0.125, ws=10 * A, wsb=1 << 16)
+        a.update(kw)
+        return fa.fa_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"], a["dV"],
+                         a["B"], a["H"], a["Lq"], a["Lk"], a["D"], a["causal"], a["scale"], a["ws"],
+                         a["wsb"], 0)
+    assert call(D=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(Lk=0) == fa.FA_ERR_INVALID_ARG
+    assert call(B=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(dO=0) == fa.FA_ERR_INVALID_ARG
+    assert call(dQ=7 * A + 8) == fa.FA_ERR_INVALID_ARG          # misaligned
+    assert call(ws=0) == fa.FA_ERR_INVALID_ARG                  # workspace missing
+    assert call(wsb=16) == fa.FA_ERR_INVALID_ARG                # workspace too small
+    assert call(ws=10 * A + 16) == fa.FA_ERR_INVALID_ARG        # workspace not 256-byte aligned
+    assert call(dK=A) == fa.FA_ERR_INVALID_ARG                  # dK overlaps Q
+    assert call(dV=8 * A) == fa.FA_ERR_INVALID_ARG              # dV overlaps dK
+    assert call(ws=5 * A) == fa.FA_ERR_INVALID_ARG              # workspace overlaps dO
+    assert call(B=0, Lk=0) == fa.FA_OK                           # nothing to do
+    st, n = fa.fa_bwd_workspace_size(2, 3, 100, 50, 128, 1)
+    assert st == fa.FA_OK and n == 2 * 3 * 100 * 4 + 256 - (2 * 3 * 100 * 4) % 256
+    assert fa.fa_bwd_workspace_size(1, 1, 16, 16, 96, 0)[0] == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd_workspace_size(1, 1, 16, 16, 64, 0, None) == fa.FA_ERR_INVALID_ARG

@@ -1,0 +1,189 @@
+"""GPU parity of the backward pass (fa_bwd through the C ABI) against the fp64 oracle.
+
+The method states no tolerance for gradients, so the bound used is derived from
+where the kernels round, per element, with u = 2^-8 (bf16 unit roundoff):
+  * P is rounded to bf16 before dV = P^T dO:        u * sum_i P_ij |dO_i|
+  * Delta = rowsum(dO * O) uses the bf16 output O:   e_i = 2u * sum_d |dO_id O_id|
+    (the forward's own rounding of O plus the kernel's deviation from exact O)
+  * dS is rounded to bf16 before dK = dS^T Q and dQ = dS K:
+        scale * sum (P_ij e_i + u |dS_ij|) |Q_i|   (dK),   ... |K_j| (dQ)
+  * every output is rounded to bf16:                  u * |result|
+plus 1e-3 for fp32 accumulation and the approximate exp2.  The test asserts
+|GPU - oracle| <= 2 x that bound element by element (the factor covers the
+fp32 P, LSE and the bound's first-order nature), and also reports the error
+relative to the largest gradient entry.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_60_gb300 as fa
+from exact_attention_60_gb300.workloads import WORKLOADS, make_qkv, make_workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -8
+
+
+def make_do(B, H, Lq, D, seed):
+    g = torch.Generator().manual_seed(int(seed) + 99)
+    return torch.randn((B, H, Lq, D), generator=g).to(torch.bfloat16)
+
+
+def gpu_grads(q, k, v, do, causal, scale):
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    st = fa.fa_last_device_status()
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    return o.float().cpu().numpy(), dq.float().cpu().numpy(), dk.float().cpu().numpy(), dv.float().cpu().numpy()
+
+
+def bounds_head(q, k, v, do, o, causal, scale, oracle_mod):
+    """Per-element error bounds (dQ, dK, dV) for one head, from the rounding points."""
+    P = oracle_mod.attn_head(q, k, v, causal, scale, want_p=True)[2]
+    dP = do @ v.T
+    delta = (P * dP).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    e = 2 * U * np.abs(do * o).sum(axis=1)                # Delta from the bf16 O
+    w = P * e[:, None] + U * np.abs(dS)                    # dS error per pair
+    bq = scale * w @ np.abs(k)
+    bk = scale * w.T @ np.abs(q)
+    bv = U * P.T @ np.abs(do)
+    return bq, bk, bv
+
+
+def check(oracle_mod, q, k, v, do, causal, scale, heads=None):
+    o_g, dq_g, dk_g, dv_g = gpu_grads(q, k, v, do, causal, scale)
+    B, H = q.shape[:2]
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    f64 = lambda t: t.double().numpy()
+    worst_rel = 0.0
+    for (b, h) in heads:
+        qh, kh, vh, doh = (f64(t[b, h]) for t in (q, k, v, do))
+        rq, rk, rv = oracle_mod.attn_bwd_head(qh, kh, vh, doh, causal, scale)
+        bq, bk, bv = bounds_head(qh, kh, vh, doh, o_g[b, h].astype(np.float64), causal, scale, oracle_mod)
+        for name, got, ref, bnd in (("dQ", dq_g[b, h], rq, bq), ("dK", dk_g[b, h], rk, bk),
+                                    ("dV", dv_g[b, h], rv, bv)):
+            assert np.isfinite(got).all(), name
+            tol = 2.0 * (bnd + U * np.abs(ref)) + 1e-3
+            err = np.abs(got - ref)
+            bad = err > tol
+            assert not bad.any(), (f"{name} head {(b, h)}: {bad.sum()} elements over the bound, "
+                                   f"worst excess {np.max(err - tol):.3e}, max err {err.max():.3e}")
+            worst_rel = max(worst_rel, float(err.max() / max(np.abs(ref).max(), 1e-30)))
+    return worst_rel
+
+
+SHAPES = [
+    (1, 2, 128, 128, 64, False), (1, 2, 128, 128, 64, True),
+    (1, 2, 300, 300, 128, True), (1, 2, 300, 300, 128, False),
+    (2, 2, 257, 129, 64, False), (1, 3, 129, 500, 128, True),    # Lq < Lk causal: keys past Lq get 0
+    (1, 2, 500, 200, 128, True), (1, 1, 1, 1, 64, False), (1, 1, 1, 300, 128, True),
+    (2, 1, 640, 640, 64, True), (1, 2, 1000, 1000, 128, True),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_backward_against_oracle(oracle_mod, shape):
+    B, H, Lq, Lk, D, causal = shape
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed=Lq * 3 + Lk + D + causal)
+    do = make_do(B, H, Lq, D, seed=Lq + Lk)
+    check(oracle_mod, q, k, v, do, causal, 1.0 / math.sqrt(D))
+
+
+def test_backward_large_logits(oracle_mod):
+    q, k, v = make_qkv(1, 2, 384, 384, 128, seed=7, sigma_qk=3.0)
+    do = make_do(1, 2, 384, 128, seed=7)
+    check(oracle_mod, q, k, v, do, True, 128 ** -0.5)
+    check(oracle_mod, q, k, v, do, False, 0.05)
+
+
+@pytest.mark.parametrize("name", ["seq4k_d128_causal", "seq1k_d64"])
+def test_backward_workload_sampled_heads(oracle_mod, name):
+    """Full workload on the GPU, two heads compared in full against the oracle."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    do = make_do(w.B, w.H, w.Lq, w.D, seed=w.seed)
+    heads = [(0, 0), (w.B - 1, w.H - 1)]
+    check(oracle_mod, q, k, v, do, w.causal, w.scale, heads=heads)
+
+
+def test_backward_unattended_keys_are_zero():
+    """Causal with Lq < Lk: keys j >= Lq are seen by no query; their gradients are 0."""
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(1, 2, 200, 700, 64, seed=3))
+    do = make_do(1, 2, 200, 64, seed=3).to(dev)
+    o, lse = fa.attention(q, k, v, causal=True)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert (dk[:, :, 200:] == 0).all() and (dv[:, :, 200:] == 0).all()
+    assert (dk[:, :, :200].abs().sum() > 0) and (dv[:, :, :200].abs().sum() > 0)
+
+
+def test_backward_empty_query_zero_fills():
+    dev = torch.device("cuda:0")
+    q = torch.empty((1, 2, 0, 64), dtype=torch.bfloat16, device=dev)
+    k = torch.randn((1, 2, 50, 64), device=dev).to(torch.bfloat16)
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(k, 7.0)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    st = fa.fa_bwd(q, k, k, q, q, None, None, dk, dv, 1, 2, 0, 50, 64, 0, 0.125, ws, 256, None)
+    torch.cuda.synchronize()
+    assert st == fa.FA_OK and (dk == 0).all() and (dv == 0).all()
+
+
+def test_backward_deterministic():
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(2, 4, 1500, 1500, 128, seed=5))
+    do = make_do(2, 4, 1500, 128, seed=5).to(dev)
+    o, lse = fa.attention(q, k, v, causal=True)
+    g1 = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    g2 = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_autograd_function_matches_direct_calls():
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev).requires_grad_(True) for t in make_qkv(1, 2, 300, 400, 64, seed=9))
+    do = make_do(1, 2, 300, 64, seed=9).to(dev)
+    o = fa.flash_attention(q, k, v, causal=True)
+    o.backward(do)
+    o2, lse = fa.attention(q.detach(), k.detach(), v.detach(), causal=True)
+    dq, dk, dv = fa.attention_backward(q.detach(), k.detach(), v.detach(), o2, lse, do, causal=True)
+    assert torch.equal(o, o2)
+    assert torch.equal(q.grad, dq) and torch.equal(k.grad, dk) and torch.equal(v.grad, dv)
+
+
+def test_calls_from_a_fresh_thread():
+    """A thread that never touched CUDA before (as autograd's backward thread): the
+    library makes the device's context current itself."""
+    import threading
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(1, 2, 200, 200, 128, seed=4))
+    do = make_do(1, 2, 200, 128, seed=4).to(dev)
+    o_ref, l_ref = fa.attention(q, k, v, causal=True)
+    g_ref = fa.attention_backward(q, k, v, o_ref, l_ref, do, causal=True)
+    torch.cuda.synchronize()
+    out = {}
+
+    def work():
+        try:
+            o, lse = fa.attention(q, k, v, causal=True, stream=0)
+            out["g"] = fa.attention_backward(q, k, v, o, lse, do, causal=True, stream=0)
+            torch.cuda.synchronize()
+            out["o"] = o
+        except Exception as e:   # reported in the main thread
+            out["err"] = e
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert "err" not in out, out.get("err")
+    assert torch.equal(out["o"], o_ref)
+    for a, b in zip(out["g"], g_ref):
+        assert torch.equal(a, b)
