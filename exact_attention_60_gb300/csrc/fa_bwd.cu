@@ -110,8 +110,8 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
-  const float* lse;    // [B*H][Lq] natural log
-  const float* delta;  // [B*H][Lq] rowsum(dO * O)
+  const float* delta;  // [B*H][nq*128] rowsum(dO * O), 0 past Lq
+  const float* lse2;   // [B*H][nq*128] LSE * log2(e), +inf past Lq
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -169,19 +169,29 @@ __device__ __forceinline__ void dq_unit(const BwdParams& p, int idx, int& bh, in
 }
 
 // ------------------------------------------------------------------ Delta = rowsum(dO * O)
+// Rows are numbered over whole 128-row tiles (row = bh * Lpad + q, Lpad = nq * 128), so
+// both outputs can be copied into shared memory a tile at a time with bulk copies:
+// delta[row] = dO_q . O_q and lse2[row] = LSE_q * log2(e) for q < Lq; 0 and +inf past Lq
+// (+inf makes every recomputed probability of a padded query exactly 0).
 template <int HD>
 __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __nv_bfloat16* __restrict__ O,
                                                            const __nv_bfloat16* __restrict__ dO,
+                                                           const float* __restrict__ lse,
                                                            float* __restrict__ delta,
-                                                           long long rows) {
+                                                           float* __restrict__ lse2,
+                                                           long long rows_pad, int Lq, int Lpad) {
   constexpr int kT = HD / 8;   // threads per row, 8 elements (16 bytes) each
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / kT;
   const int part = static_cast<int>(tid % kT);
+  const long long bh = row / Lpad;
+  const int q = static_cast<int>(row - bh * Lpad);
+  const bool valid = row < rows_pad && q < Lq;
+  const long long src = bh * Lq + q;   // row of O, dO and LSE
   float acc = 0.0f;
-  if (row < rows) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + row * HD) + part);
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + row * HD) + part);
+  if (valid) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + src * HD) + part);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + src * HD) + part);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -192,7 +202,10 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __nv_bfloat16* 
   }
 #pragma unroll
   for (int off = kT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (part == 0 && row < rows) delta[row] = acc;
+  if (part == 0 && row < rows_pad) {
+    delta[row] = valid ? acc : 0.0f;
+    lse2[row] = valid ? __ldg(lse + src) * kLog2e : INFINITY;
+  }
 }
 
 // ------------------------------------------------------------------ dK, dV
@@ -245,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     ptx::mbar_init(bar(L::kBarKvFull), 1);
     ptx::mbar_init(bar(L::kBarKvEmpty), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::kBarQdFull + s), 1 + 32);   // the TMA arrive + every load lane
+      ptx::mbar_init(bar(L::kBarQdFull + s), 1);
       ptx::mbar_init(bar(L::kBarQdEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kBarSFull), 1);
@@ -300,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         const int s = static_cast<int>(it % L::kStages);
         const float* lse2 = reinterpret_cast<const float*>(smem + stage_off(s) + 2 * T::kTileBytes);
         const float* dlt = lse2 + kBlk;
-        // the stage's LSE and Delta were written by the load warp's lanes: wait for them
-        // directly (and for S^T, which the MMA warp commits)
+        // the stage's LSE and Delta (bulk copies) are read here: wait for the stage
+        // itself, and for S^T, which the MMA warp commits
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarQdFull + s), (it / L::kStages) & 1, abort_flag,
                                                 limit, kSiteCompute) &&
                                          wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
@@ -414,22 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         ok = wait_warp(bar(L::kBarQdEmpty + s), ((it / L::kStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
         if (!ok) break;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(bar(L::kBarQdFull + s), 2 * T::kTileBytes);
+          const uint32_t full = bar(L::kBarQdFull + s);
+          const size_t rowp = (static_cast<size_t>(bh) * p.nq + qt) * kBlk;   // padded row of the tile
+          ptx::mbar_arrive_expect_tx(full, 2 * T::kTileBytes + 2 * kBlk * 4);
           for (int rg = 0; rg < T::kRegions; ++rg) {
-            ptx::tma_load_3d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, bar(L::kBarQdFull + s), 64 * rg, qt * kBlk, bh);
-            ptx::tma_load_3d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, bar(L::kBarQdFull + s), 64 * rg, qt * kBlk, bh);
+            ptx::tma_load_3d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, full, 64 * rg, qt * kBlk, bh);
+            ptx::tma_load_3d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, full, 64 * rg, qt * kBlk, bh);
           }
+          ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes, p.lse2 + rowp, kBlk * 4, full);
+          ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes + kBlk * 4, p.delta + rowp, kBlk * 4, full);
         }
         last_fill[s] = static_cast<int>(it);
-        float* lse2 = reinterpret_cast<float*>(smem + stage_off(s) + 2 * T::kTileBytes);
-        float* dlt = lse2 + kBlk;
-        for (int c = lane; c < kBlk; c += 32) {
-          const int q = qt * kBlk + c;
-          const size_t gi = static_cast<size_t>(bh) * p.Lq + q;
-          lse2[c] = (q < p.Lq) ? p.lse[gi] * kLog2e : INFINITY;
-          dlt[c] = (q < p.Lq) ? p.delta[gi] : 0.0f;
-        }
-        ptx::mbar_arrive(bar(L::kBarQdFull + s));
       }
     }
     // Drain: every copy this warp started has landed before the CTA exits.
@@ -620,8 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       const int q = qt * kBlk + row;   // this thread's query
       const bool valid = q < p.Lq;
       const size_t gi = static_cast<size_t>(bh) * p.Lq + (valid ? q : 0);
-      const float lse2 = valid ? p.lse[gi] * kLog2e : 0.0f;
-      const float dlt = valid ? p.delta[gi] : 0.0f;
+      const size_t gp = (static_cast<size_t>(bh) * p.nq + qt) * kBlk + row;   // padded row
+      const float lse2 = valid ? p.lse2[gp] : 0.0f;
+      const float dlt = p.delta[gp];
       // keys k allowed for this row: k < key_lim
       const int key_lim = p.causal ? min(p.Lk, q + 1) : p.Lk;
       for (int t = 0; t < n; ++t, ++it) {
@@ -889,6 +898,7 @@ bool bwd_encode_map(CUtensorMap* map, const void* base, long long BH, long long 
 fa_status bwd_check_sizes(int B, int H, int Lq, int Lk, int D, long long* rows, long long* bh) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (Lq > INT_MAX - 128) return FA_ERR_INVALID_ARG;   // rows are padded to whole 128-row tiles
   *bh = static_cast<long long>(B) * H;
   *rows = *bh * Lq;
   if (*rows == 0) return FA_OK;
@@ -918,7 +928,8 @@ extern "C" fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, 
   long long rows = 0, bh = 0;
   const fa_status st = bwd_check_sizes(B, H, Lq, Lk, D, &rows, &bh);
   if (st != FA_OK) return st;
-  *bytes = bwd_round256(static_cast<size_t>(rows) * sizeof(float));
+  const size_t rows_pad = static_cast<size_t>(bh) * ((Lq + 127) / 128) * 128;
+  *bytes = 2 * bwd_round256(rows_pad * sizeof(float));
   return FA_OK;
 }
 
@@ -953,7 +964,10 @@ extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const v
   }
   if (bits & 15u) return FA_ERR_INVALID_ARG;
   const size_t bytes_q = static_cast<size_t>(rows) * D * 2, bytes_l = static_cast<size_t>(rows) * 4;
-  const size_t need_ws = bwd_round256(bytes_l);
+  const long long nq_ll = (Lq + 127) / 128;
+  const size_t rows_pad = static_cast<size_t>(bh) * nq_ll * 128;
+  const size_t half_ws = bwd_round256(rows_pad * sizeof(float));
+  const size_t need_ws = 2 * half_ws;
   if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return FA_ERR_INVALID_ARG;
   const size_t in_bytes[6] = {bytes_q, bytes_k, bytes_k, bytes_q, bytes_q, bytes_l};
@@ -974,8 +988,9 @@ extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const v
       !bwd_encode_map(&p.tm_v, V, bh, Lk, D) || !bwd_encode_map(&p.tm_do, dO, bh, Lq, D))
     return FA_ERR_CUDA;
   float* delta = static_cast<float*>(workspace);
-  p.lse = LSE;
+  float* lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + half_ws);
   p.delta = delta;
+  p.lse2 = lse2;
   p.dq = static_cast<__nv_bfloat16*>(dQ);
   p.dk = static_cast<__nv_bfloat16*>(dK);
   p.dv = static_cast<__nv_bfloat16*>(dV);
@@ -990,18 +1005,21 @@ extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const v
   const unsigned long long lim = fa_internal_wait_limit_ns();
   p.wait_limit_ns = lim ? lim : fab::kDefaultWaitNs;
 
-  // 1. Delta = rowsum(dO * O).  Launch errors come from the launch call itself (not
-  // cudaGetLastError, which would also report an earlier error of the calling thread).
+  // 1. Delta = rowsum(dO * O) and LSE * log2(e), padded to whole tiles.  Launch errors
+  // come from the launch call itself (not cudaGetLastError, which would also report an
+  // earlier error of the calling thread).
   {
-    const long long threads = rows * (D / 8);
+    const long long threads = static_cast<long long>(rows_pad) * (D / 8);
     cudaLaunchConfig_t dc = {};
     dc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
     dc.blockDim = dim3(256);
     dc.stream = stream;
     const __nv_bfloat16* o_in = static_cast<const __nv_bfloat16*>(O);
     const __nv_bfloat16* do_in = static_cast<const __nv_bfloat16*>(dO);
-    const cudaError_t e = (D == 128) ? cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<128>, o_in, do_in, delta, rows)
-                                     : cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<64>, o_in, do_in, delta, rows);
+    const long long rp = static_cast<long long>(rows_pad);
+    const int lpad = static_cast<int>(nq_ll * 128);
+    const cudaError_t e = (D == 128) ? cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<128>, o_in, do_in, LSE, delta, lse2, rp, Lq, lpad)
+                                     : cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<64>, o_in, do_in, LSE, delta, lse2, rp, Lq, lpad);
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }
   // 2. dK, dV (one unit per key tile) and 3. dQ (one unit per query tile)
