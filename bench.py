@@ -1,7 +1,7 @@
 """Benchmark: attention forward TFLOP/s on one GB300 (and % of dense bf16 peak).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--pass forward|backward]
 
 One step = one fa_fwd launch over the whole workload (every batch, head and
 query tile), inputs already resident in HBM.  TFLOP/s counts 4*D flops per
@@ -43,6 +43,7 @@ sys.path.insert(0, ROOT)
 from exact_attention_60_gb300.workloads import WORKLOADS, make_workload_inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
+METRIC_BWD = "attention bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "seq16k_d128_causal"
 L2_BYTES = 129 * 1024 * 1024
@@ -411,6 +412,118 @@ def run_ours(args, w):
     return 0
 
 
+def time_oracle_bwd(w, q, k, v, budget_s: float):
+    """The oracle's backward on one head of the workload cut to at most 1024 query and key
+    rows, repeated until ``budget_s`` seconds: (flops, seconds, calls, threads)."""
+    import oracle
+    L = min(w.Lq, w.Lk, 1024)
+    qq, kk, vv = (np.ascontiguousarray(t[0, 0, :L].float().numpy(), dtype=np.float64) for t in (q, k, v))
+    g = np.random.default_rng(0).standard_normal(qq.shape)
+    pairs = L * (L + 1) // 2 if w.causal else L * L
+    flops = 2.5 * 4 * w.D * pairs
+    spent, calls = 0.0, 0
+    while spent < budget_s or calls == 0:
+        t0 = time.perf_counter()
+        oracle.attn_bwd_head(qq, kk, vv, g, w.causal, w.scale)
+        spent += time.perf_counter() - t0
+        calls += 1
+    return flops * calls, spent, calls, oracle.max_threads(), L
+
+
+def run_backward(args, w):
+    """One step = one fa_bwd call (Delta, dK/dV and dQ kernels) on resident inputs; the
+    forward outputs it needs are computed once, outside the timed region."""
+    import torch
+    import exact_attention_60_gb300 as fa
+    from exact_attention_60_gb300 import build as fa_build
+
+    fa_build.build()
+    fa._native.load()
+    dist, rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    if w.window is not None:
+        raise SystemExit("the backward pass covers the full and causal masks")
+    q_h, k_h, v_h = make_workload_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 99)
+    do_h = torch.randn(q_h.shape, generator=g).to(torch.bfloat16)
+    per_copy = 2 * (3 * q_h.numel() + 4 * k_h.numel()) + 8 * w.B * w.H * w.Lq
+    n_copies = max(2, math.ceil(2 * L2_BYTES / per_copy) + 1)
+    bufs = []
+    for c in range(n_copies):
+        q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+        o, lse = fa.attention(q, k, v, causal=w.causal, scale=w.scale)
+        bufs.append((q, k, v, o, do, lse, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)))
+    st, ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def launch(i):
+        q, k, v, o, do, lse, dq, dk, dv = bufs[i % n_copies]
+        st = fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.B, w.H, w.Lq, w.Lk, w.D, w.causal,
+                       w.scale, ws, ws_bytes, stream)
+        if st != fa.FA_OK:
+            raise RuntimeError(fa.fa_status_string(st))
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    if fa.fa_last_device_status(stream) != fa.FA_OK:
+        raise RuntimeError("warm-up reported a device error")
+    sampler = ClockSampler(local)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        launch(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks = sampler.stop() if not args.no_clocks else None
+    if fa.fa_last_device_status(stream) != fa.FA_OK:
+        raise RuntimeError("timed region reported a device error")
+    max_ms = reduce_max(dist, ev[0].elapsed_time(ev[1]), dev)
+    flops = 2.5 * w.flops()   # five GEMMs of the forward's size (dV, dP, dS K, dS^T Q, and S)
+    value = aggregate_tflops(world, flops, args.steps, max_ms)
+    per_gpu = flops / (max_ms / args.steps / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = peak_value(peaks, "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    cpu = None
+    if rank == 0 and not args.skip_cpu_baseline:
+        f, t, n, threads, L = time_oracle_bwd(w, q_h, k_h, v_h, args.cpu_seconds)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} backward passes of head 0 cut to {L} query and key rows, "
+                         f"{t:.1f} s of fp64 oracle time"}
+    if rank == 0:
+        line = {
+            "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(), "pass": "backward",
+                       "flops_per_step": flops, "flop_count": "2.5x forward (five GEMMs); the "
+                       "kernels execute seven (dQ is computed apart from dK, dV)",
+                       "l2": f"inputs rotate over {n_copies} copies (> 2x L2)",
+                       "parallelism": f"replica per GPU x{world}", "workspace_bytes": ws_bytes},
+            "pct_of_peak": 100.0 * per_gpu / peak,
+            "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": UNIT,
+                         "frac": per_gpu / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense (burst)",
+                         "kernel": f"fa_bwd (Delta + fa_bwd_dkdv_kernel<{w.D}> + fa_bwd_dq_kernel<{w.D}>), "
+                                   "whole pass"},
+            "cpu_baseline": cpu, "e2e": None, "clocks": clocks, "gpu_launches": 3 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,12 +536,16 @@ def main(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds-per-step", type=float, default=5.0)
+    ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
+                    help="forward (the headline metric) or backward (fa_bwd)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("need --steps >= 1 and --warmup >= 0")
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.which == "backward":
+        return run_backward(args, w)
     return run_ours(args, w)
 
 
