@@ -7,10 +7,10 @@ from __future__ import annotations
 
 import math
 
-from ._native import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
-                      FA_OK, fa_bwd, fa_bwd_workspace_size, fa_debug_set, fa_fwd, fa_fwd_noalloc,
-                      fa_fwd_window, fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status,
-                      fa_status_string)
+from ._native import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,
+                      FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, fa_bwd, fa_bwd_workspace_size,
+                      fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_strided, fa_fwd_window,
+                      fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status, fa_status_string)
 
 
 class FaError(RuntimeError):
@@ -50,21 +50,46 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     ``window=(left, right)`` restricts row i to keys i - left <= j <= i + right (-1:
     unbounded side) and calls fa_fwd_window; with ``causal`` the band is cut at the
     diagonal (right = 0).
+
+    q, k, v (and ``out``) may also be fp16, or strided views of shape [B, H, L, D] with a
+    contiguous last dimension (for instance slices of a packed [B, L, 3, H, D] projection);
+    those calls go to fa_fwd_strided.  ``out`` defaults to a contiguous tensor of q's dtype.
     """
     import torch
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bf16 or fp16")
     for t in (q, k, v):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+        if t.dtype != dtype or not t.is_cuda or t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError("q, k, v must be CUDA tensors of one dtype, [B, H, L, D], last dim contiguous")
     if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
         raise ValueError("k and v must be [B, H, Lk, D] matching q")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((B, H, Lq, D), device=q.device, dtype=dtype)
     if lse is None:
         lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor")
+    plain = dtype == torch.bfloat16 and all(t.is_contiguous() for t in (q, k, v, out))
+    if not plain:
+        if out.dtype != dtype or out.shape != q.shape or out.stride(3) != 1:
+            raise ValueError("out must have q's dtype and shape and a contiguous last dim")
+        left, right = (-1, 0 if causal else -1) if window is None else (int(window[0]), int(window[1]))
+        if window is not None and causal:
+            right = 0
+        ws, nbytes = (workspace_for(B, H, Lq, Lk, D, False, q.device)
+                      if split and (left, right) == (-1, -1) else (None, 0))
+        code = FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16
+        st = fa_fwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], out,
+                            out.stride()[:3], lse, B, H, Lq, Lk, D, left, right, scale, code,
+                            ws, nbytes, stream)
+        if st != FA_OK:
+            raise FaError(st)
+        return out, lse
     if window is not None:
         left, right = (int(x) for x in window)
         if causal:

@@ -16,9 +16,12 @@ FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP16 = 1
 
 # Every symbol include/fa.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_noalloc",
+EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_strided",
+            "fa_fwd_noalloc",
             "fa_bwd_workspace_size", "fa_bwd", "fa_status_string", "fa_last_device_status",
             "fa_debug_set")
 
@@ -46,6 +49,10 @@ def load(path: str = LIB) -> ctypes.CDLL:
                               ctypes.c_size_t, vp]
     lib.fa_fwd_window.restype = ctypes.c_int
     lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 7 + [ctypes.c_float, vp]
+    lp3 = ctypes.POINTER(ctypes.c_longlong)
+    lib.fa_fwd_strided.restype = ctypes.c_int
+    lib.fa_fwd_strided.argtypes = [vp, lp3, vp, lp3, vp, lp3, vp, lp3, vp] + [ctypes.c_int] * 7 + \
+        [ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
@@ -110,6 +117,25 @@ def fa_fwd_window(Q, K, V, O, LSE, B, H, Lq, Lk, D, window_left, window_right, s
     return load().fa_fwd_window(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
                                 int(Lq), int(Lk), int(D), int(window_left), int(window_right),
                                 float(scale), _stream(stream))
+
+
+def _strides3(st):
+    """Three element strides {batch, head, row} as a C array (None stays None)."""
+    if st is None:
+        return None
+    a, b, c = (int(x) for x in st)
+    return (ctypes.c_longlong * 3)(a, b, c)
+
+
+def fa_fwd_strided(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, LSE, B, H, Lq, Lk, D,
+                   window_left, window_right, scale, dtype, workspace=None, workspace_bytes=0,
+                   stream=None) -> int:
+    """C ``fa_fwd_strided``; strides are sequences of three element strides."""
+    return load().fa_fwd_strided(_ptr(Q), _strides3(q_stride), _ptr(K), _strides3(k_stride),
+                                 _ptr(V), _strides3(v_stride), _ptr(O), _strides3(o_stride),
+                                 _ptr(LSE), int(B), int(H), int(Lq), int(Lk), int(D),
+                                 int(window_left), int(window_right), float(scale), int(dtype),
+                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_fwd_noalloc(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, stream=None) -> int:

@@ -47,6 +47,7 @@
 #include <atomic>
 #include <climits>
 #include <mutex>
+#include <utility>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -127,12 +128,14 @@ static_assert(Layout<128>::kAlloc <= 232448, "shared memory budget (D=128)");
 static_assert(Layout<64>::kAlloc <= 232448, "shared memory budget (D=64)");
 
 struct Params {
-  CUtensorMap tm_q;   // 3-D views [B*H][L][D] of Q, K, V; box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_q;   // 4-D views [B][H][L][D] of Q, K, V (caller's strides); box 64 x 128 x 1 x 1
   CUtensorMap tm_k;
   CUtensorMap tm_v;
-  __nv_bfloat16* o;
-  float* lse;
+  uint16_t* o;        // bf16 or fp16 elements
+  long long o_sb, o_sh, o_sl;   // O strides in elements (batch, head, row); features contiguous
+  float* lse;         // contiguous [B*H][Lq]
   int bh_count;
+  int H;
   int Lq;
   int Lk;
   int causal;
@@ -277,12 +280,12 @@ __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
   }
 }
 
-// tcgen05 instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major or (b_mn_major) MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 (or
+// both fp16 with f16), A K-major, B K-major or (b_mn_major) MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major, bool f16 = false) {
   return (1u << 4)                            // D format: f32
-         | (1u << 7)                          // A format: bf16
-         | (1u << 10)                         // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)             // A format: bf16 (1) or f16 (0)
+         | ((f16 ? 0u : 1u) << 10)            // B format: the same as A
          | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);
@@ -339,7 +342,21 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned
 
 // kS selects the schedule at compile time, so the whole-unit kernel carries none
 // of the other schedules' code.
-template <int HD, int kS>
+// exp2 of a pair, packed as the I/O type (P has the type of V in the P V MMA).
+template <bool kF16>
+__device__ __forceinline__ uint32_t exp2_pair(float x0, float x1, uint64_t k2, uint64_t c2, uint64_t& acc) {
+  if constexpr (kF16) return ptx::exp2_pair_f16(x0, x1, k2, c2, acc);
+  else return ptx::exp2_pair_bf16(x0, x1, k2, c2, acc);
+}
+
+// Two floats to the packed 16-bit element pair of the I/O type.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kF16) return ptx::pack_f16x2(lo, hi);
+  else return ptx::pack_bf16x2(lo, hi);
+}
+
+template <int HD, int kS, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<HD>;
   constexpr bool kSplit = kS == kSchedSplit;
@@ -476,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            pk[c] = ptx::exp2_pair_bf16(s[2 * c], s[2 * c + 1], k2, c2, acc[c & 3]);
+            pk[c] = exp2_pair<kF16>(s[2 * c], s[2 * c + 1], k2, c2, acc[c & 3]);
           if (j > 0) {
             ok = wait_phase(bar(L::kBarPVDone + wg), (s_base + j - 1) & 1, abort_flag, limit,
                             kSiteSoftPV);
@@ -497,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ptx::tmem_st32x32b_x32(t_p, pk);
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            pk[c] = ptx::exp2_pair_bf16(s[64 + 2 * c], s[64 + 2 * c + 1], k2, c2, acc[c & 3]);
+            pk[c] = exp2_pair<kF16>(s[64 + 2 * c], s[64 + 2 * c + 1], k2, c2, acc[c & 3]);
           ptx::tmem_st32x32b_x32(t_p + 32, pk);
           float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
           float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
@@ -508,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-              pk[c] = ptx::exp2_pair_bf16(s[64 * h + 2 * c], s[64 * h + 2 * c + 1], k2, c2, acc[c & 3]);
+              pk[c] = exp2_pair<kF16>(s[64 * h + 2 * c], s[64 * h + 2 * c + 1], k2, c2, acc[c & 3]);
             ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
           }
           float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
@@ -560,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       // Epilogue: O / l as bf16 rows, LSE = ln2 * (m + log2 l); rows >= Lq are not stored.
       const float inv_l = 1.0f / l;
       const bool store = q < p.Lq;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + (store ? q : 0)) * HD;
+      const int ob = bh / p.H, oh = bh - ob * p.H;
+      uint16_t* orow = p.o + ob * p.o_sb + oh * p.o_sh + static_cast<long long>(store ? q : 0) * p.o_sl;
 #pragma unroll
       for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t o[32];
@@ -568,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                   __uint_as_float(o[2 * c + 1]) * inv_l);
+          pk[c] = pack2<kF16>(__uint_as_float(o[2 * c]) * inv_l,
+                              __uint_as_float(o[2 * c + 1]) * inv_l);
         if (store) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
@@ -600,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       bool first = true;
       Unit u;
       for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+        const int ub = u.bh / p.H, uh = u.bh - ub * p.H;   // batch and head of the unit
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (u.nblk[i] == 0) continue;
@@ -611,8 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ptx::mbar_arrive_expect_tx(bar(L::kBarQFull + i), L::kTileBytes);
 #pragma unroll
           for (int rg = 0; rg < L::kRegions; ++rg)
-            ptx::tma_load_3d(sbase + L::kOffQ + i * L::kTileBytes + rg * L::kRegionBytes, &p.tm_q,
-                             bar(L::kBarQFull + i), 64 * rg, u.q0 + i * kBlockM, u.bh);
+            ptx::tma_load_4d(sbase + L::kOffQ + i * L::kTileBytes + rg * L::kRegionBytes, &p.tm_q,
+                             bar(L::kBarQFull + i), 64 * rg, u.q0 + i * kBlockM, uh, ub);
           ++q_count[i];
         }
         for (int j = 0; j < u.nmax && ok; ++j) {
@@ -628,9 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
 #pragma unroll
             for (int rg = 0; rg < L::kRegions; ++rg)
-              ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + rg * L::kRegionBytes,
+              ptx::tma_load_4d(sbase + L::kOffKV + s * L::kTileBytes + rg * L::kRegionBytes,
                                t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * rg,
-                               (kS != kSchedWhole ? u.kv0 + j : j) * kBlockN, u.bh);
+                               (kS != kSchedWhole ? u.kv0 + j : j) * kBlockN, uh, ub);
             last_fill[s] = static_cast<int>(it);
           }
         }
@@ -651,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     ptx::setmaxnreg_dec<kRegsOther>();
     {   // The whole warp runs the loop, so its state stays warp-uniform; one elected
         // lane issues every MMA and commit.
-      constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false);
-      constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true);
+      constexpr uint32_t kIdescS = make_idesc(kBlockM, kBlockN, false, kF16);
+      constexpr uint32_t kIdescPV = make_idesc(kBlockM, HD, true, kF16);
       // Descriptors of the first operand blocks; later blocks differ only in the
       // start-address field (bits 0..13, address >> 4), which never carries over.
       const uint64_t desc_q0 = sw128_desc(sbase + L::kOffQ, 16, 1024);
@@ -900,7 +919,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 struct CombineParams {
   const float* ws_o;
   const float* ws_ml;
-  __nv_bfloat16* o;
+  uint16_t* o;
+  long long o_sb, o_sh, o_sl;
+  int H;
   float* lse;
   long long total_steps;
   int grid;          // CTAs of the attention kernel that made the parts
@@ -922,7 +943,7 @@ constexpr int kCombineRowsPerWarp = 4;
 constexpr int kCombineRows = 4 * kCombineRowsPerWarp;   // rows per CTA (4 warps)
 constexpr int kCombineMaxParts = 256;                   // parts come from distinct CTAs
 
-template <int HD>
+template <int HD, bool kF16>
 __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__ CombineParams c) {
   __shared__ int s_slot[kCombineMaxParts];
   __shared__ int s_nparts, s_bh, s_q0;
@@ -987,13 +1008,14 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
     const int q = s_q0 + r0 + rr;
     if (q >= c.Lq) continue;
     const float inv_l = 1.0f / l[rr];
-    __nv_bfloat16* dst = c.o + (static_cast<size_t>(s_bh) * c.Lq + q) * HD + lane * kPerLane;
+    const int ob = s_bh / c.H, oh = s_bh - ob * c.H;
+    uint16_t* dst = c.o + ob * c.o_sb + oh * c.o_sh + static_cast<long long>(q) * c.o_sl + lane * kPerLane;
     if constexpr (kPerLane == 4) {
       *reinterpret_cast<uint2*>(dst) =
-          make_uint2(ptx::pack_bf16x2(acc[rr][0] * inv_l, acc[rr][1] * inv_l),
-                     ptx::pack_bf16x2(acc[rr][2] * inv_l, acc[rr][3] * inv_l));
+          make_uint2(pack2<kF16>(acc[rr][0] * inv_l, acc[rr][1] * inv_l),
+                     pack2<kF16>(acc[rr][2] * inv_l, acc[rr][3] * inv_l));
     } else {
-      *reinterpret_cast<uint32_t*>(dst) = ptx::pack_bf16x2(acc[rr][0] * inv_l, acc[rr][1] * inv_l);
+      *reinterpret_cast<uint32_t*>(dst) = pack2<kF16>(acc[rr][0] * inv_l, acc[rr][1] * inv_l);
     }
     if (lane == 0)
       c.lse[static_cast<size_t>(s_bh) * c.Lq + q] = (m[rr] + log2f(l[rr])) * 0.69314718055994531f;
@@ -1013,7 +1035,7 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
-  bool attr[2][3] = {};   // [D == 128][schedule]: shared-memory opt-in done
+  bool attr[2][3][2] = {};   // [D == 128][schedule][fp16]: shared-memory opt-in done
 };
 
 std::mutex g_mutex;
@@ -1027,16 +1049,21 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return na && nb && pa < pb + nb && pb < pa + na;
 }
 
-// The attention kernel instance for head dimension D and schedule `sched` (fa::Sched).
+// The attention kernel instance for head dimension D, schedule `sched` (fa::Sched) and
+// element type (bf16, or fp16 with f16).
 using KernelFn = void (*)(const Params);
-KernelFn attention_kernel(int D, int sched) {
+template <bool kF16>
+KernelFn attention_kernel_t(int D, int sched) {
   if (D == 64)
-    return sched == fa::kSchedBand    ? fa::fa_fwd_kernel<64, fa::kSchedBand>
-           : sched == fa::kSchedSplit ? fa::fa_fwd_kernel<64, fa::kSchedSplit>
-                                      : fa::fa_fwd_kernel<64, fa::kSchedWhole>;
-  return sched == fa::kSchedBand    ? fa::fa_fwd_kernel<128, fa::kSchedBand>
-         : sched == fa::kSchedSplit ? fa::fa_fwd_kernel<128, fa::kSchedSplit>
-                                    : fa::fa_fwd_kernel<128, fa::kSchedWhole>;
+    return sched == fa::kSchedBand    ? fa::fa_fwd_kernel<64, fa::kSchedBand, kF16>
+           : sched == fa::kSchedSplit ? fa::fa_fwd_kernel<64, fa::kSchedSplit, kF16>
+                                      : fa::fa_fwd_kernel<64, fa::kSchedWhole, kF16>;
+  return sched == fa::kSchedBand    ? fa::fa_fwd_kernel<128, fa::kSchedBand, kF16>
+         : sched == fa::kSchedSplit ? fa::fa_fwd_kernel<128, fa::kSchedSplit, kF16>
+                                    : fa::fa_fwd_kernel<128, fa::kSchedWhole, kF16>;
+}
+KernelFn attention_kernel(int D, int sched, bool f16) {
+  return f16 ? attention_kernel_t<true>(D, sched) : attention_kernel_t<false>(D, sched);
 }
 
 // Shared-memory opt-in for one kernel instance, and a check that the registers it
@@ -1056,7 +1083,7 @@ fa_status configure_kernel(void (*kernel)(const Params), int smem_bytes) {
 
 // Per-device set-up: capability check, kernel attributes, encoder entry point.
 // On success *sm_count holds the device's number of SMs.
-fa_status prepare_device(int dev, int D, int* sm_count) {
+fa_status prepare_device(int dev, int D, int* sm_count, bool f16 = false) {
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo& info = g_devices[dev];
@@ -1081,28 +1108,35 @@ fa_status prepare_device(int dev, int D, int* sm_count) {
       return FA_ERR_CUDA;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  const int di = (D == 128) ? 1 : 0;
+  const int di = (D == 128) ? 1 : 0, ti = f16 ? 1 : 0;
   for (int sc = 0; sc < 3; ++sc) {
-    if (info.attr[di][sc]) continue;
-    const fa_status st = configure_kernel(attention_kernel(D, sc),
+    if (info.attr[di][sc][ti]) continue;
+    const fa_status st = configure_kernel(attention_kernel(D, sc, f16),
                                           D == 64 ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc);
     if (st != FA_OK) return st;
-    info.attr[di][sc] = true;
+    info.attr[di][sc][ti] = true;
   }
   return FA_OK;
 }
 
-// 3-D tensor map over a contiguous [BH][L][D] bf16 tensor; box = 64 features x 128 rows x 1 head.
-bool encode_map(CUtensorMap* map, const void* base, long long BH, long long L, int D) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L) * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estrides[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
-                              dims, strides, box, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+// 4-D tensor map [B][H][L][D] over a tensor with element strides st = {batch, head, row}
+// (features contiguous); box = 64 features x 128 rows x 1 head x 1 batch.  A size-1
+// dimension's stride is never used to address anything and is replaced by a valid one.
+bool encode_map(CUtensorMap* map, const void* base, long long B, long long H, long long L, int D,
+                const long long* st, bool f16) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const long long row = L > 1 ? st[2] : D;
+  const long long head = H > 1 ? st[1] : row * L;
+  const long long batch = B > 1 ? st[0] : head * H;
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(row) * 2, static_cast<cuuint64_t>(head) * 2,
+                           static_cast<cuuint64_t>(batch) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estrides[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              4, const_cast<void*>(base), dims, strides, box, estrides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -1125,7 +1159,17 @@ struct Problem {
   bool band = false;     // local attention over the band below (fa_fwd_window)
   int win_left = -1;     // key j allowed for row i iff i - win_left <= j <= i + win_right
   int win_right = -1;    //   (-1: unbounded side)
+  bool f16 = false;      // fp16 instead of bf16 inputs and output
+  int B = 0, H = 0;
+  long long qs[3] = {0, 0, 0}, ks[3] = {0, 0, 0}, vs[3] = {0, 0, 0}, os[3] = {0, 0, 0};   // element strides {batch, head, row}
 };
+
+// Contiguous [B,H,L,D] strides.
+void contiguous_strides(long long H, long long L, int D, long long* st) {
+  st[2] = D;
+  st[1] = L * D;
+  st[0] = H * L * D;
+}
 
 // FA_OK with *empty = true means there is nothing to compute (no launch).
 fa_status check_problem(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
@@ -1161,6 +1205,12 @@ fa_status check_problem(const void* Q, const void* K, const void* V, void* O, fl
   *pr = Problem{Q, K, V, O, LSE, Lq, Lk, D, causal ? 1 : 0, scale, bh,
                 static_cast<int>(n_pairs), static_cast<int>(n_pairs * bh),
                 (Lk + fa::kBlockN - 1) / fa::kBlockN, bytes_q, bytes_k, bytes_lse};
+  pr->B = B;
+  pr->H = H;
+  contiguous_strides(H, Lq, D, pr->qs);
+  contiguous_strides(H, Lk, D, pr->ks);
+  contiguous_strides(H, Lk, D, pr->vs);
+  contiguous_strides(H, Lq, D, pr->os);
   return FA_OK;
 }
 
@@ -1199,11 +1249,15 @@ Plan plan_schedule(const Problem& pr, int sm_count) {
 
 fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cudaStream_t stream) {
   Params p;
-  if (!encode_map(&p.tm_q, pr.Q, pr.bh, pr.Lq, pr.D) ||
-      !encode_map(&p.tm_k, pr.K, pr.bh, pr.Lk, pr.D) ||
-      !encode_map(&p.tm_v, pr.V, pr.bh, pr.Lk, pr.D))
+  if (!encode_map(&p.tm_q, pr.Q, pr.B, pr.H, pr.Lq, pr.D, pr.qs, pr.f16) ||
+      !encode_map(&p.tm_k, pr.K, pr.B, pr.H, pr.Lk, pr.D, pr.ks, pr.f16) ||
+      !encode_map(&p.tm_v, pr.V, pr.B, pr.H, pr.Lk, pr.D, pr.vs, pr.f16))
     return FA_ERR_CUDA;
-  p.o = static_cast<__nv_bfloat16*>(pr.O);
+  p.o = static_cast<uint16_t*>(pr.O);
+  p.o_sb = pr.os[0];
+  p.o_sh = pr.os[1];
+  p.o_sl = pr.os[2];
+  p.H = pr.H;
   p.lse = pr.LSE;
   p.bh_count = static_cast<int>(pr.bh);
   p.Lq = pr.Lq;
@@ -1240,7 +1294,7 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   cfg.stream = stream;
   cfg.dynamicSmemBytes = (pr.D == 64) ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc;
   const int sched = pl.band ? fa::kSchedBand : pl.split ? fa::kSchedSplit : fa::kSchedWhole;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched), p);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched, pr.f16), p);
   if (err != cudaSuccess) return FA_ERR_CUDA;
   if (pl.split && pl.grid > 1) {
     // Merge the parts of every split unit (same stream: runs after the parts exist).
@@ -1248,6 +1302,10 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
     c.ws_o = p.ws_o;
     c.ws_ml = p.ws_ml;
     c.o = p.o;
+    c.o_sb = p.o_sb;
+    c.o_sh = p.o_sh;
+    c.o_sl = p.o_sl;
+    c.H = p.H;
     c.lse = p.lse;
     c.total_steps = p.total_steps;
     c.grid = pl.grid;
@@ -1259,8 +1317,12 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
     cc.gridDim = dim3(static_cast<unsigned>(pl.grid - 1), 2, fa::kBlockM / fa::kCombineRows);
     cc.blockDim = dim3(128);
     cc.stream = stream;
-    err = (pr.D == 64) ? cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<64>, c)
-                       : cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<128>, c);
+    if (pr.f16)
+      err = (pr.D == 64) ? cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<64, true>, c)
+                         : cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<128, true>, c);
+    else
+      err = (pr.D == 64) ? cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<64, false>, c)
+                         : cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<128, false>, c);
     if (err != cudaSuccess) return FA_ERR_CUDA;
   }
   return FA_OK;
@@ -1377,6 +1439,140 @@ extern "C" fa_status fa_fwd_window(const void* Q, const void* K, const void* V, 
   pl.band = pr.band;
   pl.grid = std::min(pr.n_units, sm_count);
   return launch(pr, sm_count, pl, nullptr, stream);
+}
+
+// ---------------------------------------------------------------- strided / fp16 entry point
+namespace {
+
+// Byte span [lo, lo + bytes) that a [B,H,L,D] tensor with element strides st touches.
+size_t span_bytes(long long B, long long H, long long L, int D, const long long* st) {
+  const long long last = (B - 1) * st[0] + (H - 1) * st[1] + (L - 1) * st[2] + D;
+  return static_cast<size_t>(last) * 2;
+}
+
+// Strides of one tensor: non-negative multiples of 8 elements (16 bytes, the tensor-memory-
+// access unit's rule) for every dimension of size > 1, and byte offsets below 2^40.
+bool strides_ok(long long B, long long H, long long L, int D, const long long* st) {
+  const long long size[3] = {B, H, L};
+  for (int i = 0; i < 3; ++i) {
+    if (size[i] <= 1) continue;
+    if (st[i] < 0 || (st[i] & 7) || st[i] >= (1ll << 39)) return false;
+  }
+  return span_bytes(B, H, L, D, st) < (1ull << 40);
+}
+
+// No two elements of the tensor share an address: with the dimensions of size > 1 ordered
+// by stride (features innermost, stride 1, extent D), each stride covers the extent of the
+// dimension inside it.
+bool no_self_overlap(long long B, long long H, long long L, int D, const long long* st) {
+  std::pair<long long, long long> dims[4] = {{1, D}};   // (stride, extent)
+  int n = 1;
+  const long long size[3] = {B, H, L};
+  for (int i = 0; i < 3; ++i)
+    if (size[i] > 1) dims[n++] = {st[i], size[i]};
+  std::sort(dims, dims + n);
+  for (int i = 1; i < n; ++i)
+    if (dims[i].first < dims[i - 1].first * dims[i - 1].second) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K,
+                                    const long long* k_stride, const void* V,
+                                    const long long* v_stride, void* O, const long long* o_stride,
+                                    float* LSE, int B, int H, int Lq, int Lk, int D,
+                                    int window_left, int window_right, float scale, int dtype,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * Lq == 0) return FA_OK;
+  if (Lk < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O || !LSE || !q_stride || !k_stride || !v_stride || !o_stride)
+    return FA_ERR_INVALID_ARG;
+  const uintptr_t align_bits = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                               reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                               reinterpret_cast<uintptr_t>(LSE);
+  if (align_bits & 15u) return FA_ERR_INVALID_ARG;
+  if (!strides_ok(B, H, Lq, D, q_stride) || !strides_ok(B, H, Lk, D, k_stride) ||
+      !strides_ok(B, H, Lk, D, v_stride) || !strides_ok(B, H, Lq, D, o_stride) ||
+      !no_self_overlap(B, H, Lq, D, o_stride))
+    return FA_ERR_INVALID_ARG;
+  const long long n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  if (bh > INT_MAX || n_pairs * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  // Q, K and V may share memory (they are only read); O must not meet any input or the LSE.
+  const size_t sq = span_bytes(B, H, Lq, D, q_stride), sk = span_bytes(B, H, Lk, D, k_stride);
+  const size_t sv = span_bytes(B, H, Lk, D, v_stride), so = span_bytes(B, H, Lq, D, o_stride);
+  const size_t sl = static_cast<size_t>(bh * Lq) * 4;
+  if (overlaps(O, so, Q, sq) || overlaps(O, so, K, sk) || overlaps(O, so, V, sv) ||
+      overlaps(O, so, LSE, sl) || overlaps(LSE, sl, Q, sq) || overlaps(LSE, sl, K, sk) ||
+      overlaps(LSE, sl, V, sv))
+    return FA_ERR_INVALID_ARG;
+  int left = window_left, right = window_right;
+  if (left >= Lq - 1) left = -1;
+  if (right >= Lk - 1) right = -1;
+  if (left >= 0 && Lq - 1 - left > Lk - 1) return FA_ERR_INVALID_ARG;   // a row without keys
+
+  Problem pr{};
+  pr.Q = Q;
+  pr.K = K;
+  pr.V = V;
+  pr.O = O;
+  pr.LSE = LSE;
+  pr.Lq = Lq;
+  pr.Lk = Lk;
+  pr.D = D;
+  pr.scale = scale;
+  pr.bh = bh;
+  pr.n_pairs = static_cast<int>(n_pairs);
+  pr.n_units = static_cast<int>(n_pairs * bh);
+  pr.nkv = (Lk + fa::kBlockN - 1) / fa::kBlockN;
+  pr.B = B;
+  pr.H = H;
+  pr.f16 = dtype == FA_DTYPE_FP16;
+  for (int i = 0; i < 3; ++i) {
+    pr.qs[i] = q_stride[i];
+    pr.ks[i] = k_stride[i];
+    pr.vs[i] = v_stride[i];
+    pr.os[i] = o_stride[i];
+  }
+  int sm_count = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;   // primary context current here
+  const fa_status prep = prepare_device(dev, D, &sm_count, pr.f16);
+  if (prep != FA_OK) return prep;
+  const bool force_band = (g_debug_flags.load() & 4u) != 0;
+  Plan pl{};
+  if (!force_band && left < 0 && (right < 0 || right == 0)) {
+    pr.causal = (right == 0) ? 1 : 0;
+    pl = plan_schedule(pr, sm_count);
+    if (pl.split) {   // the split schedule only with a workspace that fits
+      const bool ws_ok = workspace && workspace_bytes >= pl.ws_bytes &&
+                         !(reinterpret_cast<uintptr_t>(workspace) & 255u) &&
+                         !overlaps(workspace, pl.ws_bytes, Q, sq) &&
+                         !overlaps(workspace, pl.ws_bytes, K, sk) &&
+                         !overlaps(workspace, pl.ws_bytes, V, sv) &&
+                         !overlaps(workspace, pl.ws_bytes, O, so) &&
+                         !overlaps(workspace, pl.ws_bytes, LSE, sl);
+      if (!ws_ok) {
+        if (workspace) return FA_ERR_INVALID_ARG;   // given but unusable
+        pl.split = false;
+        pl.grid = std::min(pr.n_units, sm_count);
+      }
+    }
+  } else {
+    pr.band = true;
+    pr.win_left = left;
+    pr.win_right = right;
+    pl.band = true;
+    pl.grid = std::min(pr.n_units, sm_count);
+  }
+  return launch(pr, sm_count, pl, workspace, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation entry point

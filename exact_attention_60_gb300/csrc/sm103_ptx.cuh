@@ -77,6 +77,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// 4-D tiled load: coordinates (x = feature, y = row, z = head, w = batch).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -213,6 +223,24 @@ __device__ __forceinline__ uint32_t exp2_pair_bf16(float x0, float x1, uint64_t 
   return packed;
 }
 
+// The same with the pair packed as f16x2 (for fp16 operands).
+__device__ __forceinline__ uint32_t exp2_pair_f16(float x0, float x1, uint64_t k2, uint64_t c2,
+                                                  uint64_t& acc) {
+  uint32_t packed;
+  asm("{\n\t.reg .b64 t;\n\t.reg .f32 a, b;\n\t"
+      "mov.b64 t, {%2, %3};\n\t"
+      "fma.rn.ftz.f32x2 t, t, %4, %5;\n\t"
+      "mov.b64 {a, b}, t;\n\t"
+      "ex2.approx.ftz.f32 a, a;\n\t"
+      "ex2.approx.ftz.f32 b, b;\n\t"
+      "cvt.rn.f16x2.f32 %0, b, a;\n\t"
+      "mov.b64 t, {a, b};\n\t"
+      "add.rn.ftz.f32x2 %1, %1, t;\n\t}"
+      : "=r"(packed), "+l"(acc)
+      : "f"(x0), "f"(x1), "l"(k2), "l"(c2));
+  return packed;
+}
+
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -229,6 +257,13 @@ __device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two floats to packed f16x2 (round to nearest even); `lo` lands in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

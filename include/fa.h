@@ -44,6 +44,12 @@
 extern "C" {
 #endif
 
+/* Element type of Q, K, V and O for fa_fwd_strided (LSE is always fp32). */
+typedef enum {
+    FA_DTYPE_BF16 = 0,
+    FA_DTYPE_FP16 = 1
+} fa_dtype;
+
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,   /* a null/misaligned/overlapping pointer, a bad size or scale */
@@ -139,6 +145,41 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
 fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O, float* LSE,
                         int B, int H, int Lq, int Lk, int D, int window_left, int window_right,
                         float scale, cudaStream_t stream);
+
+/*
+ * fa_fwd_strided -- the forward pass on strided tensors, in bf16 or fp16.
+ *
+ * The wsisp.com post "FlashAttention-2 forward in Triton" passes four strides per
+ * tensor to its kernel (batch, head, row, feature) and stores O in fp16; this entry
+ * point takes the first three of those strides (the feature stride is 1) for each of
+ * Q, K, V and O, so layouts such as [B, L, H, D] or the Q/K/V parts of one packed
+ * projection output are read in place, and it accepts fp16 as well as bf16.
+ *
+ *   Q, K, V  : const device pointers to elements of `dtype` (FA_DTYPE_BF16 or FA_DTYPE_FP16).
+ *   q_stride, k_stride, v_stride, o_stride : host arrays of three element strides
+ *              {batch, head, row}; element (b, h, i, d) of Q is at Q + b*s[0] + h*s[1] +
+ *              i*s[2] + d.  Each stride of a dimension longer than 1 must be a
+ *              non-negative multiple of 8 elements (16 bytes); Q, K and V may overlap
+ *              (they are only read); no two elements of O may share an address, and O
+ *              must not meet Q, K, V or LSE (checked on the byte spans the tensors cover).
+ *   O        : device pointer, elements of `dtype`, written (round to nearest even).
+ *   LSE      : fp32 device pointer, contiguous [B,H,Lq] (as fa_fwd).
+ *   window_left, window_right : the band of fa_fwd_window; (-1, -1) is the full softmax
+ *              and (-1, 0) the causal mask.
+ *   workspace, workspace_bytes : optional (NULL, 0); with the full mask, a workspace of
+ *              at least fa_fwd_workspace_size(B, H, Lq, Lk, D, 0) bytes lets the split
+ *              schedule of fa_fwd_ws run.  A non-NULL workspace that is too small,
+ *              misaligned or overlapping is an argument error.
+ *   B, H, Lq, Lk, D, scale, stream : as fa_fwd.
+ * Results are bit-identical to fa_fwd / fa_fwd_window / fa_fwd_ws on the same values
+ * laid out contiguously (the addressing is the only difference).  Errors as those calls;
+ * a bad stride or dtype is FA_ERR_INVALID_ARG.
+ */
+fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K,
+                         const long long* k_stride, const void* V, const long long* v_stride,
+                         void* O, const long long* o_stride, float* LSE, int B, int H, int Lq,
+                         int Lk, int D, int window_left, int window_right, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * fa_fwd_noalloc -- fa_fwd_ws without a workspace argument, for callers that

@@ -183,3 +183,39 @@ def test_bwd_rejects_bad_arguments_before_any_cuda_call(lib):
     assert st == fa.FA_OK and n == 2 * (2 * 3 * 128 * 4)
     assert fa.fa_bwd_workspace_size(1, 1, 16, 16, 96, 0)[0] == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_bwd_workspace_size(1, 1, 16, 16, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
+def call_strided(qs=(32768, 2048, 64), ks=(32768, 2048, 64), vs=(32768, 2048, 64),
+                 os_=(32768, 2048, 64), dtype=0, **kw):
+    a = dict(Q=ALIGNED, K=2 * ALIGNED, V=3 * ALIGNED, O=4 * ALIGNED, LSE=5 * ALIGNED, B=2, H=16,
+             Lq=32, Lk=32, D=64, left=-1, right=-1, scale=0.125, ws=None, wsb=0)
+    a.update(kw)
+    return fa.fa_fwd_strided(a["Q"], qs, a["K"], ks, a["V"], vs, a["O"], os_, a["LSE"], a["B"], a["H"],
+                             a["Lq"], a["Lk"], a["D"], a["left"], a["right"], a["scale"], dtype,
+                             a["ws"], a["wsb"], 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=2), fa.FA_ERR_INVALID_ARG),                                  # unknown dtype
+    (dict(qs=(32768, 2048, 60)), fa.FA_ERR_INVALID_ARG),                     # row stride not 16 bytes
+    (dict(ks=(32768, -2048, 64)), fa.FA_ERR_INVALID_ARG),                    # negative stride
+    (dict(os_=(32768, 2048, 32)), fa.FA_ERR_INVALID_ARG),                    # O rows overlap (stride < D)
+    (dict(os_=(32768, 1024, 64)), fa.FA_ERR_INVALID_ARG),                    # O heads overlap
+    (dict(O=ALIGNED + 4096), fa.FA_ERR_INVALID_ARG),                        # O inside Q's span
+    (dict(LSE=4 * ALIGNED + 256), fa.FA_ERR_INVALID_ARG),                   # LSE inside O's span
+    (dict(left=-3), fa.FA_ERR_INVALID_ARG),
+    (dict(left=0, right=0, Lq=40, Lk=32), fa.FA_ERR_INVALID_ARG),           # rows without keys
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(Q=ALIGNED + 8), fa.FA_ERR_INVALID_ARG),                           # misaligned
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_strided_rejects_bad_arguments_before_any_cuda_call(lib, kw, expect):
+    assert call_strided(**kw) == expect
+
+
+def test_fwd_strided_accepts_shared_inputs_and_empty(lib):
+    # empty problems need no pointers
+    assert fa.fa_fwd_strided(None, None, None, None, None, None, None, None, None, 0, 4, 16, 16, 64,
+                             -1, -1, 0.125, 0, None, 0, 0) == fa.FA_OK
+    # a missing stride array with work to do is an argument error
+    assert call_strided(qs=None) == fa.FA_ERR_INVALID_ARG

@@ -1,0 +1,134 @@
+"""GPU tests of fa_fwd_strided: strided layouts and fp16 I/O.
+
+Strided inputs and outputs change only the addressing, so their results must equal
+the contiguous bf16 calls bit for bit.  fp16 changes the arithmetic (P and O rounded
+to fp16), so fp16 results are compared with the fp64 oracle on the fp16 input values,
+at the forward's tolerances (max-abs 2e-2 on O, 1e-3 on LSE).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_60_gb300 as fa
+from exact_attention_60_gb300.workloads import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 2e-2
+TOL_LSE = 1e-3
+DEV = torch.device("cuda:0")
+
+
+def packed_qkv(B, H, Lq, D, seed, dtype=torch.bfloat16):
+    """Q, K, V as views of one [B, L, 3, H, D] projection output (Lq == Lk)."""
+    q, k, v = make_qkv(B, H, Lq, Lq, D, seed)
+    packed = torch.empty((B, Lq, 3, H, D), dtype=dtype, device=DEV)
+    for i, t in enumerate((q, k, v)):
+        packed[:, :, i] = t.to(dtype).to(DEV).transpose(1, 2)
+    views = tuple(packed[:, :, i].transpose(1, 2) for i in range(3))   # [B, H, L, D], strided
+    return views, (q, k, v)
+
+
+@pytest.mark.parametrize("B,H,L,D,causal", [(2, 3, 300, 128, True), (1, 4, 257, 64, False),
+                                            (3, 1, 129, 128, False), (1, 1, 1000, 64, True),
+                                            (2, 8, 640, 128, True)])
+def test_packed_qkv_equals_contiguous(B, H, L, D, causal):
+    (qv, kv, vv), (q, k, v) = packed_qkv(B, H, L, D, seed=L + D)
+    assert not qv.is_contiguous()
+    o_ref, l_ref = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, split=False)
+    o, lse = fa.attention(qv, kv, vv, causal=causal, split=False)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_strided_output_equals_contiguous():
+    q, k, v = (t.to(DEV) for t in make_qkv(2, 4, 500, 700, 128, seed=3))
+    o_ref, l_ref = fa.attention(q, k, v, causal=True, split=False)
+    buf = torch.full((2, 500, 4, 128), 7.0, dtype=torch.bfloat16, device=DEV)   # [B, L, H, D]
+    out = buf.transpose(1, 2)
+    o, lse = fa.attention(q, k, v, causal=True, out=out)
+    assert o.data_ptr() == buf.data_ptr()
+    assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
+
+
+@pytest.mark.parametrize("window", [(100, 0), (64, 64), (-1, 3)])
+def test_strided_band_equals_contiguous(window):
+    (qv, kv, vv), (q, k, v) = packed_qkv(2, 2, 700, 128, seed=11)
+    o_ref, l_ref = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), window=window)
+    o, lse = fa.attention(qv, kv, vv, window=window)
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_strided_split_schedule_equals_contiguous():
+    """Few query tiles, long keys: the split schedule with a workspace, strided inputs."""
+    q, k, v = (t.to(DEV) for t in make_qkv(1, 4, 512, 8192, 128, seed=5))
+    o_ref, l_ref = fa.attention(q, k, v, causal=False)   # fa_fwd_ws, split
+    st, ws_bytes = fa.fa_fwd_workspace_size(1, 4, 512, 8192, 128, 0)
+    assert ws_bytes > 0
+    kt = k.transpose(1, 2).contiguous().transpose(1, 2)   # [B, L, H, D] memory, [B, H, L, D] view
+    vt = v.transpose(1, 2).contiguous().transpose(1, 2)
+    o, lse = fa.attention(q, kt, vt, causal=False)
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def fp16_inputs(B, H, Lq, Lk, D, seed, sigma_qk=1.0):
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed, sigma_qk=sigma_qk)   # bf16 draws, exact in fp16 too
+    return tuple(t.to(torch.float16) for t in (q, k, v))
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,D,causal", [(1, 2, 128, 128, 64, False), (2, 2, 300, 260, 128, True),
+                                                (1, 3, 257, 500, 64, True), (2, 1, 700, 129, 128, False)])
+def test_fp16_against_oracle(oracle_mod, B, H, Lq, Lk, D, causal):
+    q, k, v = fp16_inputs(B, H, Lq, Lk, D, seed=Lq + Lk)
+    o, lse = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal)
+    assert o.dtype == torch.float16 and fa.fa_last_device_status() == fa.FA_OK
+    ref_o, ref_l = oracle_mod.attn_full(q.float(), k.float(), v.float(), causal, 1.0 / math.sqrt(D))
+    assert np.abs(o.float().cpu().numpy() - ref_o).max() <= TOL_O
+    assert np.abs(lse.cpu().numpy() - ref_l).max() <= TOL_LSE
+
+
+def test_fp16_is_more_accurate_than_bf16(oracle_mod):
+    """fp16 keeps 3 more significand bits for P and O: its error is smaller."""
+    q, k, v = fp16_inputs(1, 4, 512, 512, 128, seed=17)
+    ref_o, _ = oracle_mod.attn_full(q.float(), k.float(), v.float(), True, 128 ** -0.5)
+    o16, _ = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    ob, _ = fa.attention(q.to(DEV).bfloat16(), k.to(DEV).bfloat16(), v.to(DEV).bfloat16(), causal=True)
+    e16 = np.abs(o16.float().cpu().numpy() - ref_o).max()
+    eb = np.abs(ob.float().cpu().numpy() - ref_o).max()
+    assert e16 < eb / 2, (e16, eb)
+
+
+def test_fp16_band_and_split_against_oracle(oracle_mod):
+    q, k, v = fp16_inputs(1, 2, 600, 600, 128, seed=23)
+    o, lse = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), window=(200, 50))
+    ref_o, ref_l = oracle_mod.attn_full_window(q.float(), k.float(), v.float(), 200, 50, 128 ** -0.5)
+    assert np.abs(o.float().cpu().numpy() - ref_o).max() <= TOL_O
+    assert np.abs(lse.cpu().numpy() - ref_l).max() <= TOL_LSE
+    q, k, v = fp16_inputs(1, 2, 256, 4000, 64, seed=29, sigma_qk=2.0)
+    st, ws_bytes = fa.fa_fwd_workspace_size(1, 2, 256, 4000, 64, 0)
+    assert ws_bytes > 0   # the split schedule runs
+    o, lse = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=False)
+    ref_o, ref_l = oracle_mod.attn_full(q.float(), k.float(), v.float(), False, 0.125)
+    assert np.abs(o.float().cpu().numpy() - ref_o).max() <= TOL_O
+    assert np.abs(lse.cpu().numpy() - ref_l).max() <= TOL_LSE
+
+
+def test_fp16_packed_strided_equals_fp16_contiguous():
+    (qv, kv, vv), (q, k, v) = packed_qkv(2, 2, 400, 128, seed=31, dtype=torch.float16)
+    o_ref, l_ref = fa.attention(*(t.to(torch.float16).to(DEV) for t in (q, k, v)), causal=True)
+    o, lse = fa.attention(qv, kv, vv, causal=True)
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_strided_guard_band_untouched():
+    """Strided O inside a larger buffer: nothing outside O's elements is written."""
+    q, k, v = (t.to(DEV) for t in make_qkv(1, 2, 300, 300, 64, seed=37))
+    buf = torch.full((1, 300, 2, 96), 5.0, dtype=torch.bfloat16, device=DEV)   # 32 spare features per row
+    out = buf[..., :64].transpose(1, 2)
+    fa.attention(q, k, v, causal=True, out=out)
+    torch.cuda.synchronize()
+    assert (buf[..., 64:] == 5.0).all()
+    o_ref, _ = fa.attention(q, k, v, causal=True, split=False)
+    assert torch.equal(out, o_ref)
