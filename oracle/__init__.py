@@ -74,6 +74,11 @@ class OracleLib:
                                                 ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                                 ctypes.c_double, lp, ctypes.c_long, dp, dp, dp,
                                                 ctypes.c_int]
+        lib.oracle_attn_head_keypad.restype = ctypes.c_int
+        lib.oracle_attn_head_keypad.argtypes = [dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                                ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                ctypes.c_long, ctypes.c_double, lp, ctypes.c_long,
+                                                dp, dp, dp, ctypes.c_int]
         lib.oracle_attn_bwd_head.restype = ctypes.c_int
         lib.oracle_attn_bwd_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
                                              ctypes.c_long, ctypes.c_int, ctypes.c_double,
@@ -149,6 +154,44 @@ class OracleLib:
             for h in range(H):
                 O[b, h], L[b, h] = self.attn_head_window(q[b, h], k[b, h], v[b, h], left, right,
                                                          scale, nthreads=nthreads)
+        return O, L
+
+    def attn_head_keypad(self, q, k, v, left: int, right: int, kv_len: int, scale: float,
+                         rows=None, want_p: bool = False, nthreads: int = 0):
+        """Band plus key padding (keys j >= kv_len masked) for one (batch, head) slice;
+        rows without any allowed key give O = 0, LSE = -inf.  Returns (O, LSE[, P])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        Lq, D = q.shape
+        Lk = k.shape[0]
+        if k.shape != (Lk, D) or v.shape != (Lk, D):
+            raise ValueError("k and v must be [Lk, D] with the same D as q")
+        if rows is None:
+            n, rp = Lq, None
+        else:
+            rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+            n = rows_arr.shape[0]
+            rp = rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+        O = np.empty((n, D), dtype=np.float64)
+        L = np.empty((n,), dtype=np.float64)
+        P = np.empty((n, Lk), dtype=np.float64) if want_p else None
+        rc = self.lib.oracle_attn_head_keypad(_dptr(q), _dptr(k), _dptr(v), Lq, Lk, D, int(left),
+                                              int(right), int(kv_len), float(scale), rp, n,
+                                              _dptr(O), _dptr(L), _dptr(P), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_head_keypad failed with code {rc}")
+        return (O, L, P) if want_p else (O, L)
+
+    def attn_full_keypad(self, q, k, v, left: int, right: int, kv_len, scale: float,
+                         nthreads: int = 0):
+        """Band plus per-batch key padding over [B, H, L, D] tensors: (O, LSE)."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, Lq, D = q.shape
+        O = np.empty((B, H, Lq, D))
+        L = np.empty((B, H, Lq))
+        for b in range(B):
+            for h in range(H):
+                O[b, h], L[b, h] = self.attn_head_keypad(q[b, h], k[b, h], v[b, h], left, right,
+                                                         int(kv_len[b]), scale, nthreads=nthreads)
         return O, L
 
     def attn_bwd_head(self, q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
@@ -230,6 +273,14 @@ def attn_full_window(*args, **kwargs):
 
 def attn_bwd_head(*args, **kwargs):
     return _get().attn_bwd_head(*args, **kwargs)
+
+
+def attn_head_keypad(*args, **kwargs):
+    return _get().attn_head_keypad(*args, **kwargs)
+
+
+def attn_full_keypad(*args, **kwargs):
+    return _get().attn_full_keypad(*args, **kwargs)
 
 
 def attn_bwd_full(*args, **kwargs):

@@ -218,6 +218,72 @@ int oracle_attn_head_window(const double *Q, const double *K, const double *V,
 }
 
 /*
+ * Key-padding mask on top of the band: query row i of a head whose batch has kv_len
+ * valid keys may attend to key j iff  i - left <= j <= i + right  (as in
+ * oracle_attn_head_window, -1 = unbounded) and  j < kv_len  (keys at or past kv_len
+ * are padding).  This is one of the mask variants that the "FlashAttention-2 forward
+ * in Triton" post (wsisp.com) leaves to later work.  A row whose allowed set is
+ * empty -- kv_len = 0, or a band that lies entirely in the padding -- has no softmax;
+ * the reading taken for it is O = 0 and LSE = -infinity (the log of an empty sum).
+ * kv_len is clamped to [0, Lk].  Arguments otherwise as oracle_attn_head_window.
+ */
+int oracle_attn_head_keypad(const double *Q, const double *K, const double *V,
+                            long Lq, long Lk, long D, long left, long right, long kv_len,
+                            double scale, const long *rows, long nrows,
+                            double *O, double *LSE, double *P, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE) return ORACLE_BAD_ARG;
+    if (Lq < 0 || Lk < 1 || D < 1 || nrows < 0 || left < -1 || right < -1) return ORACLE_BAD_ARG;
+    if (!rows && nrows != Lq) return ORACLE_BAD_ARG;
+    if (rows)
+        for (long r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= Lq) return ORACLE_BAD_ARG;
+    const long kv = kv_len < 0 ? 0 : (kv_len > Lk ? Lk : kv_len);
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *S = (double *)malloc(sizeof(double) * (size_t)Lk);
+        double *Pr = (double *)malloc(sizeof(double) * (size_t)Lk);
+        if (!S || !Pr) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = ORACLE_NO_MEMORY;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+            for (long r = 0; r < nrows; ++r) {
+                const long i = rows ? rows[r] : r;
+                const long lo = (left < 0 || i - left < 0) ? 0 : i - left;
+                long hi = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;
+                if (hi > kv - 1) hi = kv - 1;
+                double *p_row = P ? P + r * Lk : NULL;
+                if (lo > hi) {   /* no allowed key: O = 0, LSE = -inf */
+                    for (long d = 0; d < D; ++d) O[r * D + d] = 0.0;
+                    LSE[r] = -INFINITY;
+                    if (p_row)
+                        for (long j = 0; j < Lk; ++j) p_row[j] = 0.0;
+                    continue;
+                }
+                attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo + 1, D, hi - lo + 1, scale,
+                           S, Pr, O + r * D, LSE + r, p_row ? p_row + lo : NULL);
+                if (p_row) {
+                    for (long j = 0; j < lo; ++j) p_row[j] = 0.0;
+                    for (long j = hi + 1; j < Lk; ++j) p_row[j] = 0.0;
+                }
+            }
+        }
+        free(S);
+        free(Pr);
+    }
+    return status;
+}
+
+/*
  * Gradients of the attention of one (batch, head) slice -- the backward pass that
  * the "FlashAttention-2 forward in Triton" post (wsisp.com) leaves to later work
  * and whose principle it states: recompute the probabilities rather than store

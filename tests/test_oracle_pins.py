@@ -336,6 +336,68 @@ BWD_PINS = [pin_bwd_finite_differences, pin_bwd_constant_v, pin_bwd_sums, pin_bw
 PINS.extend(BWD_PINS)
 
 
+# --------------------------------------------------------------------------
+# Key padding: keys j >= kv_len masked on top of the band; empty rows give
+# O = 0, LSE = -inf.
+# --------------------------------------------------------------------------
+
+KEYPAD_CASES = [(9, 12, -1, -1, 7), (10, 10, -1, 0, 4), (8, 15, 3, 2, 11), (6, 6, 0, 0, 3),
+                (7, 9, -1, -1, 0), (12, 20, 2, -1, 20)]
+
+
+def pin_keypad_torch_f64(lib):
+    """Brute force with torch fp64 and explicit band and padding masks."""
+    for (Lq, Lk, left, right, kv) in KEYPAD_CASES:
+        g = torch.Generator().manual_seed(Lq * 13 + Lk + kv)
+        q = torch.randn(Lq, 6, generator=g, dtype=torch.float64)
+        k = torch.randn(Lk, 6, generator=g, dtype=torch.float64)
+        v = torch.randn(Lk, 6, generator=g, dtype=torch.float64)
+        i = torch.arange(Lq)[:, None]
+        j = torch.arange(Lk)[None, :]
+        keep = (j < kv) & (i >= 0)   # [Lq, Lk]
+        if left >= 0:
+            keep = keep & (j >= i - left)
+        if right >= 0:
+            keep = keep & (j <= i + right)
+        s = (q @ k.T * 0.3).masked_fill(~keep, float("-inf"))
+        O, L = lib.attn_head_keypad(q.numpy(), k.numpy(), v.numpy(), left, right, kv, 0.3)
+        full = keep.any(dim=1)
+        ref_o = torch.where(full[:, None], torch.softmax(s, -1).nan_to_num(0.0) @ v, torch.zeros(1, dtype=torch.float64))
+        np.testing.assert_allclose(O, ref_o.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L[full.numpy()], torch.logsumexp(s, -1)[full].numpy(), rtol=0, atol=1e-12)
+        assert np.all(np.isneginf(L[~full.numpy()])) and np.all(O[~full.numpy()] == 0.0)
+
+
+def pin_keypad_uniform(lib):
+    """Q = 0: the mean of the values of the unpadded part of the band, LSE = ln(count)."""
+    for (Lq, Lk, left, right, kv) in KEYPAD_CASES:
+        q, k, v = np.zeros((Lq, 4)), _rand((Lk, 4), 90), _rand((Lk, 4), 91)
+        O, L = lib.attn_head_keypad(q, k, v, left, right, kv, 1.0)
+        for i in range(Lq):
+            lo, hi = _window(i, Lk, left, right)
+            hi = min(hi, kv - 1)
+            if lo > hi:
+                assert np.isneginf(L[i]) and np.all(O[i] == 0.0)
+            else:
+                np.testing.assert_allclose(O[i], v[lo:hi + 1].mean(axis=0), rtol=0, atol=1e-12)
+                assert abs(L[i] - math.log(hi - lo + 1)) < 1e-12
+
+
+def pin_keypad_no_padding_is_window(lib):
+    """kv_len >= Lk: exactly the band oracle."""
+    q, k, v = _rand((11, 5), 92), _rand((13, 5), 93), _rand((13, 5), 94)
+    for (left, right) in ((-1, -1), (-1, 0), (4, 2)):
+        a = lib.attn_head_keypad(q, k, v, left, right, 13, 0.6)
+        b = lib.attn_head_window(q, k, v, left, right, 0.6)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+        c = lib.attn_head_keypad(q, k, v, left, right, 99, 0.6)   # clamped to Lk
+        assert np.array_equal(c[0], b[0])
+
+
+KEYPAD_PINS = [pin_keypad_torch_f64, pin_keypad_uniform, pin_keypad_no_padding_is_window]
+PINS.extend(KEYPAD_PINS)
+
+
 def test_window_rejects_empty_rows(oracle_mod):
     q, k, v = _rand((5, 4), 1), _rand((3, 4), 2), _rand((3, 4), 3)
     with pytest.raises(ValueError):   # row 4 would need key 4 >= Lk
@@ -369,12 +431,16 @@ MUTATIONS = {
     "lse_missing_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "no_normalisation": ("for (long j = 0; j < n_allowed; ++j) P[j] /= l;", ";"),
     "causal_ignored": ("if (!causal) return Lk;", "return Lk;"),
-    "window_drops_last_key": ("attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo + 1, D, hi - lo + 1, scale,",
-                              "attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo, D, hi - lo, scale,"),
+    "window_drops_last_key": ("double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo + 1, D, hi - lo + 1, scale,",
+                              "double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo, D, hi - lo, scale,"),
+    "keypad_empty_row_not_zeroed": ("for (long d = 0; d < D; ++d) O[r * D + d] = 0.0;\n                    LSE[r] = -INFINITY;",
+                                    "for (long d = 0; d < D; ++d) O[r * D + d] = 0.0;\n                    LSE[r] = 0.0;"),
     "bwd_softmax_jacobian_without_row_term": ("ds[j] = p[j] * (ds[j] - pdp);", "ds[j] = p[j] * ds[j];"),
     "bwd_dk_missing_scale": ("dK[j * D + d] = scale * ak;", "dK[j * D + d] = ak;"),
     "bwd_dv_from_queries": ("av += P[i * Lk + j] * dO[i * D + d];", "av += P[i * Lk + j] * Q[i * D + d];"),
-    "window_shifted_values": ("attend_row(Q + i * D, K + lo * D, V + lo * D,", "attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
+    "keypad_last_key_kept": ("if (hi > kv - 1) hi = kv - 1;", "if (hi > kv) hi = kv;"),
+    "window_shifted_values": ("double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D,",
+                              "double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
 }
 
 
