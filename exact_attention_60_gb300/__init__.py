@@ -39,7 +39,7 @@ def workspace_for(B, H, Lq, Lk, D, causal, device):
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-              stream=None, split: bool = True, window=None):
+              stream=None, split: bool = True, window=None, kv_len=None):
     """O, LSE = exact attention of contiguous bf16 CUDA tensors q [B,H,Lq,D], k/v [B,H,Lk,D].
 
     Allocates ``out`` (bf16 [B,H,Lq,D]) and ``lse`` (fp32 [B,H,Lq]) if not given.  With
@@ -54,6 +54,10 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     q, k, v (and ``out``) may also be fp16, or strided views of shape [B, H, L, D] with a
     contiguous last dimension (for instance slices of a packed [B, L, 3, H, D] projection);
     those calls go to fa_fwd_strided.  ``out`` defaults to a contiguous tensor of q's dtype.
+
+    ``kv_len`` (an int32 CUDA tensor of B key counts) masks keys j >= kv_len[b] of batch b
+    (key padding, on top of ``causal`` / ``window``); a row left without keys gets O = 0
+    and LSE = -inf.
     """
     import torch
     B, H, Lq, D = q.shape
@@ -74,7 +78,11 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
     if lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor")
-    plain = dtype == torch.bfloat16 and all(t.is_contiguous() for t in (q, k, v, out))
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda
+                               or kv_len.numel() != B or not kv_len.is_contiguous()):
+        raise ValueError("kv_len must be a contiguous int32 CUDA tensor of B entries")
+    plain = (dtype == torch.bfloat16 and kv_len is None
+             and all(t.is_contiguous() for t in (q, k, v, out)))
     if not plain:
         if out.dtype != dtype or out.shape != q.shape or out.stride(3) != 1:
             raise ValueError("out must have q's dtype and shape and a contiguous last dim")
@@ -84,9 +92,11 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         ws, nbytes = (workspace_for(B, H, Lq, Lk, D, False, q.device)
                       if split and (left, right) == (-1, -1) else (None, 0))
         code = FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16
+        if kv_len is not None:
+            ws, nbytes = None, 0
         st = fa_fwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], out,
-                            out.stride()[:3], lse, B, H, Lq, Lk, D, left, right, scale, code,
-                            ws, nbytes, stream)
+                            out.stride()[:3], lse, kv_len, B, H, Lq, Lk, D, left, right, scale,
+                            code, ws, nbytes, stream)
         if st != FA_OK:
             raise FaError(st)
         return out, lse

@@ -51,7 +51,7 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 7 + [ctypes.c_float, vp]
     lp3 = ctypes.POINTER(ctypes.c_longlong)
     lib.fa_fwd_strided.restype = ctypes.c_int
-    lib.fa_fwd_strided.argtypes = [vp, lp3, vp, lp3, vp, lp3, vp, lp3, vp] + [ctypes.c_int] * 7 + \
+    lib.fa_fwd_strided.argtypes = [vp, lp3, vp, lp3, vp, lp3, vp, lp3, vp, vp] + [ctypes.c_int] * 7 + \
         [ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -127,13 +127,14 @@ def _strides3(st):
     return (ctypes.c_longlong * 3)(a, b, c)
 
 
-def fa_fwd_strided(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, LSE, B, H, Lq, Lk, D,
-                   window_left, window_right, scale, dtype, workspace=None, workspace_bytes=0,
+def fa_fwd_strided(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, LSE, kv_len, B, H, Lq, Lk,
+                   D, window_left, window_right, scale, dtype, workspace=None, workspace_bytes=0,
                    stream=None) -> int:
-    """C ``fa_fwd_strided``; strides are sequences of three element strides."""
+    """C ``fa_fwd_strided``; strides are sequences of three element strides; ``kv_len`` a
+    device int32 array of per-batch key counts, or None."""
     return load().fa_fwd_strided(_ptr(Q), _strides3(q_stride), _ptr(K), _strides3(k_stride),
                                  _ptr(V), _strides3(v_stride), _ptr(O), _strides3(o_stride),
-                                 _ptr(LSE), int(B), int(H), int(Lq), int(Lk), int(D),
+                                 _ptr(LSE), _ptr(kv_len), int(B), int(H), int(Lq), int(Lk), int(D),
                                  int(window_left), int(window_right), float(scale), int(dtype),
                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
 

@@ -149,6 +149,8 @@ struct Params {
   int win_left;       // band schedule: key j allowed for row i iff i - win_left <= j <= i + win_right,
   int win_right;      //   -1 = unbounded on that side; both are below Lq / Lk
   int band_desc;      // band schedule: 1 = units in descending query order (heavier last tiles)
+  const int* kv_len;  // band schedule: per-batch count of valid keys (keys j >= kv_len[b] are
+                      //   padding), device memory; nullptr = none
   float scale_log2;   // scale * log2(e)
   uint32_t flags;     // test hooks (fa_debug_set)
   unsigned long long wait_limit_ns;
@@ -173,6 +175,7 @@ struct Unit {
   int nblk[2];   // key tiles of query tile 0 and 1 in this part (0 = tile absent)
   int first[2];  // band schedule: key tile (relative to kv0) where query tile i starts
   int nmax;      // key tiles loaded for the unit: the union of the tiles' ranges
+  int kvl;       // band schedule: valid keys of the unit's batch (Lk without padding)
   int partial;   // 1: a part of a unit split across CTAs
   int slot;      // workspace slot of this part: 2 * CTA + (first part of the CTA ? 0 : 1)
 };
@@ -192,14 +195,15 @@ __device__ __forceinline__ void unit_rows(const Params& p, int idx, Unit& u) {
   }
 }
 
-// Band schedule: allowed keys of row q are [band_lo(q), band_lim(q)).
+// Band schedule: allowed keys of row q are [band_lo(q), band_lim(q, kvl)), where kvl is
+// the number of valid (unpadded) keys of the row's batch.
 __device__ __forceinline__ int band_lo(const Params& p, int q) {
   return p.win_left < 0 ? 0 : max(0, q - p.win_left);
 }
-__device__ __forceinline__ int band_lim(const Params& p, int q) {
+__device__ __forceinline__ int band_lim(const Params& p, int q, int kvl) {
   return p.win_right < 0
-             ? p.Lk
-             : static_cast<int>(min(static_cast<long long>(p.Lk),
+             ? kvl
+             : static_cast<int>(min(static_cast<long long>(kvl),
                                     static_cast<long long>(q) + p.win_right + 1));
 }
 
@@ -217,10 +221,11 @@ __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
     const int pair = p.band_desc ? p.n_pairs - 1 - pi : pi;
     u.bh = idx % p.bh_count;
     u.q0 = pair * 2 * kBlockM;
+    u.kvl = p.kv_len ? min(max(__ldg(p.kv_len + u.bh / p.H), 0), p.Lk) : p.Lk;
     // Tile i covers key tiles a[i]..b[i]: from the band's left edge at its first
-    // row to its right edge at its last stored row (the band only moves right as
-    // the row grows, and every row's band is non-empty).  The two ranges overlap or
-    // touch, so the unit loads one contiguous run of key tiles.
+    // row to its right edge at its last stored row (both edges only move right as the
+    // row grows).  The two ranges overlap or touch, so the unit loads one contiguous
+    // run of key tiles.  With key padding a tile's range can be empty (b < a).
     int a[2], b[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -231,14 +236,15 @@ __device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
         continue;
       }
       const int last = min(qt + kBlockM, p.Lq) - 1;   // last row that is stored
-      a[i] = band_lo(p, qt) / kBlockN;
-      b[i] = (band_lim(p, last) - 1) / kBlockN;
+      const int lo = band_lo(p, qt), lim = band_lim(p, last, u.kvl);
+      a[i] = lo / kBlockN;
+      b[i] = lim > lo ? (lim - 1) / kBlockN : a[i] - 1;
     }
     u.kv0 = a[0];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      u.first[i] = a[i] - a[0];
-      u.nblk[i] = b[i] - a[i] + 1;   // 0 when the tile is absent
+      u.nblk[i] = max(0, b[i] - a[i] + 1);   // 0 when the tile is absent or has no keys
+      u.first[i] = u.nblk[i] > 0 ? a[i] - a[0] : 0;
     }
     u.nmax = max(u.nblk[0], u.first[1] + u.nblk[1]);
     u.partial = 0;
@@ -425,17 +431,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     Unit u;
     for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
       const int n_blocks = wg ? u.nblk[1] : u.nblk[0];
-      if (n_blocks == 0) continue;
+      if (n_blocks == 0) {
+        // Band schedule: a present tile whose rows have no allowed key (key padding):
+        // O = 0 and LSE = -inf, written here without any MMA.
+        if constexpr (kBand) {
+          const int qz = u.q0 + wg * kBlockM + row;
+          if (qz < p.Lq) {
+            const int zb = u.bh / p.H, zh = u.bh - zb * p.H;
+            uint16_t* zrow = p.o + zb * p.o_sb + zh * p.o_sh + static_cast<long long>(qz) * p.o_sl;
+#pragma unroll
+            for (int c = 0; c < HD; c += 8) *reinterpret_cast<uint4*>(zrow + c) = make_uint4(0, 0, 0, 0);
+            p.lse[static_cast<size_t>(u.bh) * p.Lq + qz] = -INFINITY;
+          }
+        }
+        continue;
+      }
       const int bh = u.bh;
       const int qt = u.q0 + wg * kBlockM;
       const int q = qt + row;
-      const int key_lim = kBand ? band_lim(p, q) : (p.causal ? min(p.Lk, q + 1) : p.Lk);
+      const int key_lim = kBand ? band_lim(p, q, u.kvl) : (p.causal ? min(p.Lk, q + 1) : p.Lk);
       const int first_diag = p.causal ? qt / kBlockN : INT_MAX;
       // Band: row q keeps keys [key_lo, key_lim); a key tile needs masking when the
       // band's left edge (of the tile's last row) or right edge (of its first row) cuts it.
       const int key_lo = kBand ? band_lo(p, q) : 0;
       const int lo_last = kBand ? band_lo(p, qt + kBlockM - 1) : 0;
-      const int lim_first = kBand ? band_lim(p, qt) : 0;
+      const int lim_first = kBand ? band_lim(p, qt, u.kvl) : 0;
       const int jb0 = kBand ? u.kv0 + (wg ? u.first[1] : u.first[0]) : (kSplit ? u.kv0 : 0);
       float m = -INFINITY;   // running max of scaled scores, log2 units (possibly stale by < 8)
       float l = 0.0f;        // running sum of exp2(s*sl2 - m)
@@ -575,7 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         continue;
       }
       // Epilogue: O / l as bf16 rows, LSE = ln2 * (m + log2 l); rows >= Lq are not stored.
-      const float inv_l = 1.0f / l;
+      // (band schedule: a row with no allowed key has l = 0 and gets O = 0, LSE = -inf)
+      const float inv_l = kBand ? (l > 0.0f ? 1.0f / l : 0.0f) : 1.0f / l;
       const bool store = q < p.Lq;
       const int ob = bh / p.H, oh = bh - ob * p.H;
       uint16_t* orow = p.o + ob * p.o_sb + oh * p.o_sh + static_cast<long long>(store ? q : 0) * p.o_sl;
@@ -704,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         // softmax has read the tile's previous S), then the P V GEMMs of key tile j.
         uint32_t s_iss[2] = {0, 0};   // S_i GEMMs issued so far (s_free phase)
         for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+          if (kBand && u.nmax == 0) continue;   // no keys at all (key padding): nothing to issue
           const int nblk[2] = {u.nblk[0], u.nblk[1]};
           const int nmax = u.nmax;
           const int fst[2] = {0, kBand ? u.first[1] : 0};
@@ -798,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
       }
       for (int r = 0; !L::kDecoupled && ok && unit_of<kS>(p, r, u); ++r) {
+        if (kBand && u.nmax == 0) continue;   // no keys at all (key padding): nothing to issue
         const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
         const int nblk[2] = {nb0, nb1};
         // Step j of the unit (key tile kv0 + j) is step j - fst[i] of query tile i.
@@ -1160,6 +1183,7 @@ struct Problem {
   int win_left = -1;     // key j allowed for row i iff i - win_left <= j <= i + win_right
   int win_right = -1;    //   (-1: unbounded side)
   bool f16 = false;      // fp16 instead of bf16 inputs and output
+  const int* kv_len = nullptr;   // per-batch valid keys (device), band schedule only
   int B = 0, H = 0;
   long long qs[3] = {0, 0, 0}, ks[3] = {0, 0, 0}, vs[3] = {0, 0, 0}, os[3] = {0, 0, 0};   // element strides {batch, head, row}
 };
@@ -1271,6 +1295,7 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   p.win_right = pr.win_right;
   // Heaviest units first: the last query tiles unless only the left side is bounded.
   p.band_desc = (pr.win_left >= 0 && pr.win_right < 0) ? 0 : 1;
+  p.kv_len = pr.kv_len;
   p.total_steps = static_cast<long long>(pr.n_units) * pr.nkv;
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
@@ -1481,9 +1506,10 @@ bool no_self_overlap(long long B, long long H, long long L, int D, const long lo
 extern "C" fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K,
                                     const long long* k_stride, const void* V,
                                     const long long* v_stride, void* O, const long long* o_stride,
-                                    float* LSE, int B, int H, int Lq, int Lk, int D,
-                                    int window_left, int window_right, float scale, int dtype,
-                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                                    float* LSE, const int* kv_len, int B, int H, int Lq, int Lk,
+                                    int D, int window_left, int window_right, float scale,
+                                    int dtype, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
   if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
@@ -1515,7 +1541,10 @@ extern "C" fa_status fa_fwd_strided(const void* Q, const long long* q_stride, co
   int left = window_left, right = window_right;
   if (left >= Lq - 1) left = -1;
   if (right >= Lk - 1) right = -1;
-  if (left >= 0 && Lq - 1 - left > Lk - 1) return FA_ERR_INVALID_ARG;   // a row without keys
+  // A row without keys is an argument error, except with key padding, where lengths in
+  // device memory can empty any row and such rows get O = 0, LSE = -inf.
+  if (!kv_len && left >= 0 && Lq - 1 - left > Lk - 1) return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
 
   Problem pr{};
   pr.Q = Q;
@@ -1548,7 +1577,8 @@ extern "C" fa_status fa_fwd_strided(const void* Q, const long long* q_stride, co
   if (prep != FA_OK) return prep;
   const bool force_band = (g_debug_flags.load() & 4u) != 0;
   Plan pl{};
-  if (!force_band && left < 0 && (right < 0 || right == 0)) {
+  pr.kv_len = kv_len;
+  if (!kv_len && !force_band && left < 0 && (right < 0 || right == 0)) {
     pr.causal = (right == 0) ? 1 : 0;
     pl = plan_schedule(pr, sm_count);
     if (pl.split) {   // the split schedule only with a workspace that fits

@@ -164,6 +164,14 @@ fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O, fl
  *              must not meet Q, K, V or LSE (checked on the byte spans the tensors cover).
  *   O        : device pointer, elements of `dtype`, written (round to nearest even).
  *   LSE      : fp32 device pointer, contiguous [B,H,Lq] (as fa_fwd).
+ *   kv_len   : NULL, or a 4-byte aligned device array of B int32 key counts: key
+ *              padding, another of the mask variants the post leaves to later work.
+ *              Keys j >= kv_len[b] (clamped to [0, Lk]) are masked for every head and
+ *              query of batch b, on top of the band.  The values are read by the kernel,
+ *              so the host cannot see them: a row left with no allowed key (kv_len[b] = 0,
+ *              or a band lying wholly in the padding) gets O = 0 and LSE = -inf instead
+ *              of the argument error the band alone would give.  Key padding always runs
+ *              the band schedule (never the split one).
  *   window_left, window_right : the band of fa_fwd_window; (-1, -1) is the full softmax
  *              and (-1, 0) the causal mask.
  *   workspace, workspace_bytes : optional (NULL, 0); with the full mask, a workspace of
@@ -177,9 +185,10 @@ fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O, fl
  */
 fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K,
                          const long long* k_stride, const void* V, const long long* v_stride,
-                         void* O, const long long* o_stride, float* LSE, int B, int H, int Lq,
-                         int Lk, int D, int window_left, int window_right, float scale, int dtype,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                         void* O, const long long* o_stride, float* LSE, const int* kv_len,
+                         int B, int H, int Lq, int Lk, int D, int window_left, int window_right,
+                         float scale, int dtype, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
 
 /*
  * fa_fwd_noalloc -- fa_fwd_ws without a workspace argument, for callers that

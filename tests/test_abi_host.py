@@ -190,7 +190,7 @@ def call_strided(qs=(32768, 2048, 64), ks=(32768, 2048, 64), vs=(32768, 2048, 64
     a = dict(Q=ALIGNED, K=2 * ALIGNED, V=3 * ALIGNED, O=4 * ALIGNED, LSE=5 * ALIGNED, B=2, H=16,
              Lq=32, Lk=32, D=64, left=-1, right=-1, scale=0.125, ws=None, wsb=0)
     a.update(kw)
-    return fa.fa_fwd_strided(a["Q"], qs, a["K"], ks, a["V"], vs, a["O"], os_, a["LSE"], a["B"], a["H"],
+    return fa.fa_fwd_strided(a["Q"], qs, a["K"], ks, a["V"], vs, a["O"], os_, a["LSE"], a.get("kv"), a["B"], a["H"],
                              a["Lq"], a["Lk"], a["D"], a["left"], a["right"], a["scale"], dtype,
                              a["ws"], a["wsb"], 0)
 
@@ -208,6 +208,7 @@ def call_strided(qs=(32768, 2048, 64), ks=(32768, 2048, 64), vs=(32768, 2048, 64
     (dict(D=96), fa.FA_ERR_UNSUPPORTED),
     (dict(Q=ALIGNED + 8), fa.FA_ERR_INVALID_ARG),                           # misaligned
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(kv=6 * ALIGNED + 2), fa.FA_ERR_INVALID_ARG),                      # kv_len misaligned
 ])
 def test_fwd_strided_rejects_bad_arguments_before_any_cuda_call(lib, kw, expect):
     assert call_strided(**kw) == expect
@@ -215,7 +216,7 @@ def test_fwd_strided_rejects_bad_arguments_before_any_cuda_call(lib, kw, expect)
 
 def test_fwd_strided_accepts_shared_inputs_and_empty(lib):
     # empty problems need no pointers
-    assert fa.fa_fwd_strided(None, None, None, None, None, None, None, None, None, 0, 4, 16, 16, 64,
-                             -1, -1, 0.125, 0, None, 0, 0) == fa.FA_OK
+    assert fa.fa_fwd_strided(None, None, None, None, None, None, None, None, None, None, 0, 4, 16, 16,
+                             64, -1, -1, 0.125, 0, None, 0, 0) == fa.FA_OK
     # a missing stride array with work to do is an argument error
     assert call_strided(qs=None) == fa.FA_ERR_INVALID_ARG
