@@ -413,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
+  // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
+  // above overlapped its tail; nothing in global memory is touched before it completes.
+  // The next kernel may be scheduled now (it waits the same way before touching memory).
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
@@ -972,6 +977,7 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
   __shared__ int s_nparts, s_bh, s_q0;
   const int b = blockIdx.x + 1;   // boundary between CTA b-1 and CTA b
   const int tile = blockIdx.y;
+  ptx::grid_dependency_wait();   // the parts come from the attention kernel before this one
   if (threadIdx.x == 0) {
     const long long G = c.grid;
     auto lo = [&](long long g) { return c.total_steps * g / G; };
@@ -1318,6 +1324,20 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   cfg.blockDim = dim3(fa::kThreads);
   cfg.stream = stream;
   cfg.dynamicSmemBytes = (pr.D == 64) ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc;
+  // Programmatic dependent launch for short kernels: the kernel's set-up may overlap the
+  // previous kernel in the stream (it waits for it with griddepcontrol.wait before
+  // touching memory), which hides the launch gap.  Used when a CTA's share of the work
+  // is at most 256 key-tile steps (about a quarter of a millisecond): side by side it
+  // gained 11-13 % on 1K-token D = 64 batches and 2 % on 4K causal, while on 16K causal
+  // (about 430 steps per CTA) it gave 1620-1784 TFLOP/s against a steady 1761-1782.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const long long steps_per_cta =
+      static_cast<long long>(pr.n_units) * pr.nkv / std::max(1, pl.grid);
+  const bool dependent_launch = steps_per_cta <= 256;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent_launch ? 1 : 0;
   const int sched = pl.band ? fa::kSchedBand : pl.split ? fa::kSchedSplit : fa::kSchedWhole;
   cudaError_t err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched, pr.f16), p);
   if (err != cudaSuccess) return FA_ERR_CUDA;
@@ -1342,6 +1362,8 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
     cc.gridDim = dim3(static_cast<unsigned>(pl.grid - 1), 2, fa::kBlockM / fa::kCombineRows);
     cc.blockDim = dim3(128);
     cc.stream = stream;
+    cc.attrs = attr;
+    cc.numAttrs = dependent_launch ? 1 : 0;
     if (pr.f16)
       err = (pr.D == 64) ? cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<64, true>, c)
                          : cudaLaunchKernelEx(&cc, fa::fa_combine_kernel<128, true>, c);
