@@ -20,14 +20,16 @@
 //                         query tiles that see it.  TMEM: S^T | dP^T | dV | dK.
 //                           S^T  = K Q^T,  dP^T = V dO^T        (A, B in smem)
 //                           dV  += P^T dO, dK  += dS^T Q        (A = P^T / dS^T in TMEM)
-//                         One warpgroup (thread = key row) turns S^T into P^T
-//                         (bf16, over S^T) and dP^T into dS^T (bf16, over dP^T).
+//                         Two warpgroups (thread = key row, 64 columns each) turn
+//                         S^T into P^T (bf16, over S^T) and dP^T into dS^T (bf16,
+//                         over dP^T).
 //   fa_bwd_dq_kernel    : one unit = one 128-query tile; streams its key tiles.
 //                         TMEM: S | dP | dQ.  S = Q K^T, dP = dO V^T, dQ += dS K.
 // Splitting dQ from dK/dV costs two extra GEMMs per tile pair but needs no
-// atomics and no dQ accumulator in global memory.  Roles per CTA (192 threads):
-// warps 0-3 compute warpgroup, warp 4 TMA loads, warp 5 MMA issue (the whole warp
-// runs the loop; one elected lane issues each tcgen05.mma / commit).  Every wait
+// atomics and no dQ accumulator in global memory.  Roles per CTA (320 threads):
+// warps 0-7 two compute warpgroups sharing each row's columns, warp 8 TMA loads, warp
+// 9 MMA issue (the whole warp runs the loop; one elected lane issues each tcgen05.mma /
+// commit).  Every wait
 // is bounded in time; a wait that runs out records FA_ERR_TIMEOUT in this file's
 // status word (read by fa_last_device_status) and every role drains and exits.
 #include <cuda.h>
@@ -53,9 +55,19 @@ namespace ptx = fa::ptx;
 __device__ unsigned int g_bwd_status;
 
 constexpr int kBlk = 128;          // rows per tile (queries or keys), one M=128 MMA
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;     // two compute warpgroups, load warp, MMA warp
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kComputeThreads = 256;
+
+// The per-element work of the backward pass (P from S and the saved LSE, dS from P, dP
+// and Delta) needs no reduction along a row, so the two compute warpgroups share each
+// row: warpgroup g takes columns [64g, 64g + 64) of S (dP) and writes its 32 packed
+// bf16 columns of P (dS) over the first half of that range, which only it has read.
+// The A operand of the next MMA (K = 128) is then columns [0, 32) and [64, 96).
+__device__ __forceinline__ uint32_t packed_col(int kk) {   // TMEM column of K-slice kk (16 rows)
+  return kk < 4 ? 8u * kk : 64u + 8u * (kk - 4);
+}
 constexpr unsigned long long kDefaultWaitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -223,10 +235,10 @@ struct DkdvLayout {
   static constexpr int kBarQdEmpty = kBarQdFull + kStages;      // [kStages]
   static constexpr int kBarSFull = kBarQdEmpty + kStages;
   static constexpr int kBarDpFull = kBarSFull + 1;
-  static constexpr int kBarPFull = kBarDpFull + 1;              // count 128
-  static constexpr int kBarDsFull = kBarPFull + 1;              // count 128
+  static constexpr int kBarPFull = kBarDpFull + 1;              // count 256 (compute threads)
+  static constexpr int kBarDsFull = kBarPFull + 1;              // count 256 (compute threads)
   static constexpr int kBarAccFull = kBarDsFull + 1;
-  static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 128
+  static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 256 (compute threads)
   static constexpr int kBarDrain = kBarAccEmpty + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffAbort = kOffBar + kNumBars * 8;
@@ -263,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     }
     ptx::mbar_init(bar(L::kBarSFull), 1);
     ptx::mbar_init(bar(L::kBarDpFull), 1);
-    ptx::mbar_init(bar(L::kBarPFull), 128);
-    ptx::mbar_init(bar(L::kBarDsFull), 128);
+    ptx::mbar_init(bar(L::kBarPFull), kComputeThreads);
+    ptx::mbar_init(bar(L::kBarDsFull), kComputeThreads);
     ptx::mbar_init(bar(L::kBarAccFull), 1);
-    ptx::mbar_init(bar(L::kBarAccEmpty), 128);
+    ptx::mbar_init(bar(L::kBarAccEmpty), kComputeThreads);
     ptx::mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -281,12 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
 
-  if (warp < 4) {
-    // ------------------------------------------------ compute warpgroup: thread = key row
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + L::kColS;
-    const uint32_t t_dp = tmem + lane_off + L::kColDp;
+  if (warp < 8) {
+    // ------------------------------------------------ compute warpgroups: thread = key row
+    const int g = warp >> 2;                   // columns [64g, 64g + 64) of the row
+    const int rw = warp & 3;                   // TMEM lane quarter this warp may access
+    const int row = rw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(rw * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::kColS + 64 * g;
+    const uint32_t t_dp = tmem + lane_off + L::kColDp + 64 * g;
     const float sl2 = p.scale_log2;
     uint32_t it = 0;          // query tiles processed (s_full, dp_full phases; ring position)
     uint32_t acc_count = 0;   // units whose accumulators were read
@@ -299,19 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const int n = max(0, p.nq - q_first);
       const int k = kt * kBlk + row;   // this thread's key
       const size_t orow = (static_cast<size_t>(bh) * p.Lk + (k < p.Lk ? k : 0)) * HD;
+      __nv_bfloat16* mine = (g ? p.dk : p.dv) + orow;   // warpgroup 0 writes dV, 1 writes dK
       if (n == 0) {   // no query sees these keys: their gradients are zero
-        if (k < p.Lk) {
-          for (int c = 0; c < HD; c += 8) {
-            *reinterpret_cast<uint4*>(p.dv + orow + c) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(p.dk + orow + c) = make_uint4(0, 0, 0, 0);
-          }
-        }
+        if (k < p.Lk)
+          for (int c = 0; c < HD; c += 8) *reinterpret_cast<uint4*>(mine + c) = make_uint4(0, 0, 0, 0);
         continue;
       }
       for (int t = 0; t < n; ++t, ++it) {
         const int qt = q_first + t;
         const int s = static_cast<int>(it % L::kStages);
-        const float* lse2 = reinterpret_cast<const float*>(smem + stage_off(s) + 2 * T::kTileBytes);
+        const float* lse2 = reinterpret_cast<const float*>(smem + stage_off(s) + 2 * T::kTileBytes) + 64 * g;
         const float* dlt = lse2 + kBlk;
         // the stage's LSE and Delta (bulk copies) are read here: wait for the stage
         // itself, and for S^T, which the MMA warp commits
@@ -320,59 +331,51 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
                                          wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t sr[128];
-        ptx::tmem_ld32x32b_x128(t_s, sr);
+        uint32_t sr[2][32];
+        ptx::tmem_ld32x32b_x32(t_s, sr[0]);
+        ptx::tmem_ld32x32b_x32(t_s + 32, sr[1]);
         // P^T_kq = exp2(sl2 * S - lse_q * log2e); padded queries carry lse2 = +inf (P = 0)
-        float pr[128];
+        float pr[64];
         const bool diag = p.causal && qt == kt;   // causal: query q >= key k
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2[c]));
-          pr[c] = (diag && c < row) ? 0.0f : x;
+        for (int c = 0; c < 64; ++c) {
+          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
+          pr[c] = (diag && 64 * g + c < row) ? 0.0f : x;
         }
         uint32_t pk[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(pr[64 * h + 2 * c], pr[64 * h + 2 * c + 1]);
-          ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
-        }
+        for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        ptx::tmem_st32x32b_x32(t_s, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarPFull));
-        // dS^T_kq = P^T_kq (dP^T_kq - Delta_q), in four 32-column chunks; each chunk's bf16
-        // result lands in columns already read.
+        // dS^T_kq = P^T_kq (dP^T_kq - Delta_q); the packed result lands over this warpgroup's
+        // first 32 dP^T columns, after both halves have been read.
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
+        ptx::tmem_ld32x32b_x32(t_dp, sr[0]);
+        ptx::tmem_ld32x32b_x32(t_dp + 32, sr[1]);
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t d[32];
-          ptx::tmem_ld32x32b_x32(t_dp + c0, d);
-          uint32_t q16[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float a = pr[c0 + 2 * c] * (__uint_as_float(d[2 * c]) - dlt[c0 + 2 * c]);
-            const float b = pr[c0 + 2 * c + 1] * (__uint_as_float(d[2 * c + 1]) - dlt[c0 + 2 * c + 1]);
-            q16[c] = ptx::pack_bf16x2(a, b);
-          }
-          ptx::tmem_st32x32b_x16(t_dp + c0 / 2, q16);
+        for (int c = 0; c < 32; ++c) {
+          const float a = pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt[2 * c]);
+          const float b = pr[2 * c + 1] * (__uint_as_float(sr[c >> 4][(2 * c + 1) & 31]) - dlt[2 * c + 1]);
+          pk[c] = ptx::pack_bf16x2(a, b);
         }
+        ptx::tmem_st32x32b_x32(t_dp, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarDsFull));
       }
       if (!ok) break;
-      // Epilogue: dV and scale * dK of this thread's key row.
+      // Epilogue: warpgroup 0 writes dV, warpgroup 1 scale * dK, of this thread's key row.
       ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarAccFull), acc_count & 1, abort_flag, limit, kSiteEpilogue));
       if (!ok) break;
       ++acc_count;
       ptx::tc_fence_after();
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t t_acc = tmem + lane_off + (which ? L::kColDk : L::kColDv);
-        const float mul = which ? p.scale : 1.0f;
-        __nv_bfloat16* dst = (which ? p.dk : p.dv) + orow;
+      {
+        const uint32_t t_acc = tmem + lane_off + (g ? L::kColDk : L::kColDv);
+        const float mul = g ? p.scale : 1.0f;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t a[32];
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
           if (k < p.Lk) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-              reinterpret_cast<uint4*>(dst + c0)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+              reinterpret_cast<uint4*>(mine + c0)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
           }
         }
       }
@@ -464,9 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     // acc (+)= X^T B, X^T (bf16) in TMEM columns a_col, B MN-major [128 queries x HD].
     auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint64_t b, bool accumulate) {
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk)
-        ptx::mma_ts_warp(tmem + d_col, tmem + a_col + kk * 8, b + ((kk * 16 * 128) >> 4), kIdescAcc,
-                         (accumulate || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kBlk / 16; ++kk)   // X^T packed by the two warpgroups
+        ptx::mma_ts_warp(tmem + d_col, tmem + a_col + packed_col(kk), b + ((kk * 16 * 128) >> 4),
+                         kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
     };
     uint32_t it = 0, units = 0, acc_units = 0;
     bool ok = true;
@@ -543,21 +546,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
 template <int HD>
 struct DqLayout {
   using T = Tiles<HD>;
-  static constexpr int kStages = (HD == 128) ? 2 : 4;           // (K, V) ring
+  // Separate K and V rings: K is read twice per key tile (S early, dQ last) and V once
+  // (dP), so K gets the deeper ring and each V slot is freed as soon as its dP is done.
+  static constexpr int kKStages = (HD == 128) ? 3 : 4;
+  static constexpr int kVStages = (HD == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDo = T::kTileBytes;
-  static constexpr int kOffStage = 2 * T::kTileBytes;
-  static constexpr int kStageBytes = 2 * T::kTileBytes;          // K | V
-  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  static constexpr int kOffK = 2 * T::kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * T::kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * T::kTileBytes;
   static constexpr int kBarQdFull = 0, kBarQdEmpty = 1;
-  static constexpr int kBarKvFull = 2;                          // [kStages]
-  static constexpr int kBarKvEmpty = kBarKvFull + kStages;      // [kStages]
-  static constexpr int kBarSFull = kBarKvEmpty + kStages;
-  static constexpr int kBarSFree = kBarSFull + 1;               // count 128
+  static constexpr int kBarKFull = 2;                           // [kKStages]
+  static constexpr int kBarKEmpty = kBarKFull + kKStages;       // [kKStages]
+  static constexpr int kBarVFull = kBarKEmpty + kKStages;       // [kVStages]
+  static constexpr int kBarVEmpty = kBarVFull + kVStages;       // [kVStages]
+  static constexpr int kBarSFull = kBarVEmpty + kVStages;
+  static constexpr int kBarSFree = kBarSFull + 1;               // count 256 (compute threads)
   static constexpr int kBarDpFull = kBarSFree + 1;
-  static constexpr int kBarDsFull = kBarDpFull + 1;             // count 128
+  static constexpr int kBarDsFull = kBarDpFull + 1;             // count 256 (compute threads)
   static constexpr int kBarAccFull = kBarDsFull + 1;
-  static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 128
+  static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 256 (compute threads)
   static constexpr int kBarDrain = kBarAccEmpty + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffAbort = kOffBar + kNumBars * 8;
@@ -569,6 +577,7 @@ struct DqLayout {
   static constexpr uint32_t kTmemCols = 512;
 };
 static_assert(DqLayout<128>::kAlloc <= 232448, "dQ shared memory (D=128)");
+static_assert(DqLayout<64>::kAlloc <= 232448, "dQ shared memory (D=64)");
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -581,22 +590,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
-  auto stage_off = [&](int s) -> uint32_t { return L::kOffStage + s * L::kStageBytes; };
+  auto k_off = [&](int s) -> uint32_t { return L::kOffK + s * T::kTileBytes; };
+  auto v_off = [&](int s) -> uint32_t { return L::kOffV + s * T::kTileBytes; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(L::kBarQdFull), 1);
     ptx::mbar_init(bar(L::kBarQdEmpty), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::kBarKvFull + s), 1);
-      ptx::mbar_init(bar(L::kBarKvEmpty + s), 1);
+    for (int s = 0; s < L::kKStages; ++s) {
+      ptx::mbar_init(bar(L::kBarKFull + s), 1);
+      ptx::mbar_init(bar(L::kBarKEmpty + s), 1);
+    }
+    for (int s = 0; s < L::kVStages; ++s) {
+      ptx::mbar_init(bar(L::kBarVFull + s), 1);
+      ptx::mbar_init(bar(L::kBarVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kBarSFull), 1);
-    ptx::mbar_init(bar(L::kBarSFree), 128);
+    ptx::mbar_init(bar(L::kBarSFree), kComputeThreads);
     ptx::mbar_init(bar(L::kBarDpFull), 1);
-    ptx::mbar_init(bar(L::kBarDsFull), 128);
+    ptx::mbar_init(bar(L::kBarDsFull), kComputeThreads);
     ptx::mbar_init(bar(L::kBarAccFull), 1);
-    ptx::mbar_init(bar(L::kBarAccEmpty), 128);
+    ptx::mbar_init(bar(L::kBarAccEmpty), kComputeThreads);
     ptx::mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -611,12 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
 
-  if (warp < 4) {
-    // ------------------------------------------------ compute warpgroup: thread = query row
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + L::kColS;
-    const uint32_t t_dp = tmem + lane_off + L::kColDp;
+  if (warp < 8) {
+    // ------------------------------------------------ compute warpgroups: thread = query row
+    const int g = warp >> 2;                   // columns [64g, 64g + 64) of the row
+    const int rw = warp & 3;
+    const int row = rw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(rw * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::kColS + 64 * g;
+    const uint32_t t_dp = tmem + lane_off + L::kColDp + 64 * g;
     const float sl2 = p.scale_log2;
     uint32_t it = 0, acc_count = 0;
     bool ok = true;
@@ -637,31 +653,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t sr[128];
-        ptx::tmem_ld32x32b_x128(t_s, sr);
+        uint32_t sr[2][32];
+        ptx::tmem_ld32x32b_x32(t_s, sr[0]);
+        ptx::tmem_ld32x32b_x32(t_s + 32, sr[1]);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarSFree));   // S is in registers: the next S may overwrite it
-        const int lim = key_lim - t * kBlk;    // columns c < lim are allowed keys
-        float pr[128];
+        const int lim = key_lim - t * kBlk - 64 * g;   // this warpgroup's columns c < lim are allowed
+        float pr[64];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+        for (int c = 0; c < 64; ++c) {
+          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
           pr[c] = (c < lim) ? x : 0.0f;
         }
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
+        ptx::tmem_ld32x32b_x32(t_dp, sr[0]);
+        ptx::tmem_ld32x32b_x32(t_dp + 32, sr[1]);
+        uint32_t pk[32];
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t d[32];
-          ptx::tmem_ld32x32b_x32(t_dp + c0, d);
-          uint32_t q16[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            q16[c] = ptx::pack_bf16x2(pr[c0 + 2 * c] * (__uint_as_float(d[2 * c]) - dlt),
-                                      pr[c0 + 2 * c + 1] * (__uint_as_float(d[2 * c + 1]) - dlt));
-          ptx::tmem_st32x32b_x16(t_dp + c0 / 2, q16);
-        }
+        for (int c = 0; c < 32; ++c)
+          pk[c] = ptx::pack_bf16x2(pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt),
+                                   pr[2 * c + 1] * (__uint_as_float(sr[c >> 4][(2 * c + 1) & 31]) - dlt));
+        ptx::tmem_st32x32b_x32(t_dp, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarDsFull));
@@ -671,11 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (!ok) break;
       ++acc_count;
       ptx::tc_fence_after();
-      __nv_bfloat16* dst = p.dq + gi * HD;
+      // Epilogue: each warpgroup writes its half of the row's columns.
+      __nv_bfloat16* dst = p.dq + gi * HD + (HD / 2) * g;
 #pragma unroll
-      for (int c0 = 0; c0 < HD; c0 += 32) {
+      for (int c0 = 0; c0 < HD / 2; c0 += 32) {
         uint32_t a[32];
-        ptx::tmem_ld32x32b_x32(tmem + lane_off + L::kColDq + c0, a);
+        ptx::tmem_ld32x32b_x32(tmem + lane_off + L::kColDq + (HD / 2) * g + c0, a);
         uint32_t pk16[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
@@ -698,8 +713,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       ptx::prefetch_tensormap(&p.tm_do);
     }
     uint32_t it = 0, units = 0;
-    int last_fill[L::kStages];
-    for (int s = 0; s < L::kStages; ++s) last_fill[s] = -1;
+    int last_k[L::kKStages], last_v[L::kVStages];
+    for (int s = 0; s < L::kKStages; ++s) last_k[s] = -1;
+    for (int s = 0; s < L::kVStages; ++s) last_v[s] = -1;
     bool ok = true;
     int idx;
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
@@ -719,23 +735,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       }
       ++units;
       for (int t = 0; t < n; ++t, ++it) {
-        const int s = static_cast<int>(it % L::kStages);
-        ok = wait_warp(bar(L::kBarKvEmpty + s), ((it / L::kStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
+        const int sk = static_cast<int>(it % L::kKStages), sv = static_cast<int>(it % L::kVStages);
+        ok = wait_warp(bar(L::kBarKEmpty + sk), ((it / L::kKStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
         if (!ok) break;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(bar(L::kBarKvFull + s), 2 * T::kTileBytes);
-          for (int rg = 0; rg < T::kRegions; ++rg) {
-            ptx::tma_load_3d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKvFull + s), 64 * rg, t * kBlk, bh);
-            ptx::tma_load_3d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull + s), 64 * rg, t * kBlk, bh);
-          }
+          ptx::mbar_arrive_expect_tx(bar(L::kBarKFull + sk), T::kTileBytes);
+          for (int rg = 0; rg < T::kRegions; ++rg)
+            ptx::tma_load_3d(sbase + k_off(sk) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKFull + sk), 64 * rg, t * kBlk, bh);
         }
-        last_fill[s] = static_cast<int>(it);
+        last_k[sk] = static_cast<int>(it);
+        ok = wait_warp(bar(L::kBarVEmpty + sv), ((it / L::kVStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
+        if (!ok) break;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(bar(L::kBarVFull + sv), T::kTileBytes);
+          for (int rg = 0; rg < T::kRegions; ++rg)
+            ptx::tma_load_3d(sbase + v_off(sv) + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarVFull + sv), 64 * rg, t * kBlk, bh);
+        }
+        last_v[sv] = static_cast<int>(it);
       }
     }
     if (lane == 0) {
       if (units > 0) drain_phase(bar(L::kBarQdFull), (units - 1) & 1, limit);
-      for (int s = 0; s < L::kStages; ++s)
-        if (last_fill[s] >= 0) drain_phase(bar(L::kBarKvFull + s), (last_fill[s] / L::kStages) & 1, limit);
+      for (int s = 0; s < L::kKStages; ++s)
+        if (last_k[s] >= 0) drain_phase(bar(L::kBarKFull + s), (last_k[s] / L::kKStages) & 1, limit);
+      for (int s = 0; s < L::kVStages; ++s)
+        if (last_v[s] >= 0) drain_phase(bar(L::kBarVFull + s), (last_v[s] / L::kVStages) & 1, limit);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -753,11 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ptx::mma_ss_warp(tmem + d_col, a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
       }
     };
-    auto issue_acc = [&](uint64_t b, bool accumulate) {   // dQ (+)= dS K
+    auto issue_acc = [&](uint64_t b, bool accumulate) {   // dQ (+)= dS K, dS packed by both warpgroups
 #pragma unroll
       for (int kk = 0; kk < kBlk / 16; ++kk)
-        ptx::mma_ts_warp(tmem + L::kColDq, tmem + L::kColDp + kk * 8, b + ((kk * 16 * 128) >> 4), kIdescAcc,
-                         (accumulate || kk > 0) ? 1u : 0u);
+        ptx::mma_ts_warp(tmem + L::kColDq, tmem + L::kColDp + packed_col(kk), b + ((kk * 16 * 128) >> 4),
+                         kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
     };
     uint32_t it = 0, units = 0, acc_units = 0;
     bool ok = true;
@@ -770,24 +794,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (!ok) break;
       ++units;
       {
-        const int s0 = static_cast<int>(it % L::kStages);
-        ok = wait_warp(bar(L::kBarKvFull + s0), (it / L::kStages) & 1, abort_flag, limit, kSiteMma);
+        const int k0 = static_cast<int>(it % L::kKStages), v0 = static_cast<int>(it % L::kVStages);
+        ok = wait_warp(bar(L::kBarKFull + k0), (it / L::kKStages) & 1, abort_flag, limit, kSiteMma);
+        if (ok) ok = wait_warp(bar(L::kBarVFull + v0), (it / L::kVStages) & 1, abort_flag, limit, kSiteMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_rows(L::kColS, desc_q, kmaj(stage_off(s0)));
+        issue_rows(L::kColS, desc_q, kmaj(k_off(k0)));
         ptx::mma_commit_warp(bar(L::kBarSFull));
-        issue_rows(L::kColDp, desc_do, kmaj(stage_off(s0) + T::kTileBytes));
+        issue_rows(L::kColDp, desc_do, kmaj(v_off(v0)));
         ptx::mma_commit_warp(bar(L::kBarDpFull));
+        ptx::mma_commit_warp(bar(L::kBarVEmpty + v0));   // V read only by dP
       }
       for (int t = 0; t < n && ok; ++t, ++it) {
-        const int s = static_cast<int>(it % L::kStages);
-        const int s1 = static_cast<int>((it + 1) % L::kStages);
+        const int sk = static_cast<int>(it % L::kKStages);
+        const int k1 = static_cast<int>((it + 1) % L::kKStages), v1 = static_cast<int>((it + 1) % L::kVStages);
         if (t + 1 < n) {   // next S as soon as this S has left TMEM
           ok = wait_warp(bar(L::kBarSFree), it & 1, abort_flag, limit, kSiteMma);
-          if (ok) ok = wait_warp(bar(L::kBarKvFull + s1), ((it + 1) / L::kStages) & 1, abort_flag, limit, kSiteMma);
+          if (ok) ok = wait_warp(bar(L::kBarKFull + k1), ((it + 1) / L::kKStages) & 1, abort_flag, limit, kSiteMma);
           if (!ok) break;
           ptx::tc_fence_after();
-          issue_rows(L::kColS, desc_q, kmaj(stage_off(s1)));
+          issue_rows(L::kColS, desc_q, kmaj(k_off(k1)));
           ptx::mma_commit_warp(bar(L::kBarSFull));
         }
         if (t == 0 && acc_units > 0) {
@@ -797,11 +823,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ok = wait_warp(bar(L::kBarDsFull), it & 1, abort_flag, limit, kSiteMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_acc(mnmaj(stage_off(s)), t > 0);
-        ptx::mma_commit_warp(bar(L::kBarKvEmpty + s));   // K, V of stage s read for the last time
+        issue_acc(mnmaj(k_off(sk)), t > 0);
+        ptx::mma_commit_warp(bar(L::kBarKEmpty + sk));   // K of this key tile read for the last time
         if (t + 1 < n) {   // next dP overwrites dS: issued after the MMA that reads it
-          issue_rows(L::kColDp, desc_do, kmaj(stage_off(s1) + T::kTileBytes));
+          ok = wait_warp(bar(L::kBarVFull + v1), ((it + 1) / L::kVStages) & 1, abort_flag, limit, kSiteMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_rows(L::kColDp, desc_do, kmaj(v_off(v1)));
           ptx::mma_commit_warp(bar(L::kBarDpFull));
+          ptx::mma_commit_warp(bar(L::kBarVEmpty + v1));
         }
       }
       if (!ok) break;
