@@ -299,3 +299,29 @@ def test_attention_from_host(oracle_mod, causal, chunks):
     ref_o, ref_l = oracle_mod.attn_full(q, k, v, causal, 1.0 / math.sqrt(D))
     assert np.abs(o.float().numpy() - ref_o).max() <= TOL_O
     assert np.abs(lse.numpy() - ref_l).max() <= TOL_LSE
+
+
+@pytest.mark.parametrize("shape,kw", [((4, 16, 1024, 1024, 64), dict(causal=True)),          # dependent launches
+                                      ((1, 4, 512, 8192, 128), dict(causal=False)),          # split + combine
+                                      ((2, 8, 700, 700, 128), dict(window=(100, 0)))])       # band
+def test_chained_calls_see_previous_results(shape, kw):
+    """Each call's output is the next call's Q (read after write) and the previous call's
+    input buffer is the next call's output (write after read): back-to-back launches, which
+    may overlap their set-up, must give the same bits as calls separated by a device sync."""
+    B, H, Lq, Lk, D = shape
+    dev = torch.device("cuda:0")
+    q0, k, v = (t.to(dev) for t in make_qkv(B, H, Lq, Lk, D, seed=61))
+    def chain(sync):
+        bufs = [q0.clone(), torch.empty_like(q0)]
+        lse = torch.empty((B, H, Lq), device=dev, dtype=torch.float32)
+        for i in range(6):
+            src, dst = bufs[i % 2], bufs[(i + 1) % 2]
+            fa.attention(src, k, v, out=dst, lse=lse, **kw)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return bufs[0].clone(), lse.clone()
+    a = chain(sync=True)
+    b = chain(sync=False)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
