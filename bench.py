@@ -279,32 +279,55 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
 
     q_h, k_h, v_h = make_workload_inputs(w)
+    # Variants of the same workload (fa_fwd_strided): fp16 values, Q/K/V read in place
+    # from [B, L, H, D] memory, per-batch key padding.
+    variant = args.dtype != "bf16" or args.layout != "bhld" or args.kv_pad > 0
+    io_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    if args.dtype == "fp16":
+        q_h, k_h, v_h = (t.to(torch.float16) for t in (q_h, k_h, v_h))
+    kv_len_h = None
+    if args.kv_pad > 0:
+        g = np.random.default_rng(0xCAFE + w.index)
+        lo = max(1, int(round(w.Lk * (1.0 - 2.0 * args.kv_pad))))
+        kv_len_h = g.integers(lo, w.Lk + 1, size=w.B).astype(np.int32)
     in_bytes = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     out_bytes = q_h.numel() * 2 + w.B * w.H * w.Lq * 4
     n_copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)) + 1)
     bufs = []
-    base = tuple(t.to(dev) for t in (q_h, k_h, v_h))
+
+    def place(t):   # [B, H, L, D] values, stored [B, L, H, D] with --layout bshd
+        t = t.to(dev)
+        return t.transpose(1, 2).contiguous().transpose(1, 2) if args.layout == "bshd" else t
+
+    base = tuple(place(t) for t in (q_h, k_h, v_h))
     for c in range(n_copies):
-        qkv = base if c == 0 else tuple(t.clone() for t in base)
-        o = torch.empty_like(qkv[0])
+        qkv = base if c == 0 else tuple(place(t) for t in (q_h, k_h, v_h))
+        o = torch.empty((w.B, w.H, w.Lq, w.D), device=dev, dtype=io_dtype)
         lse = torch.empty((w.B, w.H, w.Lq), device=dev, dtype=torch.float32)
         bufs.append((*qkv, o, lse))
+    kv_len = torch.from_numpy(kv_len_h).to(dev) if kv_len_h is not None else None
     torch.cuda.synchronize(dev)
 
     # Workspace for the split-key schedule, allocated once outside the timed region
     # (zero bytes, and plain fa_fwd semantics, for causal workloads).
     # Local-window workloads run fa_fwd_window (whole units, no workspace).
-    if w.window is None:
+    if w.window is None and kv_len is None:
         st, ws_bytes = fa.fa_fwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
         if st != fa.FA_OK:
             raise RuntimeError(fa.fa_status_string(st))
     else:
         ws_bytes = 0
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    left, right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
+    code = fa.FA_DTYPE_FP16 if args.dtype == "fp16" else fa.FA_DTYPE_BF16
 
     def launch(i):
         q, k, v, o, lse = bufs[i % n_copies]
-        if w.window is not None:
+        if variant:
+            st = fa.fa_fwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], o,
+                                   o.stride()[:3], lse, kv_len, w.B, w.H, w.Lq, w.Lk, w.D, left,
+                                   right, w.scale, code, ws, ws_bytes, stream)
+        elif w.window is not None:
             st = fa.fa_fwd_window(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.window[0],
                                   w.window[1], w.scale, stream)
         else:
@@ -346,13 +369,19 @@ def run_ours(args, w):
         raise RuntimeError(f"timed region reported {fa.fa_status_string(st)}")
     max_ms = reduce_max(dist, total_ms, dev)
     flops = w.flops()
+    if kv_len_h is not None:   # only the unpadded pairs count
+        i = np.arange(w.Lq, dtype=np.int64)
+        lo = np.zeros_like(i) if left < 0 else np.maximum(0, i - left)
+        hi_band = np.full_like(i, w.Lk - 1) if right < 0 else np.minimum(w.Lk - 1, i + right)
+        pairs = sum(int(np.maximum(0, np.minimum(hi_band, kl - 1) - lo + 1).sum()) for kl in kv_len_h)
+        flops = 4 * w.D * w.H * pairs
     value = aggregate_tflops(world, flops, args.steps, max_ms)
     ms_per_step = max_ms / args.steps
     kernel_tflops = flops / (statistics.mean(per_launch_ms) / 1e3) / 1e12
 
     # ---------------- end to end: pinned host buffers through the public call
     e2e = None
-    if not args.skip_e2e:
+    if not args.skip_e2e and not variant:
         q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
         o_p = torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory()
         l_p = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32).pin_memory()
@@ -380,10 +409,27 @@ def run_ours(args, w):
 
     peaks, peak_src = load_peaks()
     peak = peak_value(peaks, "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    traffic = measured_traffic(w.name)
-    roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
-                "frac": kernel_tflops / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense (burst)", "kernel": f"{KERNEL_NAME}<{w.D}>"}
+    hbm_peak = peak_value(peaks, "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    traffic = measured_traffic(w.name) if not variant else None   # measured on bf16, [B,H,L,D]
+    # The bound is the roof the workload's algorithmic intensity (flops per algorithmic
+    # byte: Q, K, V read once, O and LSE written once) meets first; both are reported.
+    alg_bytes = w.algorithmic_bytes()
+    if kv_len_h is not None:   # padded keys are never read
+        kv_bytes = 2 * 2 * w.H * w.D * int(kv_len_h.sum())
+        alg_bytes = alg_bytes - 2 * 2 * w.B * w.H * w.Lk * w.D + kv_bytes
+    launch_s = statistics.mean(per_launch_ms) / 1e3
+    hbm_gbs = alg_bytes / launch_s / 1e9
+    tensor_bound = flops / alg_bytes >= peak * 1e12 / (hbm_peak * 1e9)
+    if tensor_bound:
+        roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
+                    "frac": kernel_tflops / peak, "peak_source": f"{peak_src} bf16 dense (burst)"}
+    else:
+        roofline = {"bound": "hbm", "achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": hbm_gbs / hbm_peak, "peak_source": f"{peak_src} HBM copy"}
+    roofline.update({"traffic": traffic, "kernel": f"{KERNEL_NAME}<{w.D}>",
+                     "algorithmic_bytes": alg_bytes, "flops_per_byte": flops / alg_bytes,
+                     "tensor_frac": kernel_tflops / peak, "hbm_achieved_gbs": hbm_gbs,
+                     "hbm_frac": hbm_gbs / hbm_peak})
 
     cpu = None
     if rank == 0 and not args.skip_cpu_baseline:
@@ -396,10 +442,11 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic",
             "config": {"workload": w.name, "shape": w.describe(),
-                       "flops_per_step": flops,
+                       "flops_per_step": flops, "io_dtype": args.dtype, "layout": args.layout,
+                       "kv_len": None if kv_len_h is None else [int(x) for x in kv_len_h],
                        "l2": f"inputs rotate over {n_copies} copies "
                              f"({n_copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
                        "parallelism": f"replica per GPU x{world}",
@@ -542,6 +589,12 @@ def main(argv=None):
     ap.add_argument("--ref-seconds-per-step", type=float, default=5.0)
     ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
                     help="forward (the headline metric) or backward (fa_bwd)")
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
+                    help="forward I/O type (fp16 runs fa_fwd_strided)")
+    ap.add_argument("--layout", choices=["bhld", "bshd"], default="bhld",
+                    help="bshd: Q, K, V stored [B, L, H, D] and read in place (fa_fwd_strided)")
+    ap.add_argument("--kv-pad", type=float, default=0.0,
+                    help="mean fraction of padded keys per batch (key-padding mask, fa_fwd_strided)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("need --steps >= 1 and --warmup >= 0")
