@@ -79,6 +79,11 @@ class OracleLib:
                                                 ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                                 ctypes.c_long, ctypes.c_double, lp, ctypes.c_long,
                                                 dp, dp, dp, ctypes.c_int]
+        lib.oracle_attn_bwd_head_masked.restype = ctypes.c_int
+        lib.oracle_attn_bwd_head_masked.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                                    ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                    ctypes.c_long, ctypes.c_double, dp, dp, dp,
+                                                    ctypes.c_int]
         lib.oracle_attn_bwd_head.restype = ctypes.c_int
         lib.oracle_attn_bwd_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
                                              ctypes.c_long, ctypes.c_int, ctypes.c_double,
@@ -211,6 +216,23 @@ class OracleLib:
             raise ValueError(f"oracle_attn_bwd_head failed with code {rc}")
         return dq, dk, dv
 
+    def attn_bwd_head_masked(self, q, k, v, do, left: int, right: int, kv_len: int,
+                             scale: float, nthreads: int = 0):
+        """Gradients (dQ, dK, dV) under the band and key-padding mask of attn_head_keypad."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        Lq, D = q.shape
+        Lk = k.shape[0]
+        if k.shape != (Lk, D) or v.shape != (Lk, D) or do.shape != (Lq, D):
+            raise ValueError("k, v must be [Lk, D] and do [Lq, D] with the same D as q")
+        dq, dk, dv = np.empty((Lq, D)), np.empty((Lk, D)), np.empty((Lk, D))
+        rc = self.lib.oracle_attn_bwd_head_masked(_dptr(q), _dptr(k), _dptr(v), _dptr(do), Lq, Lk,
+                                                  D, int(left), int(right), int(kv_len),
+                                                  float(scale), _dptr(dq), _dptr(dk), _dptr(dv),
+                                                  int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_head_masked failed with code {rc}")
+        return dq, dk, dv
+
     def attn_bwd_full(self, q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
         """Gradients over contiguous [B, H, L, D] tensors: returns (dQ, dK, dV)."""
         q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -285,3 +307,7 @@ def attn_full_keypad(*args, **kwargs):
 
 def attn_bwd_full(*args, **kwargs):
     return _get().attn_bwd_full(*args, **kwargs)
+
+
+def attn_bwd_head_masked(*args, **kwargs):
+    return _get().attn_bwd_head_masked(*args, **kwargs)

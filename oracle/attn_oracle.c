@@ -370,6 +370,85 @@ int oracle_attn_bwd_head(const double *Q, const double *K, const double *V, cons
     return ORACLE_OK;
 }
 
+/*
+ * Gradients under the band and key-padding mask of oracle_attn_head_keypad: the same
+ * chain rule as oracle_attn_bwd_head, with row i's allowed keys the contiguous range
+ * [lo_i, hi_i] (i - left <= j <= i + right, j < kv_len; -1 = unbounded side) instead of
+ * a prefix.  A row without allowed keys has O = 0 (not a function of Q, K or V), so it
+ * contributes nothing: dQ_i = 0 and no term to dK or dV.  kv_len is clamped to [0, Lk].
+ */
+int oracle_attn_bwd_head_masked(const double *Q, const double *K, const double *V,
+                                const double *dO, long Lq, long Lk, long D, long left,
+                                long right, long kv_len, double scale, double *dQ, double *dK,
+                                double *dV, int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return ORACLE_BAD_ARG;
+    if (Lq < 0 || Lk < 1 || D < 1 || left < -1 || right < -1) return ORACLE_BAD_ARG;
+    const long kv = kv_len < 0 ? 0 : (kv_len > Lk ? Lk : kv_len);
+    double *P = (double *)calloc((size_t)(Lq > 0 ? Lq : 1) * (size_t)Lk, sizeof(double));
+    double *dS = (double *)calloc((size_t)(Lq > 0 ? Lq : 1) * (size_t)Lk, sizeof(double));
+    if (!P || !dS) {
+        free(P);
+        free(dS);
+        return ORACLE_NO_MEMORY;
+    }
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (long i = 0; i < Lq; ++i) {
+        const long lo = (left < 0 || i - left < 0) ? 0 : i - left;
+        long hi = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;
+        if (hi > kv - 1) hi = kv - 1;
+        double *p = P + i * Lk, *ds = dS + i * Lk;
+        for (long d = 0; d < D; ++d) dQ[i * D + d] = 0.0;
+        if (lo > hi) continue;   /* no allowed key: P and dS stay 0 */
+        double m = -INFINITY;
+        for (long j = lo; j <= hi; ++j) {
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d) dot += Q[i * D + d] * K[j * D + d];
+            p[j] = scale * dot;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (long j = lo; j <= hi; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        for (long j = lo; j <= hi; ++j) p[j] /= l;
+        double pdp = 0.0;
+        for (long j = lo; j <= hi; ++j) {
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d) dot += dO[i * D + d] * V[j * D + d];
+            ds[j] = dot;
+            pdp += p[j] * dot;
+        }
+        for (long j = lo; j <= hi; ++j) ds[j] = p[j] * (ds[j] - pdp);
+        for (long d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (long j = lo; j <= hi; ++j) acc += ds[j] * K[j * D + d];
+            dQ[i * D + d] = scale * acc;
+        }
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (long j = 0; j < Lk; ++j) {
+        for (long d = 0; d < D; ++d) {
+            double av = 0.0, ak = 0.0;
+            for (long i = 0; i < Lq; ++i) {
+                av += P[i * Lk + j] * dO[i * D + d];
+                ak += dS[i * Lk + j] * Q[i * D + d];
+            }
+            dV[j * D + d] = av;
+            dK[j * D + d] = scale * ak;
+        }
+    }
+    free(P);
+    free(dS);
+    return ORACLE_OK;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int oracle_max_threads(void)
 {

@@ -398,6 +398,42 @@ KEYPAD_PINS = [pin_keypad_torch_f64, pin_keypad_uniform, pin_keypad_no_padding_i
 PINS.extend(KEYPAD_PINS)
 
 
+def pin_bwd_masked_finite_differences(lib):
+    """Band + key padding gradients equal central differences of the key-padding forward
+    (rows without keys have O = 0 and no gradient)."""
+    for (Lq, Lk, D, left, right, kv) in [(6, 7, 3, 2, 1, 7), (7, 5, 2, -1, 0, 3), (5, 8, 3, 1, 3, 4),
+                                         (6, 6, 2, 0, 0, 2)]:
+        q, k, v = _rand((Lq, D), 95 + Lq, 1.5), _rand((Lk, D), 96 + Lk, 1.5), _rand((Lk, D), 97)
+        g = _rand((Lq, D), 98)
+        dq, dk, dv = lib.attn_bwd_head_masked(q, k, v, g, left, right, kv, 0.7)
+
+        def loss(**kw):
+            a = dict(q=q, k=k, v=v)
+            a.update(kw)
+            return float((lib.attn_head_keypad(a["q"], a["k"], a["v"], left, right, kv, 0.7)[0] * g).sum())
+        for name, x, got in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += 1e-6
+                xm[idx] -= 1e-6
+                fd[idx] = (loss(**{name: xp}) - loss(**{name: xm})) / 2e-6
+            np.testing.assert_allclose(got, fd, rtol=0, atol=1e-7)
+
+
+def pin_bwd_masked_reduces_to_causal_and_full(lib):
+    q, k, v, g = _rand((9, 4), 99), _rand((11, 4), 100), _rand((11, 4), 101), _rand((9, 4), 102)
+    for causal, (left, right) in ((False, (-1, -1)), (True, (-1, 0))):
+        a = lib.attn_bwd_head(q, k, v, g, causal, 0.8)
+        b = lib.attn_bwd_head_masked(q, k, v, g, left, right, 11, 0.8)
+        for x, y in zip(a, b):
+            np.testing.assert_allclose(x, y, rtol=0, atol=1e-13)
+
+
+BWD_PINS.extend([pin_bwd_masked_finite_differences, pin_bwd_masked_reduces_to_causal_and_full])
+PINS.extend([pin_bwd_masked_finite_differences, pin_bwd_masked_reduces_to_causal_and_full])
+
+
 def test_window_rejects_empty_rows(oracle_mod):
     q, k, v = _rand((5, 4), 1), _rand((3, 4), 2), _rand((3, 4), 3)
     with pytest.raises(ValueError):   # row 4 would need key 4 >= Lk
@@ -435,10 +471,13 @@ MUTATIONS = {
                               "double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D, hi - lo, D, hi - lo, scale,"),
     "keypad_empty_row_not_zeroed": ("for (long d = 0; d < D; ++d) O[r * D + d] = 0.0;\n                    LSE[r] = -INFINITY;",
                                     "for (long d = 0; d < D; ++d) O[r * D + d] = 0.0;\n                    LSE[r] = 0.0;"),
-    "bwd_softmax_jacobian_without_row_term": ("ds[j] = p[j] * (ds[j] - pdp);", "ds[j] = p[j] * ds[j];"),
-    "bwd_dk_missing_scale": ("dK[j * D + d] = scale * ak;", "dK[j * D + d] = ak;"),
-    "bwd_dv_from_queries": ("av += P[i * Lk + j] * dO[i * D + d];", "av += P[i * Lk + j] * Q[i * D + d];"),
-    "keypad_last_key_kept": ("if (hi > kv - 1) hi = kv - 1;", "if (hi > kv) hi = kv;"),
+    "bwd_softmax_jacobian_without_row_term": ("ds[j] = p[j] * (ds[j] - pdp);", "ds[j] = p[j] * ds[j];", 0),
+    "bwd_dk_missing_scale": ("dK[j * D + d] = scale * ak;", "dK[j * D + d] = ak;", 0),
+    "bwd_dv_from_queries": ("av += P[i * Lk + j] * dO[i * D + d];", "av += P[i * Lk + j] * Q[i * D + d];", 0),
+    "bwd_masked_jacobian_without_row_term": ("ds[j] = p[j] * (ds[j] - pdp);", "ds[j] = p[j] * ds[j];", 1),
+    "bwd_masked_dk_missing_scale": ("dK[j * D + d] = scale * ak;", "dK[j * D + d] = ak;", 1),
+    "bwd_masked_padding_ignored": ("if (hi > kv - 1) hi = kv - 1;", ";", 1),
+    "keypad_last_key_kept": ("if (hi > kv - 1) hi = kv - 1;", "if (hi > kv) hi = kv;", 0),
     "window_shifted_values": ("double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D,",
                               "double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
 }
@@ -448,10 +487,17 @@ MUTATIONS = {
 def test_planted_mistake_is_caught(tmp_path, name):
     src = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
     text = open(src).read()
-    old, new = MUTATIONS[name]
-    assert text.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    old, new, *which = MUTATIONS[name]
+    which = which[0] if which else None   # occurrence to mutate when the text repeats
+    if which is None:
+        assert text.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+        at = text.index(old)
+    else:
+        at = -1
+        for _ in range(which + 1):
+            at = text.index(old, at + 1)
     mutated = tmp_path / f"oracle_{name}.c"
-    mutated.write_text(text.replace(old, new))
+    mutated.write_text(text[:at] + new + text[at + len(old):])
     lib = oracle.OracleLib(oracle.build(force=True, src=str(mutated),
                                         out=str(tmp_path / f"lib_{name}.so")))
     failures = 0
