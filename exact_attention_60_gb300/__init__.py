@@ -8,7 +8,8 @@ from __future__ import annotations
 import math
 
 from ._native import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,
-                      FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, fa_bwd, fa_bwd_workspace_size,
+                      FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, fa_bwd, fa_bwd_masked,
+                      fa_bwd_workspace_size,
                       fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_strided, fa_fwd_window,
                       fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status, fa_status_string)
 
@@ -119,11 +120,12 @@ _bwd_workspaces = {}
 
 
 def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-                       dq=None, dk=None, dv=None, stream=None):
+                       dq=None, dk=None, dv=None, stream=None, window=None, kv_len=None):
     """dQ, dK, dV of ``attention`` given its inputs, its outputs ``o``/``lse`` and
     ``do`` = dLoss/dO (contiguous bf16 / fp32 CUDA tensors of the forward's shapes).
     Allocates the gradients if not given; uses a cached per-device workspace, so calls
-    on one device must be ordered on one stream."""
+    on one device must be ordered on one stream.  ``window`` and ``kv_len`` as for
+    ``attention`` (fa_bwd_masked)."""
     import torch
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
@@ -145,14 +147,25 @@ def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float |
     if ws is None or ws.numel() < max(nbytes, 256):
         ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
         _bwd_workspaces[key] = ws
-    st = fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Lq, Lk, D, causal, scale, ws, ws.numel(),
-                stream)
+    if window is None and kv_len is None:
+        st = fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Lq, Lk, D, causal, scale, ws, ws.numel(),
+                    stream)
+    else:
+        left, right = (-1, 0 if causal else -1) if window is None else (int(window[0]), int(window[1]))
+        if window is not None and causal:
+            right = 0
+        if kv_len is not None and (kv_len.dtype != torch.int32 or kv_len.numel() != B
+                                   or not kv_len.is_cuda or not kv_len.is_contiguous()):
+            raise ValueError("kv_len must be a contiguous int32 CUDA tensor of B entries")
+        st = fa_bwd_masked(q, k, v, o, do, lse, dq, dk, dv, kv_len, B, H, Lq, Lk, D, left, right,
+                           scale, ws, ws.numel(), stream)
     if st != FA_OK:
         raise FaError(st)
     return dq, dk, dv
 
 
-def flash_attention(q, k, v, causal: bool = False, scale: float | None = None):
+def flash_attention(q, k, v, causal: bool = False, scale: float | None = None, window=None,
+                    kv_len=None):
     """Differentiable exact attention: ``attention`` forward, ``attention_backward``
     for the gradients (torch.autograd glue only)."""
     import torch
@@ -160,14 +173,15 @@ def flash_attention(q, k, v, causal: bool = False, scale: float | None = None):
     class _Fn(torch.autograd.Function):
         @staticmethod
         def forward(ctx, q, k, v):
-            o, lse = attention(q, k, v, causal=causal, scale=scale)
+            o, lse = attention(q, k, v, causal=causal, scale=scale, window=window, kv_len=kv_len)
             ctx.save_for_backward(q, k, v, o, lse)
             return o
 
         @staticmethod
         def backward(ctx, do):
             q, k, v, o, lse = ctx.saved_tensors
-            return attention_backward(q, k, v, o, lse, do.contiguous(), causal=causal, scale=scale)
+            return attention_backward(q, k, v, o, lse, do.contiguous(), causal=causal, scale=scale,
+                                      window=window, kv_len=kv_len)
 
     return _Fn.apply(q, k, v)
 

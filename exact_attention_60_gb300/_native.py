@@ -22,7 +22,8 @@ FA_DTYPE_FP16 = 1
 # Every symbol include/fa.h declares.
 EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_strided",
             "fa_fwd_noalloc",
-            "fa_bwd_workspace_size", "fa_bwd", "fa_status_string", "fa_last_device_status",
+            "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_masked", "fa_status_string",
+            "fa_last_device_status",
             "fa_debug_set")
 
 _lib = None
@@ -60,6 +61,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd.argtypes = [vp] * 9 + [ctypes.c_int] * 6 + [ctypes.c_float, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd_masked.restype = ctypes.c_int
+    lib.fa_bwd_masked.argtypes = [vp] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, vp, ctypes.c_size_t, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_last_device_status.restype = ctypes.c_int
@@ -162,6 +165,15 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Lq, Lk, D, causal, scale, work
                          _ptr(dK), _ptr(dV), int(B), int(H), int(Lq), int(Lk), int(D),
                          int(bool(causal)), float(scale), _ptr(workspace), int(workspace_bytes),
                          _stream(stream))
+
+
+def fa_bwd_masked(Q, K, V, O, dO, LSE, dQ, dK, dV, kv_len, B, H, Lq, Lk, D, window_left,
+                  window_right, scale, workspace, workspace_bytes, stream=None) -> int:
+    """C ``fa_bwd_masked``: fa_bwd under a band (-1 = unbounded side) and key padding."""
+    return load().fa_bwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                                _ptr(dK), _ptr(dV), _ptr(kv_len), int(B), int(H), int(Lq), int(Lk),
+                                int(D), int(window_left), int(window_right), float(scale),
+                                _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_status_string(status: int) -> str:

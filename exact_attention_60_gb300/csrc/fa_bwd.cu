@@ -7,7 +7,8 @@
 //   dP_ij = dO_i . V_j
 //   dS_ij = P_ij (dP_ij - Delta_i),  Delta_i = dO_i . O_i  (= sum_j P_ij dP_ij)
 //   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
-// over the allowed pairs (all j < Lk, or j <= i when causal).  The principle --
+// over the allowed pairs (all j < Lk, j <= i when causal, or the band and key-padding
+// mask of the strided forward).  The principle --
 // keep the per-row statistic from the forward pass and recompute P from it
 // instead of storing the score matrix -- is the one the wsisp.com post
 // "FlashAttention-2 forward in Triton" states for the backward pass, which it
@@ -128,9 +129,12 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int bh_count;
+  int H;
   int Lq;
   int Lk;
-  int causal;
+  int win_left;        // key j allowed for query i iff i - win_left <= j <= i + win_right
+  int win_right;       //   (-1: unbounded side); causal is (-1, 0), the full mask (-1, -1)
+  const int* kv_len;   // per-batch valid keys (key padding), device memory; nullptr = none
   int nq;              // query tiles: ceil(Lq / 128)
   int nk;              // key tiles:   ceil(Lk / 128)
   int n_units;
@@ -146,13 +150,35 @@ struct Tiles {
   static constexpr int kRegions = HD / 64;
 };
 
-// Row tiles a unit streams: dK/dV units (key tile kt) see query tiles [q_first, nq);
-// dQ units (query tile qt) see key tiles [0, k_count).
-__device__ __forceinline__ int dkdv_first_q(const BwdParams& p, int kt) {
-  return p.causal ? kt : 0;   // causal: query q >= key k, so query tiles from the key tile's index
+// Valid (unpadded) keys of head bh's batch.
+__device__ __forceinline__ int batch_keys(const BwdParams& p, int bh) {
+  return p.kv_len ? min(max(__ldg(p.kv_len + bh / p.H), 0), p.Lk) : p.Lk;
 }
-__device__ __forceinline__ int dq_key_tiles(const BwdParams& p, int qt) {
-  return p.causal ? min(p.nk, qt + 1) : p.nk;
+
+// The query tiles a dK/dV unit (key tile kt) streams, [*qa, *qa + *n): those holding a query
+// q with q - left <= k <= q + right for some unpadded key k of the tile.
+__device__ __forceinline__ void dkdv_range(const BwdParams& p, int kt, int kvl, int* qa, int* n) {
+  const long long k0 = static_cast<long long>(kt) * kBlk, k1 = min(k0 + kBlk - 1, static_cast<long long>(kvl) - 1);
+  const long long q_lo = p.win_right < 0 ? 0 : max(0ll, k0 - p.win_right);
+  const long long q_hi = p.win_left < 0 ? p.Lq - 1 : min(static_cast<long long>(p.Lq) - 1, k1 + p.win_left);
+  *qa = 0;
+  *n = 0;
+  if (k1 < k0 || q_hi < q_lo) return;
+  *qa = static_cast<int>(q_lo / kBlk);
+  *n = static_cast<int>(q_hi / kBlk) - *qa + 1;
+}
+
+// The key tiles a dQ unit (query tile qt) streams, [*ka, *ka + *n): those holding an
+// allowed key of some query of the tile.
+__device__ __forceinline__ void dq_range(const BwdParams& p, int qt, int kvl, int* ka, int* n) {
+  const long long q0 = static_cast<long long>(qt) * kBlk, q1 = min(q0 + kBlk - 1, static_cast<long long>(p.Lq) - 1);
+  const long long lo = p.win_left < 0 ? 0 : max(0ll, q0 - p.win_left);
+  const long long lim = p.win_right < 0 ? kvl : min(static_cast<long long>(kvl), q1 + p.win_right + 1);
+  *ka = 0;
+  *n = 0;
+  if (lim <= lo) return;
+  *ka = static_cast<int>(lo / kBlk);
+  *n = static_cast<int>((lim - 1) / kBlk) - *ka + 1;
 }
 
 // Unit r of this CTA (boustrophedon over the grid), heaviest first.
@@ -162,7 +188,7 @@ __device__ __forceinline__ bool unit_index(const BwdParams& p, int r, int& idx) 
   return idx < p.n_units;
 }
 __device__ __forceinline__ void dkdv_unit(const BwdParams& p, int idx, int& bh, int& kt) {
-  if (p.causal) {   // the first key tiles are seen by the most query tiles
+  if (p.win_left < 0 && p.win_right >= 0) {   // causal-like: the first key tiles are seen by the most queries
     kt = idx / p.bh_count;
     bh = idx % p.bh_count;
   } else {          // a head's tiles run together and share its query tiles in L2
@@ -171,7 +197,7 @@ __device__ __forceinline__ void dkdv_unit(const BwdParams& p, int idx, int& bh, 
   }
 }
 __device__ __forceinline__ void dq_unit(const BwdParams& p, int idx, int& bh, int& qt) {
-  if (p.causal) {   // the last query tiles see the most key tiles
+  if (p.win_left < 0 && p.win_right >= 0) {   // causal-like: the last query tiles see the most keys
     qt = p.nq - 1 - idx / p.bh_count;
     bh = idx % p.bh_count;
   } else {
@@ -309,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
       int bh, kt;
       dkdv_unit(p, idx, bh, kt);
-      const int q_first = dkdv_first_q(p, kt);
-      const int n = max(0, p.nq - q_first);
+      const int kvl = batch_keys(p, bh);
+      int q_first, n;
+      dkdv_range(p, kt, kvl, &q_first, &n);
       const int k = kt * kBlk + row;   // this thread's key
       const size_t orow = (static_cast<size_t>(bh) * p.Lk + (k < p.Lk ? k : 0)) * HD;
       __nv_bfloat16* mine = (g ? p.dk : p.dv) + orow;   // warpgroup 0 writes dV, 1 writes dK
@@ -334,13 +361,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         uint32_t sr[2][32];
         ptx::tmem_ld32x32b_x32(t_s, sr[0]);
         ptx::tmem_ld32x32b_x32(t_s + 32, sr[1]);
-        // P^T_kq = exp2(sl2 * S - lse_q * log2e); padded queries carry lse2 = +inf (P = 0)
+        // P^T_kq = exp2(sl2 * S - lse_q * log2e); padded queries carry lse2 = +inf (P = 0).
+        // Key k is seen by query q iff k - right <= q <= k + left and k < kvl; only tiles the
+        // band or the padding cuts are masked (a query without keys, LSE = -inf, is always in
+        // such a tile).
+        const int qb = qt * kBlk;   // first query of the tile
+        const int kmin = kt * kBlk, kmax = kmin + kBlk - 1;
+        const bool cut = kmax >= kvl || (p.win_right >= 0 && qb < kmax - p.win_right) ||
+                         (p.win_left >= 0 && qb + kBlk - 1 > kmin + p.win_left);
+        const int base = qb + 64 * g;   // query of column 0 of this warpgroup
+        const int c_lo = (p.win_right < 0 ? 0 : k - p.win_right) - base;
+        const int c_hi = (p.win_left < 0 ? INT_MAX / 2 : k + p.win_left) - base;
+        const bool key_ok = k < kvl;
         float pr[64];
-        const bool diag = p.causal && qt == kt;   // causal: query q >= key k
+        if (cut) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
-          pr[c] = (diag && 64 * g + c < row) ? 0.0f : x;
+          for (int c = 0; c < 64; ++c) {
+            const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
+            pr[c] = (key_ok && c >= c_lo && c <= c_hi) ? x : 0.0f;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            pr[c] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
         }
         uint32_t pk[32];
 #pragma unroll
@@ -410,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
       int bh, kt;
       dkdv_unit(p, idx, bh, kt);
-      const int q_first = dkdv_first_q(p, kt);
-      const int n = max(0, p.nq - q_first);
+      int q_first, n;
+      dkdv_range(p, kt, batch_keys(p, bh), &q_first, &n);
       if (units > 0) {
         ok = wait_warp(bar(L::kBarKvEmpty), (units - 1) & 1, abort_flag, limit, kSiteLoad);
         if (!ok) break;
@@ -477,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
       int bh, kt;
       dkdv_unit(p, idx, bh, kt);
-      const int n = max(0, p.nq - dkdv_first_q(p, kt));
+      int qa_unused, n;
+      dkdv_range(p, kt, batch_keys(p, bh), &qa_unused, &n);
       ok = wait_warp(bar(L::kBarKvFull), units & 1, abort_flag, limit, kSiteMma);
       if (!ok) break;
       ++units;
@@ -640,15 +684,33 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
       int bh, qt;
       dq_unit(p, idx, bh, qt);
-      const int n = dq_key_tiles(p, qt);
+      const int kvl = batch_keys(p, bh);
+      int ka, n;
+      dq_range(p, qt, kvl, &ka, &n);
       const int q = qt * kBlk + row;   // this thread's query
       const bool valid = q < p.Lq;
       const size_t gi = static_cast<size_t>(bh) * p.Lq + (valid ? q : 0);
       const size_t gp = (static_cast<size_t>(bh) * p.nq + qt) * kBlk + row;   // padded row
       const float lse2 = valid ? p.lse2[gp] : 0.0f;
       const float dlt = p.delta[gp];
-      // keys k allowed for this row: k < key_lim
-      const int key_lim = p.causal ? min(p.Lk, q + 1) : p.Lk;
+      // keys allowed for this row: key_lo <= k < key_lim (a row without keys gets dQ = 0)
+      auto lo_of = [&](int qq) { return p.win_left < 0 ? 0 : qq - p.win_left; };
+      auto lim_of = [&](int qq) {
+        return p.win_right < 0 ? kvl
+                               : static_cast<int>(min(static_cast<long long>(kvl),
+                                                      static_cast<long long>(qq) + p.win_right + 1));
+      };
+      const int key_lo = lo_of(q), key_lim = lim_of(q);
+      // a key tile needs masking only where the band's left edge (of the tile's last row)
+      // or its right edge and the padding (of its first row) cut it; rows without keys
+      // always lie in such tiles
+      const int lo_last = lo_of(qt * kBlk + kBlk - 1), lim_first = lim_of(qt * kBlk);
+      if (n == 0) {   // no query of the tile has a key: dQ = 0, no MMA
+        if (valid)
+          for (int c = 0; c < HD / 2; c += 8)
+            *reinterpret_cast<uint4*>(p.dq + gi * HD + (HD / 2) * g + c) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       for (int t = 0; t < n; ++t, ++it) {
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
@@ -658,12 +720,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ptx::tmem_ld32x32b_x32(t_s + 32, sr[1]);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarSFree));   // S is in registers: the next S may overwrite it
-        const int lim = key_lim - t * kBlk - 64 * g;   // this warpgroup's columns c < lim are allowed
+        const int kb = (ka + t) * kBlk;
+        const bool cut = kb < lo_last || kb + kBlk > lim_first;
+        const int base = kb + 64 * g;   // key of this warpgroup's column 0
+        const int lo_c = key_lo - base, lim_c = key_lim - base;   // columns lo_c <= c < lim_c are allowed
         float pr[64];
+        if (cut) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
-          pr[c] = (c < lim) ? x : 0.0f;
+          for (int c = 0; c < 64; ++c) {
+            const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
+            pr[c] = (c >= lo_c && c < lim_c) ? x : 0.0f;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            pr[c] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
         }
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
@@ -721,7 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
       int bh, qt;
       dq_unit(p, idx, bh, qt);
-      const int n = dq_key_tiles(p, qt);
+      int ka, n;
+      dq_range(p, qt, batch_keys(p, bh), &ka, &n);
+      if (n == 0) continue;   // no keys: nothing to load
       if (units > 0) {
         ok = wait_warp(bar(L::kBarQdEmpty), (units - 1) & 1, abort_flag, limit, kSiteLoad);
         if (!ok) break;
@@ -741,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar(L::kBarKFull + sk), T::kTileBytes);
           for (int rg = 0; rg < T::kRegions; ++rg)
-            ptx::tma_load_3d(sbase + k_off(sk) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKFull + sk), 64 * rg, t * kBlk, bh);
+            ptx::tma_load_3d(sbase + k_off(sk) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKFull + sk), 64 * rg, (ka + t) * kBlk, bh);
         }
         last_k[sk] = static_cast<int>(it);
         ok = wait_warp(bar(L::kBarVEmpty + sv), ((it / L::kVStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
@@ -749,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar(L::kBarVFull + sv), T::kTileBytes);
           for (int rg = 0; rg < T::kRegions; ++rg)
-            ptx::tma_load_3d(sbase + v_off(sv) + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarVFull + sv), 64 * rg, t * kBlk, bh);
+            ptx::tma_load_3d(sbase + v_off(sv) + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarVFull + sv), 64 * rg, (ka + t) * kBlk, bh);
         }
         last_v[sv] = static_cast<int>(it);
       }
@@ -789,7 +862,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     for (int r = 0; ok && unit_index(p, r, idx); ++r) {
       int bh, qt;
       dq_unit(p, idx, bh, qt);
-      const int n = dq_key_tiles(p, qt);
+      int ka_unused, n;
+      dq_range(p, qt, batch_keys(p, bh), &ka_unused, &n);
+      if (n == 0) continue;   // no keys: nothing to issue
       ok = wait_warp(bar(L::kBarQdFull), units & 1, abort_flag, limit, kSiteMma);
       if (!ok) break;
       ++units;
@@ -963,10 +1038,11 @@ extern "C" fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, 
   return FA_OK;
 }
 
-extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Lq, int Lk,
-                            int D, int causal, float scale, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+namespace {
+fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* LSE, void* dQ, void* dK, void* dV, const int* kv_len, int B, int H,
+                   int Lq, int Lk, int D, int window_left, int window_right, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   long long rows = 0, bh = 0;
   fa_status st = bwd_check_sizes(B, H, Lq, Lk, D, &rows, &bh);
   if (st != FA_OK) return st;
@@ -1027,7 +1103,10 @@ extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const v
   p.bh_count = static_cast<int>(bh);
   p.Lq = Lq;
   p.Lk = Lk;
-  p.causal = causal ? 1 : 0;
+  p.H = H;
+  p.win_left = window_left >= Lq - 1 ? -1 : window_left;   // a side covering every key is unbounded
+  p.win_right = window_right >= Lk - 1 ? -1 : window_right;
+  p.kv_len = kv_len;
   p.nq = (Lq + 127) / 128;
   p.nk = (Lk + 127) / 128;
   p.scale = scale;
@@ -1069,4 +1148,24 @@ extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const v
                    : cudaLaunchKernelEx(&cfg, fab::fa_bwd_dq_kernel<64>, p);
   if (err != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+}  // namespace
+
+extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Lq, int Lk,
+                            int D, int causal, float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, nullptr, B, H, Lq, Lk, D, -1, causal ? 0 : -1, scale,
+                  workspace, workspace_bytes, stream);
+}
+
+extern "C" fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                                   const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                   const int* kv_len, int B, int H, int Lq, int Lk, int D,
+                                   int window_left, int window_right, float scale, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, kv_len, B, H, Lq, Lk, D, window_left, window_right,
+                  scale, workspace, workspace_bytes, stream);
 }

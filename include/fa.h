@@ -257,6 +257,21 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  int D, int causal, float scale, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream);
 
+/*
+ * fa_bwd_masked -- fa_bwd under the band and key-padding mask of fa_fwd_strided: query
+ * i attends to key j iff i - window_left <= j <= i + window_right (-1 = unbounded side)
+ * and j < kv_len[b] (kv_len: NULL, or a 4-byte aligned device array of B int32 counts,
+ * clamped to [0, Lk]).  LSE must come from the forward with the same mask (a row left
+ * without keys has LSE = -inf there; it gets dQ = 0 and adds nothing to dK, dV).  The
+ * bands (-1, -1) and (-1, 0) without kv_len are fa_bwd's full and causal masks.
+ * Arguments, layout, workspace and errors otherwise as fa_bwd; a side below -1 or a
+ * misaligned kv_len is FA_ERR_INVALID_ARG.
+ */
+fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, void* dQ, void* dK, void* dV, const int* kv_len, int B,
+                        int H, int Lq, int Lk, int D, int window_left, int window_right,
+                        float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -187,3 +187,87 @@ def test_calls_from_a_fresh_thread():
     assert torch.equal(out["o"], o_ref)
     for a, b in zip(out["g"], g_ref):
         assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- band and key padding
+def check_masked(oracle_mod, q, k, v, do, left, right, kv_len, scale):
+    """fa_bwd_masked against oracle_attn_bwd_head_masked, with the per-element bound of
+    ``check`` (P from the key-padding forward oracle)."""
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    kl = None if kv_len is None else torch.tensor(kv_len, dtype=torch.int32, device=dev)
+    o, lse = fa.attention(qd, kd, vd, window=(left, right), kv_len=kl, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, window=(left, right), kv_len=kl, scale=scale)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    got = [t.float().cpu().numpy() for t in (dq, dk, dv)]
+    o_g = o.float().cpu().numpy()
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    f64 = lambda t: t.double().numpy()
+    for b in range(B):
+        kvb = Lk if kv_len is None else kv_len[b]
+        for h in range(H):
+            qh, kh, vh, doh = (f64(t[b, h]) for t in (q, k, v, do))
+            refs = oracle_mod.attn_bwd_head_masked(qh, kh, vh, doh, left, right, kvb, scale)
+            P = oracle_mod.attn_head_keypad(qh, kh, vh, left, right, kvb, scale, want_p=True)[2]
+            dP = doh @ vh.T
+            dS = P * (dP - (P * dP).sum(axis=1)[:, None])
+            e = 2 * U * np.abs(doh * o_g[b, h]).sum(axis=1)
+            w = P * e[:, None] + U * np.abs(dS)
+            bnds = (scale * w @ np.abs(kh), scale * w.T @ np.abs(qh), U * P.T @ np.abs(doh))
+            for name, g_, ref, bnd in zip(("dQ", "dK", "dV"), got, refs, bnds):
+                gh = g_[b, h]
+                assert np.isfinite(gh).all(), name
+                tol = 2.0 * (bnd + U * np.abs(ref)) + 1e-3
+                bad = np.abs(gh - ref) > tol
+                assert not bad.any(), f"{name} {(b, h)}: {bad.sum()} over the bound, max err {np.abs(gh - ref).max():.3e}"
+
+
+@pytest.mark.parametrize("left,right", [(100, 0), (64, 64), (-1, 30), (200, -1), (0, 0)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_band_against_oracle(oracle_mod, left, right, D):
+    q, k, v = make_qkv(1, 2, 500, 500, D, seed=left + 3 * right + D)
+    do = make_do(1, 2, 500, D, seed=left + right)
+    check_masked(oracle_mod, q, k, v, do, left, right, None, 1.0 / math.sqrt(D))
+
+
+@pytest.mark.parametrize("left,right", [(-1, -1), (-1, 0), (50, 50)])
+def test_backward_key_padding_against_oracle(oracle_mod, left, right):
+    q, k, v = make_qkv(4, 2, 300, 420, 128, seed=71 + left)
+    do = make_do(4, 2, 300, 128, seed=71)
+    check_masked(oracle_mod, q, k, v, do, left, right, [420, 0, 1, 257], 128 ** -0.5)
+
+
+def test_backward_masked_full_and_causal_equal_fa_bwd():
+    """(-1, -1) and (-1, 0) with no padding through fa_bwd_masked give fa_bwd's bits."""
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(2, 2, 600, 700, 128, seed=73))
+    do = make_do(2, 2, 600, 128, seed=73).to(dev)
+    for causal, win in ((False, (-1, -1)), (True, (-1, 0))):
+        o, lse = fa.attention(q, k, v, causal=causal, split=False)
+        a = fa.attention_backward(q, k, v, o, lse, do, causal=causal)
+        st, nb = fa.fa_bwd_workspace_size(2, 2, 600, 700, 128, causal)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        b = [torch.empty_like(t) for t in (q, k, v)]
+        assert fa.fa_bwd_masked(q, k, v, o, do, lse, *b, None, 2, 2, 600, 700, 128, win[0], win[1],
+                                128 ** -0.5, ws, nb, None) == fa.FA_OK
+        torch.cuda.synchronize()
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
+def test_autograd_with_window_and_padding(oracle_mod):
+    dev = torch.device("cuda:0")
+    q, k, v = make_qkv(2, 2, 256, 256, 64, seed=79)
+    do = make_do(2, 2, 256, 64, seed=79)
+    kl = torch.tensor([256, 100], dtype=torch.int32, device=dev)
+    qg, kg, vg = (t.to(dev).requires_grad_(True) for t in (q, k, v))
+    o = fa.flash_attention(qg, kg, vg, window=(40, 0), kv_len=kl)
+    o.backward(do.to(dev))
+    for b, kvb in enumerate((256, 100)):
+        for h in range(2):
+            ref = oracle_mod.attn_bwd_head_masked(q[b, h].double().numpy(), k[b, h].double().numpy(),
+                                                  v[b, h].double().numpy(), do[b, h].double().numpy(),
+                                                  40, 0, kvb, 0.125)
+            for g_, r in zip((qg.grad, kg.grad, vg.grad), ref):
+                assert np.abs(g_[b, h].float().cpu().numpy() - r).max() < 5e-2
