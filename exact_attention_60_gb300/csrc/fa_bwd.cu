@@ -140,6 +140,7 @@ struct BwdParams {
   int n_units;
   float scale;
   float scale_log2;    // scale * log2(e)
+  uint32_t flags;      // test hooks (fa_debug_set): bit 0 withholds the first V tile of dK/dV
   unsigned long long wait_limit_ns;
 };
 
@@ -460,10 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         if (!ok) break;
       }
       if (lane == 0) {
+        // test hook (bit 0): the first unit's V tile is never loaded, so kv_full never
+        // completes and the waits on it run out (FA_ERR_TIMEOUT) instead of the kernel hanging
+        const bool withhold_v = (p.flags & 1u) && units == 0;
         ptx::mbar_arrive_expect_tx(bar(L::kBarKvFull), 2 * T::kTileBytes);
         for (int rg = 0; rg < T::kRegions; ++rg) {
           ptx::tma_load_3d(sbase + L::kOffK + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
-          ptx::tma_load_3d(sbase + L::kOffV + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
+          if (!withhold_v)
+            ptx::tma_load_3d(sbase + L::kOffV + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
         }
       }
       ++units;
@@ -1113,6 +1118,8 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   const unsigned long long lim = fa_internal_wait_limit_ns();
   p.wait_limit_ns = lim ? lim : fab::kDefaultWaitNs;
+  p.flags = fa_internal_debug_flags();
+  if (p.flags & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
 
   // 1. Delta = rowsum(dO * O) and LSE * log2(e), padded to whole tiles.  Launch errors
   // come from the launch call itself (not cudaGetLastError, which would also report an

@@ -1702,6 +1702,7 @@ extern "C" fa_status fa_last_device_status(cudaStream_t stream) {
 }
 
 unsigned long long fa_internal_wait_limit_ns() { return g_wait_limit_ns.load(); }
+unsigned fa_internal_debug_flags() { return g_debug_flags.load(); }
 
 extern "C" fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns) {
   g_debug_flags.store(flags);

@@ -8,3 +8,6 @@ unsigned fa_bwd_take_device_status();
 
 // The wait limit set with fa_debug_set (0 = the default of one second).
 unsigned long long fa_internal_wait_limit_ns();
+
+// The test-hook flags set with fa_debug_set.
+unsigned fa_internal_debug_flags();

@@ -287,9 +287,10 @@ fa_status fa_last_device_status(cudaStream_t stream);
 /*
  * fa_debug_set -- test hook, process-wide.  `wait_limit_ns` bounds every
  * pipeline wait inside the kernels (0 restores the default of one second).
- * `flags` bit 0 makes the load warp withhold the first value-tile load, so
- * that the consumers' waits run out and the kernel reports FA_ERR_TIMEOUT
- * through fa_last_device_status() instead of completing.  Bit 1 makes every
+ * `flags` bit 0 makes the load warp withhold the first value-tile load (of the
+ * forward kernel, and of the backward's dK/dV kernel), so that the consumers' waits
+ * run out and the kernel reports FA_ERR_TIMEOUT through fa_last_device_status()
+ * instead of completing.  Bit 1 makes every
  * launch fail with FA_ERR_CUDA before anything is queued.  Bit 2 makes
  * fa_fwd_window run its band kernel also for the bands (-1, 0) and (-1, -1), so
  * that it can be compared with fa_fwd's kernels.  Not for production use;

@@ -53,3 +53,35 @@ def test_simulated_launch_failure(restore_hooks):
     assert st == fa.FA_ERR_CUDA
     torch.cuda.synchronize()
     assert (o.float() == 7.0).all() and (lse == 7.0).all()
+
+
+def test_backward_withheld_load_times_out_and_context_survives(oracle_mod, restore_hooks):
+    """The dK/dV kernel's first V tile is withheld: its waits run out, the status word says
+    FA_ERR_TIMEOUT, and the next backward is exact again."""
+    dev = torch.device("cuda:0")
+    q, k, v = make_qkv(1, 2, 300, 300, 128, seed=23)
+    g = torch.Generator().manual_seed(5)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention(qd, kd, vd, causal=True)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    fa.fa_debug_set(1, 20_000_000)
+    fa.attention_backward(qd, kd, vd, o, lse, dod, causal=True)
+    assert fa.fa_last_device_status() == fa.FA_ERR_TIMEOUT
+    fa.fa_debug_set(0, 0)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=True)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    ref = oracle_mod.attn_bwd_head(q[0, 1].double().numpy(), k[0, 1].double().numpy(),
+                                   v[0, 1].double().numpy(), do[0, 1].double().numpy(), True, 128 ** -0.5)
+    for got, r in zip((dq, dk, dv), ref):
+        assert np.abs(got[0, 1].float().cpu().numpy() - r).max() < 5e-2
+
+
+def test_backward_simulated_launch_failure(restore_hooks):
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(1, 1, 128, 128, 64, seed=24))
+    o, lse = fa.attention(q, k, v)
+    fa.fa_debug_set(2, 0)
+    with pytest.raises(fa.FaError) as e:
+        fa.attention_backward(q, k, v, o, lse, torch.randn_like(q))
+    assert e.value.status == fa.FA_ERR_CUDA
