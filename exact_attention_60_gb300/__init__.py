@@ -9,7 +9,7 @@ import math
 
 from ._native import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,
                       FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, fa_bwd, fa_bwd_masked,
-                      fa_bwd_workspace_size,
+                      fa_bwd_strided, fa_bwd_workspace_size,
                       fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_strided, fa_fwd_window,
                       fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status, fa_status_string)
 
@@ -131,14 +131,17 @@ def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float |
     Lk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v, o, do must be bf16 or fp16")
     for t in (q, k, v, o, do):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
+        if t.dtype != dtype or not t.is_cuda or t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError("q, k, v, o, do must be CUDA tensors of one dtype, [B, H, L, D], last dim contiguous")
     if lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 CUDA tensor")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = torch.empty((B, H, Lq, D), dtype=dtype, device=q.device) if dq is None else dq
+    dk = torch.empty((B, H, Lk, D), dtype=dtype, device=q.device) if dk is None else dk
+    dv = torch.empty((B, H, Lk, D), dtype=dtype, device=q.device) if dv is None else dv
     st, nbytes = fa_bwd_workspace_size(B, H, Lq, Lk, D, causal)
     if st != FA_OK:
         raise FaError(st)
@@ -147,16 +150,26 @@ def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float |
     if ws is None or ws.numel() < max(nbytes, 256):
         ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
         _bwd_workspaces[key] = ws
-    if window is None and kv_len is None:
+    if kv_len is not None and (kv_len.dtype != torch.int32 or kv_len.numel() != B
+                               or not kv_len.is_cuda or not kv_len.is_contiguous()):
+        raise ValueError("kv_len must be a contiguous int32 CUDA tensor of B entries")
+    plain = dtype == torch.bfloat16 and all(t.is_contiguous() for t in (q, k, v, o, do, dq, dk, dv))
+    if not plain:
+        left, right = (-1, 0 if causal else -1) if window is None else (int(window[0]), int(window[1]))
+        if window is not None and causal:
+            right = 0
+        code = FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16
+        st = fa_bwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], o, o.stride()[:3],
+                            do, do.stride()[:3], lse, dq, dq.stride()[:3], dk, dk.stride()[:3], dv,
+                            dv.stride()[:3], kv_len, B, H, Lq, Lk, D, left, right, scale, code, ws,
+                            ws.numel(), stream)
+    elif window is None and kv_len is None:
         st = fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Lq, Lk, D, causal, scale, ws, ws.numel(),
                     stream)
     else:
         left, right = (-1, 0 if causal else -1) if window is None else (int(window[0]), int(window[1]))
         if window is not None and causal:
             right = 0
-        if kv_len is not None and (kv_len.dtype != torch.int32 or kv_len.numel() != B
-                                   or not kv_len.is_cuda or not kv_len.is_contiguous()):
-            raise ValueError("kv_len must be a contiguous int32 CUDA tensor of B entries")
         st = fa_bwd_masked(q, k, v, o, do, lse, dq, dk, dv, kv_len, B, H, Lq, Lk, D, left, right,
                            scale, ws, ws.numel(), stream)
     if st != FA_OK:

@@ -22,7 +22,7 @@ FA_DTYPE_FP16 = 1
 # Every symbol include/fa.h declares.
 EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_strided",
             "fa_fwd_noalloc",
-            "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_masked", "fa_status_string",
+            "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_masked", "fa_bwd_strided", "fa_status_string",
             "fa_last_device_status",
             "fa_debug_set")
 
@@ -63,6 +63,10 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_bwd.argtypes = [vp] * 9 + [ctypes.c_int] * 6 + [ctypes.c_float, vp, ctypes.c_size_t, vp]
     lib.fa_bwd_masked.restype = ctypes.c_int
     lib.fa_bwd_masked.argtypes = [vp] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd_strided.restype = ctypes.c_int
+    lib.fa_bwd_strided.argtypes = [vp, lp3, vp, lp3, vp, lp3, vp, lp3, vp, lp3, vp, vp, lp3, vp, lp3,
+                                   vp, lp3, vp] + [ctypes.c_int] * 7 + \
+        [ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_last_device_status.restype = ctypes.c_int
@@ -174,6 +178,19 @@ def fa_bwd_masked(Q, K, V, O, dO, LSE, dQ, dK, dV, kv_len, B, H, Lq, Lk, D, wind
                                 _ptr(dK), _ptr(dV), _ptr(kv_len), int(B), int(H), int(Lq), int(Lk),
                                 int(D), int(window_left), int(window_right), float(scale),
                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_strided(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, dO, do_stride, LSE, dQ,
+                   dq_stride, dK, dk_stride, dV, dv_stride, kv_len, B, H, Lq, Lk, D, window_left,
+                   window_right, scale, dtype, workspace, workspace_bytes, stream=None) -> int:
+    """C ``fa_bwd_strided``; strides are sequences of three element strides."""
+    return load().fa_bwd_strided(_ptr(Q), _strides3(q_stride), _ptr(K), _strides3(k_stride), _ptr(V),
+                                 _strides3(v_stride), _ptr(O), _strides3(o_stride), _ptr(dO),
+                                 _strides3(do_stride), _ptr(LSE), _ptr(dQ), _strides3(dq_stride),
+                                 _ptr(dK), _strides3(dk_stride), _ptr(dV), _strides3(dv_stride),
+                                 _ptr(kv_len), int(B), int(H), int(Lq), int(Lk), int(D),
+                                 int(window_left), int(window_right), float(scale), int(dtype),
+                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_status_string(status: int) -> str:

@@ -35,9 +35,11 @@
 // status word (read by fa_last_device_status) and every role drains and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <string.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -106,9 +108,32 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, unsigned
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
 // B K-major or (b_mn_major) MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major, bool f16 = false) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two floats to the packed 16-bit pair of the I/O type, and back.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kF16) return ptx::pack_f16x2(lo, hi);
+  else return ptx::pack_bf16x2(lo, hi);
+}
+template <bool kF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (kF16) {
+    __half2 h;
+    memcpy(&h, &v, 4);
+    return __half22float2(h);
+  } else {
+    return ptx::unpack_bf16x2(v);
+  }
+}
+
+// Element (bh, row) of a [B,H,L,D] tensor with element strides st.
+__device__ __forceinline__ long long row_offset(const long long* st, int H, int bh, long long row) {
+  const int b = bh / H, h = bh - b * H;
+  return b * st[0] + h * st[1] + row * st[2];
 }
 
 // Shared-memory descriptor of a 128B-swizzled operand (see the forward kernel).
@@ -119,15 +144,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 }
 
 struct BwdParams {
-  CUtensorMap tm_q;    // 3-D views [B*H][L][D], box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_q;    // 4-D views [B][H][L][D] (caller's strides), box 64 x 128 x 1 x 1, 128B swizzle
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
   const float* delta;  // [B*H][nq*128] rowsum(dO * O), 0 past Lq
   const float* lse2;   // [B*H][nq*128] LSE * log2(e), +inf past Lq
-  __nv_bfloat16* dq;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  uint16_t* dq;        // bf16 or fp16 elements, written through the strides below
+  uint16_t* dk;
+  uint16_t* dv;
+  long long dq_s[3], dk_s[3], dv_s[3];   // element strides {batch, head, row}
   int bh_count;
   int H;
   int Lq;
@@ -212,38 +238,44 @@ __device__ __forceinline__ void dq_unit(const BwdParams& p, int idx, int& bh, in
 // both outputs can be copied into shared memory a tile at a time with bulk copies:
 // delta[row] = dO_q . O_q and lse2[row] = LSE_q * log2(e) for q < Lq; 0 and +inf past Lq
 // (+inf makes every recomputed probability of a padded query exactly 0).
-template <int HD>
-__global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __nv_bfloat16* __restrict__ O,
-                                                           const __nv_bfloat16* __restrict__ dO,
-                                                           const float* __restrict__ lse,
-                                                           float* __restrict__ delta,
-                                                           float* __restrict__ lse2,
-                                                           long long rows_pad, int Lq, int Lpad) {
+// Rows of O and dO are read through their strides (o_s, do_s: {batch, head, row}).
+struct DeltaArgs {
+  const uint16_t* O;
+  const uint16_t* dO;
+  const float* lse;
+  float* delta;
+  float* lse2;
+  long long o_s[3], do_s[3];
+  long long rows_pad;
+  int Lq, Lpad, H;
+};
+
+template <int HD, bool kF16>
+__global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __grid_constant__ DeltaArgs a) {
   constexpr int kT = HD / 8;   // threads per row, 8 elements (16 bytes) each
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / kT;
   const int part = static_cast<int>(tid % kT);
-  const long long bh = row / Lpad;
-  const int q = static_cast<int>(row - bh * Lpad);
-  const bool valid = row < rows_pad && q < Lq;
-  const long long src = bh * Lq + q;   // row of O, dO and LSE
+  const int bh = static_cast<int>(row / a.Lpad);
+  const int q = static_cast<int>(row - static_cast<long long>(bh) * a.Lpad);
+  const bool valid = row < a.rows_pad && q < a.Lq;
   float acc = 0.0f;
   if (valid) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + src * HD) + part);
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + src * HD) + part);
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    const uint4 x4 = __ldg(reinterpret_cast<const uint4*>(a.O + row_offset(a.o_s, a.H, bh, q)) + part);
+    const uint4 y4 = __ldg(reinterpret_cast<const uint4*>(a.dO + row_offset(a.do_s, a.H, bh, q)) + part);
+    const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 x = ptx::unpack_bf16x2(av[e]), y = ptx::unpack_bf16x2(bv[e]);
+      const float2 x = unpack2<kF16>(xv[e]), y = unpack2<kF16>(yv[e]);
       acc = fmaf(x.x, y.x, acc);
       acc = fmaf(x.y, y.y, acc);
     }
   }
 #pragma unroll
   for (int off = kT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (part == 0 && row < rows_pad) {
-    delta[row] = valid ? acc : 0.0f;
-    lse2[row] = valid ? __ldg(lse + src) * kLog2e : INFINITY;
+  if (part == 0 && row < a.rows_pad) {
+    a.delta[row] = valid ? acc : 0.0f;
+    a.lse2[row] = valid ? __ldg(a.lse + static_cast<long long>(bh) * a.Lq + q) * kLog2e : INFINITY;
   }
 }
 
@@ -279,7 +311,7 @@ struct DkdvLayout {
 static_assert(DkdvLayout<128>::kAlloc <= 232448, "dK/dV shared memory (D=128)");
 static_assert(DkdvLayout<64>::kAlloc <= 232448, "dK/dV shared memory (D=64)");
 
-template <int HD>
+template <int HD, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = DkdvLayout<HD>;
   using T = Tiles<HD>;
@@ -340,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       int q_first, n;
       dkdv_range(p, kt, kvl, &q_first, &n);
       const int k = kt * kBlk + row;   // this thread's key
-      const size_t orow = (static_cast<size_t>(bh) * p.Lk + (k < p.Lk ? k : 0)) * HD;
-      __nv_bfloat16* mine = (g ? p.dk : p.dv) + orow;   // warpgroup 0 writes dV, 1 writes dK
+      // warpgroup 0 writes dV, 1 writes dK
+      uint16_t* mine = g ? p.dk + row_offset(p.dk_s, p.H, bh, k < p.Lk ? k : 0)
+                         : p.dv + row_offset(p.dv_s, p.H, bh, k < p.Lk ? k : 0);
       if (n == 0) {   // no query sees these keys: their gradients are zero
         if (k < p.Lk)
           for (int c = 0; c < HD; c += 8) *reinterpret_cast<uint4*>(mine + c) = make_uint4(0, 0, 0, 0);
@@ -388,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         }
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack2<kF16>(pr[2 * c], pr[2 * c + 1]);
         ptx::tmem_st32x32b_x32(t_s, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -404,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         for (int c = 0; c < 32; ++c) {
           const float a = pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt[2 * c]);
           const float b = pr[2 * c + 1] * (__uint_as_float(sr[c >> 4][(2 * c + 1) & 31]) - dlt[2 * c + 1]);
-          pk[c] = ptx::pack_bf16x2(a, b);
+          pk[c] = pack2<kF16>(a, b);
         }
         ptx::tmem_st32x32b_x32(t_dp, pk);
         ptx::tmem_st_wait();
@@ -427,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
           uint32_t pk16[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            pk16[c] = ptx::pack_bf16x2(__uint_as_float(a[2 * c]) * mul, __uint_as_float(a[2 * c + 1]) * mul);
+            pk16[c] = pack2<kF16>(__uint_as_float(a[2 * c]) * mul, __uint_as_float(a[2 * c + 1]) * mul);
           if (k < p.Lk) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
@@ -466,9 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         const bool withhold_v = (p.flags & 1u) && units == 0;
         ptx::mbar_arrive_expect_tx(bar(L::kBarKvFull), 2 * T::kTileBytes);
         for (int rg = 0; rg < T::kRegions; ++rg) {
-          ptx::tma_load_3d(sbase + L::kOffK + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
+          ptx::tma_load_4d(sbase + L::kOffK + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
           if (!withhold_v)
-            ptx::tma_load_3d(sbase + L::kOffV + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh);
+            ptx::tma_load_4d(sbase + L::kOffV + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarKvFull), 64 * rg, kt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
         }
       }
       ++units;
@@ -482,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
           const size_t rowp = (static_cast<size_t>(bh) * p.nq + qt) * kBlk;   // padded row of the tile
           ptx::mbar_arrive_expect_tx(full, 2 * T::kTileBytes + 2 * kBlk * 4);
           for (int rg = 0; rg < T::kRegions; ++rg) {
-            ptx::tma_load_3d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, full, 64 * rg, qt * kBlk, bh);
-            ptx::tma_load_3d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, full, 64 * rg, qt * kBlk, bh);
+            ptx::tma_load_4d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, full, 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
+            ptx::tma_load_4d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, full, 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
           }
           ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes, p.lse2 + rowp, kBlk * 4, full);
           ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes + kBlk * 4, p.delta + rowp, kBlk * 4, full);
@@ -498,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA warp (warp-uniform, elected issue)
-    constexpr uint32_t kIdescS = make_idesc(kBlk, kBlk, false);   // S^T, dP^T: 128 x 128, K = HD
-    constexpr uint32_t kIdescAcc = make_idesc(kBlk, HD, true);    // dV, dK: 128 x HD, K = 128 queries
+    constexpr uint32_t kIdescS = make_idesc(kBlk, kBlk, false, kF16);   // S^T, dP^T: 128 x 128, K = HD
+    constexpr uint32_t kIdescAcc = make_idesc(kBlk, HD, true, kF16);    // dV, dK: 128 x HD, K = 128 queries
     const uint64_t desc_k = sw128_desc(sbase + L::kOffK, 16, 1024);
     const uint64_t desc_v = sw128_desc(sbase + L::kOffV, 16, 1024);
     auto kmaj = [&](uint32_t off) { return sw128_desc(sbase + off, 16, 1024); };
@@ -628,7 +661,7 @@ struct DqLayout {
 static_assert(DqLayout<128>::kAlloc <= 232448, "dQ shared memory (D=128)");
 static_assert(DqLayout<64>::kAlloc <= 232448, "dQ shared memory (D=64)");
 
-template <int HD>
+template <int HD, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = DqLayout<HD>;
   using T = Tiles<HD>;
@@ -694,7 +727,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       dq_range(p, qt, kvl, &ka, &n);
       const int q = qt * kBlk + row;   // this thread's query
       const bool valid = q < p.Lq;
-      const size_t gi = static_cast<size_t>(bh) * p.Lq + (valid ? q : 0);
       const size_t gp = (static_cast<size_t>(bh) * p.nq + qt) * kBlk + row;   // padded row
       const float lse2 = valid ? p.lse2[gp] : 0.0f;
       const float dlt = p.delta[gp];
@@ -713,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (n == 0) {   // no query of the tile has a key: dQ = 0, no MMA
         if (valid)
           for (int c = 0; c < HD / 2; c += 8)
-            *reinterpret_cast<uint4*>(p.dq + gi * HD + (HD / 2) * g + c) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(p.dq + row_offset(p.dq_s, p.H, bh, q) + (HD / 2) * g + c) =
+                make_uint4(0, 0, 0, 0);
         continue;
       }
       for (int t = 0; t < n; ++t, ++it) {
@@ -749,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          pk[c] = ptx::pack_bf16x2(pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt),
+          pk[c] = pack2<kF16>(pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt),
                                    pr[2 * c + 1] * (__uint_as_float(sr[c >> 4][(2 * c + 1) & 31]) - dlt));
         ptx::tmem_st32x32b_x32(t_dp, pk);
         ptx::tmem_st_wait();
@@ -762,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       ++acc_count;
       ptx::tc_fence_after();
       // Epilogue: each warpgroup writes its half of the row's columns.
-      __nv_bfloat16* dst = p.dq + gi * HD + (HD / 2) * g;
+      uint16_t* dst = p.dq + row_offset(p.dq_s, p.H, bh, valid ? q : 0) + (HD / 2) * g;
 #pragma unroll
       for (int c0 = 0; c0 < HD / 2; c0 += 32) {
         uint32_t a[32];
@@ -770,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         uint32_t pk16[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk16[c] = ptx::pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale, __uint_as_float(a[2 * c + 1]) * p.scale);
+          pk16[c] = pack2<kF16>(__uint_as_float(a[2 * c]) * p.scale, __uint_as_float(a[2 * c + 1]) * p.scale);
         if (valid) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -807,8 +840,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(bar(L::kBarQdFull), 2 * T::kTileBytes);
         for (int rg = 0; rg < T::kRegions; ++rg) {
-          ptx::tma_load_3d(sbase + L::kOffQ + rg * T::kRegionBytes, &p.tm_q, bar(L::kBarQdFull), 64 * rg, qt * kBlk, bh);
-          ptx::tma_load_3d(sbase + L::kOffDo + rg * T::kRegionBytes, &p.tm_do, bar(L::kBarQdFull), 64 * rg, qt * kBlk, bh);
+          ptx::tma_load_4d(sbase + L::kOffQ + rg * T::kRegionBytes, &p.tm_q, bar(L::kBarQdFull), 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
+          ptx::tma_load_4d(sbase + L::kOffDo + rg * T::kRegionBytes, &p.tm_do, bar(L::kBarQdFull), 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
         }
       }
       ++units;
@@ -819,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar(L::kBarKFull + sk), T::kTileBytes);
           for (int rg = 0; rg < T::kRegions; ++rg)
-            ptx::tma_load_3d(sbase + k_off(sk) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKFull + sk), 64 * rg, (ka + t) * kBlk, bh);
+            ptx::tma_load_4d(sbase + k_off(sk) + rg * T::kRegionBytes, &p.tm_k, bar(L::kBarKFull + sk), 64 * rg, (ka + t) * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
         }
         last_k[sk] = static_cast<int>(it);
         ok = wait_warp(bar(L::kBarVEmpty + sv), ((it / L::kVStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
@@ -827,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar(L::kBarVFull + sv), T::kTileBytes);
           for (int rg = 0; rg < T::kRegions; ++rg)
-            ptx::tma_load_3d(sbase + v_off(sv) + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarVFull + sv), 64 * rg, (ka + t) * kBlk, bh);
+            ptx::tma_load_4d(sbase + v_off(sv) + rg * T::kRegionBytes, &p.tm_v, bar(L::kBarVFull + sv), 64 * rg, (ka + t) * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
         }
         last_v[sv] = static_cast<int>(it);
       }
@@ -842,8 +875,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA warp (warp-uniform, elected issue)
-    constexpr uint32_t kIdescS = make_idesc(kBlk, kBlk, false);
-    constexpr uint32_t kIdescAcc = make_idesc(kBlk, HD, true);
+    constexpr uint32_t kIdescS = make_idesc(kBlk, kBlk, false, kF16);
+    constexpr uint32_t kIdescAcc = make_idesc(kBlk, HD, true, kF16);
     const uint64_t desc_q = sw128_desc(sbase + L::kOffQ, 16, 1024);
     const uint64_t desc_do = sw128_desc(sbase + L::kOffDo, 16, 1024);
     auto kmaj = [&](uint32_t off) { return sw128_desc(sbase + off, 16, 1024); };
@@ -932,6 +965,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   }
 }
 
+// Zero the rows of a strided [B,H,L,D] tensor (the key gradients when there is no query).
+__global__ void __launch_bounds__(256) fa_bwd_zero_kernel(uint16_t* base, long long s0, long long s1,
+                                                          long long s2, int H, int L, long long rows,
+                                                          int D) {
+  const int per = D / 8;   // 16-byte chunks per row
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * per;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / per;
+    const int c = static_cast<int>(i - r * per) * 8;
+    const long long bh = r / L, l = r - bh * L;
+    const long long b = bh / H, h = bh - b * H;
+    *reinterpret_cast<uint4*>(base + b * s0 + h * s1 + l * s2 + c) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 }  // namespace fab
 
 // ============================================================================ host side
@@ -941,7 +989,46 @@ using fab::BwdParams;
 
 std::mutex g_bwd_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
-bool g_bwd_ready[64][2] = {};
+bool g_bwd_ready[64][2][2] = {};   // [device][D == 128][fp16]: shared-memory opt-in done
+
+using BwdKernel = void (*)(const BwdParams);
+BwdKernel dkdv_kernel(int D, bool f16) {
+  if (D == 128) return f16 ? fab::fa_bwd_dkdv_kernel<128, true> : fab::fa_bwd_dkdv_kernel<128, false>;
+  return f16 ? fab::fa_bwd_dkdv_kernel<64, true> : fab::fa_bwd_dkdv_kernel<64, false>;
+}
+BwdKernel dq_kernel(int D, bool f16) {
+  if (D == 128) return f16 ? fab::fa_bwd_dq_kernel<128, true> : fab::fa_bwd_dq_kernel<128, false>;
+  return f16 ? fab::fa_bwd_dq_kernel<64, true> : fab::fa_bwd_dq_kernel<64, false>;
+}
+using DeltaKernel = void (*)(const fab::DeltaArgs);
+DeltaKernel delta_kernel(int D, bool f16) {
+  if (D == 128) return f16 ? fab::fa_bwd_delta_kernel<128, true> : fab::fa_bwd_delta_kernel<128, false>;
+  return f16 ? fab::fa_bwd_delta_kernel<64, true> : fab::fa_bwd_delta_kernel<64, false>;
+}
+
+// Element strides {batch, head, row} of every tensor of one backward call.
+struct BwdStrides {
+  long long q[3], k[3], v[3], o[3], dO[3], dq[3], dk[3], dv[3];
+};
+
+void contiguous3(long long H, long long L, int D, long long* st) {
+  st[2] = D;
+  st[1] = L * D;
+  st[0] = H * L * D;
+}
+
+BwdStrides contiguous_bwd(int H, int Lq, int Lk, int D) {
+  BwdStrides sd;
+  contiguous3(H, Lq, D, sd.q);
+  contiguous3(H, Lk, D, sd.k);
+  contiguous3(H, Lk, D, sd.v);
+  contiguous3(H, Lq, D, sd.o);
+  contiguous3(H, Lq, D, sd.dO);
+  contiguous3(H, Lq, D, sd.dq);
+  contiguous3(H, Lk, D, sd.dk);
+  contiguous3(H, Lk, D, sd.dv);
+  return sd;
+}
 
 bool bwd_overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
@@ -950,7 +1037,7 @@ bool bwd_overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 size_t bwd_round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-fa_status bwd_prepare(int D, int* sm_count) {
+fa_status bwd_prepare(int D, bool f16, int* sm_count) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
@@ -974,34 +1061,37 @@ fa_status bwd_prepare(int D, int* sm_count) {
       return FA_ERR_CUDA;
     g_bwd_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  const int di = (D == 128) ? 1 : 0;
-  if (!g_bwd_ready[dev][di]) {
-    cudaError_t e1, e2;
-    if (D == 128) {
-      e1 = cudaFuncSetAttribute(fab::fa_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fab::DkdvLayout<128>::kAlloc);
-      e2 = cudaFuncSetAttribute(fab::fa_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fab::DqLayout<128>::kAlloc);
-    } else {
-      e1 = cudaFuncSetAttribute(fab::fa_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fab::DkdvLayout<64>::kAlloc);
-      e2 = cudaFuncSetAttribute(fab::fa_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fab::DqLayout<64>::kAlloc);
-    }
-    if (e1 != cudaSuccess || e2 != cudaSuccess) return FA_ERR_CUDA;
-    g_bwd_ready[dev][di] = true;
+  const int di = (D == 128) ? 1 : 0, ti = f16 ? 1 : 0;
+  if (!g_bwd_ready[dev][di][ti]) {
+    const int dkdv_smem = D == 128 ? fab::DkdvLayout<128>::kAlloc : fab::DkdvLayout<64>::kAlloc;
+    const int dq_smem = D == 128 ? fab::DqLayout<128>::kAlloc : fab::DqLayout<64>::kAlloc;
+    if (cudaFuncSetAttribute(dkdv_kernel(D, f16), cudaFuncAttributeMaxDynamicSharedMemorySize, dkdv_smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dq_kernel(D, f16), cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
+            cudaSuccess)
+      return FA_ERR_CUDA;
+    g_bwd_ready[dev][di][ti] = true;
   }
   return FA_OK;
 }
 
-bool bwd_encode_map(CUtensorMap* map, const void* base, long long BH, long long L, int D) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L) * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estrides[3] = {1, 1, 1};
-  return g_bwd_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                      estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// 4-D tensor map [B][H][L][D] over element strides st = {batch, head, row} (as the forward's;
+// a size-1 dimension's stride addresses nothing and is replaced by a valid one).
+bool bwd_encode_map(CUtensorMap* map, const void* base, long long B, long long H, long long L, int D,
+                    const long long* st, bool f16) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  const long long row = L > 1 ? st[2] : D;
+  const long long head = H > 1 ? st[1] : row * L;
+  const long long batch = B > 1 ? st[0] : head * H;
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(row) * 2, static_cast<cuuint64_t>(head) * 2,
+                           static_cast<cuuint64_t>(batch) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estrides[4] = {1, 1, 1, 1};
+  return g_bwd_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                      const_cast<void*>(base), dims, strides, box, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Size checks shared by fa_bwd and fa_bwd_workspace_size; *rows = B*H*Lq.
@@ -1046,19 +1136,35 @@ extern "C" fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, 
 namespace {
 fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* LSE, void* dQ, void* dK, void* dV, const int* kv_len, int B, int H,
-                   int Lq, int Lk, int D, int window_left, int window_right, float scale,
-                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                   int Lq, int Lk, int D, int window_left, int window_right, float scale, bool f16,
+                   const BwdStrides& sd, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  using fa_layout::no_self_overlap;
+  using fa_layout::span_bytes;
+  using fa_layout::strides_ok;
   long long rows = 0, bh = 0;
   fa_status st = bwd_check_sizes(B, H, Lq, Lk, D, &rows, &bh);
   if (st != FA_OK) return st;
-  const size_t bytes_k = static_cast<size_t>(bh) * Lk * D * 2;
+  if (bh * Lk == 0) return FA_OK;
   if (rows == 0) {   // no query rows: every key gradient is zero
-    if (bytes_k == 0) return FA_OK;
     if (!dK || !dV || (reinterpret_cast<uintptr_t>(dK) | reinterpret_cast<uintptr_t>(dV)) & 15u)
       return FA_ERR_INVALID_ARG;
-    if (cudaMemsetAsync(dK, 0, bytes_k, stream) != cudaSuccess ||
-        cudaMemsetAsync(dV, 0, bytes_k, stream) != cudaSuccess)
-      return FA_ERR_CUDA;
+    if (!strides_ok(B, H, Lk, D, sd.dk) || !strides_ok(B, H, Lk, D, sd.dv) ||
+        !no_self_overlap(B, H, Lk, D, sd.dk) || !no_self_overlap(B, H, Lk, D, sd.dv))
+      return FA_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+    const long long krows = bh * Lk;
+    const unsigned blocks = static_cast<unsigned>(std::min<long long>((krows * (D / 8) + 255) / 256, 65535));
+    for (int which = 0; which < 2; ++which) {
+      const long long* s3 = which ? sd.dv : sd.dk;
+      cudaLaunchConfig_t zc = {};
+      zc.gridDim = dim3(blocks);
+      zc.blockDim = dim3(256);
+      zc.stream = stream;
+      if (cudaLaunchKernelEx(&zc, fab::fa_bwd_zero_kernel, static_cast<uint16_t*>(which ? dV : dK), s3[0],
+                             s3[1], s3[2], H, Lk, krows, D) != cudaSuccess)
+        return FA_ERR_CUDA;
+    }
     return FA_OK;
   }
   if (!(scale > 0.0f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -1074,15 +1180,25 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
     bits |= reinterpret_cast<uintptr_t>(x);
   }
   if (bits & 15u) return FA_ERR_INVALID_ARG;
-  const size_t bytes_q = static_cast<size_t>(rows) * D * 2, bytes_l = static_cast<size_t>(rows) * 4;
+  if (!strides_ok(B, H, Lq, D, sd.q) || !strides_ok(B, H, Lk, D, sd.k) || !strides_ok(B, H, Lk, D, sd.v) ||
+      !strides_ok(B, H, Lq, D, sd.o) || !strides_ok(B, H, Lq, D, sd.dO) || !strides_ok(B, H, Lq, D, sd.dq) ||
+      !strides_ok(B, H, Lk, D, sd.dk) || !strides_ok(B, H, Lk, D, sd.dv) ||
+      !no_self_overlap(B, H, Lq, D, sd.dq) || !no_self_overlap(B, H, Lk, D, sd.dk) ||
+      !no_self_overlap(B, H, Lk, D, sd.dv))
+    return FA_ERR_INVALID_ARG;
+  const size_t bytes_l = static_cast<size_t>(rows) * 4;
   const long long nq_ll = (Lq + 127) / 128;
   const size_t rows_pad = static_cast<size_t>(bh) * nq_ll * 128;
   const size_t half_ws = bwd_round256(rows_pad * sizeof(float));
   const size_t need_ws = 2 * half_ws;
   if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return FA_ERR_INVALID_ARG;
-  const size_t in_bytes[6] = {bytes_q, bytes_k, bytes_k, bytes_q, bytes_q, bytes_l};
-  const size_t out_bytes[4] = {bytes_q, bytes_k, bytes_k, need_ws};
+  // Inputs may share memory (they are only read); outputs and the workspace meet nothing.
+  const size_t in_bytes[6] = {span_bytes(B, H, Lq, D, sd.q), span_bytes(B, H, Lk, D, sd.k),
+                              span_bytes(B, H, Lk, D, sd.v), span_bytes(B, H, Lq, D, sd.o),
+                              span_bytes(B, H, Lq, D, sd.dO), bytes_l};
+  const size_t out_bytes[4] = {span_bytes(B, H, Lq, D, sd.dq), span_bytes(B, H, Lk, D, sd.dk),
+                               span_bytes(B, H, Lk, D, sd.dv), need_ws};
   void* outs[4] = {dQ, dK, dV, workspace};
   for (int a = 0; a < 4; ++a) {
     for (int b = 0; b < 6; ++b)
@@ -1091,20 +1207,25 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
       if (bwd_overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_INVALID_ARG;
   }
   int sm_count = 0;
-  st = bwd_prepare(D, &sm_count);
+  st = bwd_prepare(D, f16, &sm_count);
   if (st != FA_OK) return st;
 
   BwdParams p;
-  if (!bwd_encode_map(&p.tm_q, Q, bh, Lq, D) || !bwd_encode_map(&p.tm_k, K, bh, Lk, D) ||
-      !bwd_encode_map(&p.tm_v, V, bh, Lk, D) || !bwd_encode_map(&p.tm_do, dO, bh, Lq, D))
+  if (!bwd_encode_map(&p.tm_q, Q, B, H, Lq, D, sd.q, f16) || !bwd_encode_map(&p.tm_k, K, B, H, Lk, D, sd.k, f16) ||
+      !bwd_encode_map(&p.tm_v, V, B, H, Lk, D, sd.v, f16) || !bwd_encode_map(&p.tm_do, dO, B, H, Lq, D, sd.dO, f16))
     return FA_ERR_CUDA;
   float* delta = static_cast<float*>(workspace);
   float* lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + half_ws);
   p.delta = delta;
   p.lse2 = lse2;
-  p.dq = static_cast<__nv_bfloat16*>(dQ);
-  p.dk = static_cast<__nv_bfloat16*>(dK);
-  p.dv = static_cast<__nv_bfloat16*>(dV);
+  p.dq = static_cast<uint16_t*>(dQ);
+  p.dk = static_cast<uint16_t*>(dK);
+  p.dv = static_cast<uint16_t*>(dV);
+  for (int i = 0; i < 3; ++i) {
+    p.dq_s[i] = sd.dq[i];
+    p.dk_s[i] = sd.dk[i];
+    p.dv_s[i] = sd.dv[i];
+  }
   p.bh_count = static_cast<int>(bh);
   p.Lq = Lq;
   p.Lk = Lk;
@@ -1125,18 +1246,26 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   // come from the launch call itself (not cudaGetLastError, which would also report an
   // earlier error of the calling thread).
   {
+    fab::DeltaArgs da;
+    da.O = static_cast<const uint16_t*>(O);
+    da.dO = static_cast<const uint16_t*>(dO);
+    da.lse = LSE;
+    da.delta = delta;
+    da.lse2 = lse2;
+    for (int i = 0; i < 3; ++i) {
+      da.o_s[i] = sd.o[i];
+      da.do_s[i] = sd.dO[i];
+    }
+    da.rows_pad = static_cast<long long>(rows_pad);
+    da.Lq = Lq;
+    da.Lpad = static_cast<int>(nq_ll * 128);
+    da.H = H;
     const long long threads = static_cast<long long>(rows_pad) * (D / 8);
     cudaLaunchConfig_t dc = {};
     dc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
     dc.blockDim = dim3(256);
     dc.stream = stream;
-    const __nv_bfloat16* o_in = static_cast<const __nv_bfloat16*>(O);
-    const __nv_bfloat16* do_in = static_cast<const __nv_bfloat16*>(dO);
-    const long long rp = static_cast<long long>(rows_pad);
-    const int lpad = static_cast<int>(nq_ll * 128);
-    const cudaError_t e = (D == 128) ? cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<128>, o_in, do_in, LSE, delta, lse2, rp, Lq, lpad)
-                                     : cudaLaunchKernelEx(&dc, fab::fa_bwd_delta_kernel<64>, o_in, do_in, LSE, delta, lse2, rp, Lq, lpad);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&dc, delta_kernel(D, f16), da) != cudaSuccess) return FA_ERR_CUDA;
   }
   // 2. dK, dV (one unit per key tile) and 3. dQ (one unit per query tile)
   cudaLaunchConfig_t cfg = {};
@@ -1145,15 +1274,11 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.n_units = static_cast<int>(bh * p.nk);
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.dynamicSmemBytes = (D == 128) ? fab::DkdvLayout<128>::kAlloc : fab::DkdvLayout<64>::kAlloc;
-  cudaError_t err = (D == 128) ? cudaLaunchKernelEx(&cfg, fab::fa_bwd_dkdv_kernel<128>, p)
-                               : cudaLaunchKernelEx(&cfg, fab::fa_bwd_dkdv_kernel<64>, p);
-  if (err != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, dkdv_kernel(D, f16), p) != cudaSuccess) return FA_ERR_CUDA;
   p.n_units = static_cast<int>(bh * p.nq);
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.dynamicSmemBytes = (D == 128) ? fab::DqLayout<128>::kAlloc : fab::DqLayout<64>::kAlloc;
-  err = (D == 128) ? cudaLaunchKernelEx(&cfg, fab::fa_bwd_dq_kernel<128>, p)
-                   : cudaLaunchKernelEx(&cfg, fab::fa_bwd_dq_kernel<64>, p);
-  if (err != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, dq_kernel(D, f16), p) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 }  // namespace
@@ -1163,7 +1288,7 @@ extern "C" fa_status fa_bwd(const void* Q, const void* K, const void* V, const v
                             int D, int causal, float scale, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, nullptr, B, H, Lq, Lk, D, -1, causal ? 0 : -1, scale,
-                  workspace, workspace_bytes, stream);
+                  false, contiguous_bwd(H, Lq, Lk, D), workspace, workspace_bytes, stream);
 }
 
 extern "C" fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
@@ -1174,5 +1299,36 @@ extern "C" fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, 
   if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, kv_len, B, H, Lq, Lk, D, window_left, window_right,
-                  scale, workspace, workspace_bytes, stream);
+                  scale, false, contiguous_bwd(H, Lq, Lk, D), workspace, workspace_bytes, stream);
+}
+
+extern "C" fa_status fa_bwd_strided(const void* Q, const long long* q_stride, const void* K,
+                                    const long long* k_stride, const void* V, const long long* v_stride,
+                                    const void* O, const long long* o_stride, const void* dO,
+                                    const long long* do_stride, const float* LSE, void* dQ,
+                                    const long long* dq_stride, void* dK, const long long* dk_stride,
+                                    void* dV, const long long* dv_stride, const int* kv_len, int B,
+                                    int H, int Lq, int Lk, int D, int window_left, int window_right,
+                                    float scale, int dtype, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const long long* arrays[8] = {q_stride, k_stride, v_stride, o_stride, do_stride, dq_stride, dk_stride,
+                                dv_stride};
+  for (const long long* a : arrays)
+    if (!a) return FA_ERR_INVALID_ARG;
+  BwdStrides sd;
+  for (int i = 0; i < 3; ++i) {
+    sd.q[i] = q_stride[i];
+    sd.k[i] = k_stride[i];
+    sd.v[i] = v_stride[i];
+    sd.o[i] = o_stride[i];
+    sd.dO[i] = do_stride[i];
+    sd.dq[i] = dq_stride[i];
+    sd.dk[i] = dk_stride[i];
+    sd.dv[i] = dv_stride[i];
+  }
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, kv_len, B, H, Lq, Lk, D, window_left, window_right,
+                  scale, dtype == FA_DTYPE_FP16, sd, workspace, workspace_bytes, stream);
 }

@@ -1489,41 +1489,9 @@ extern "C" fa_status fa_fwd_window(const void* Q, const void* K, const void* V, 
 }
 
 // ---------------------------------------------------------------- strided / fp16 entry point
-namespace {
-
-// Byte span [lo, lo + bytes) that a [B,H,L,D] tensor with element strides st touches.
-size_t span_bytes(long long B, long long H, long long L, int D, const long long* st) {
-  const long long last = (B - 1) * st[0] + (H - 1) * st[1] + (L - 1) * st[2] + D;
-  return static_cast<size_t>(last) * 2;
-}
-
-// Strides of one tensor: non-negative multiples of 8 elements (16 bytes, the tensor-memory-
-// access unit's rule) for every dimension of size > 1, and byte offsets below 2^40.
-bool strides_ok(long long B, long long H, long long L, int D, const long long* st) {
-  const long long size[3] = {B, H, L};
-  for (int i = 0; i < 3; ++i) {
-    if (size[i] <= 1) continue;
-    if (st[i] < 0 || (st[i] & 7) || st[i] >= (1ll << 39)) return false;
-  }
-  return span_bytes(B, H, L, D, st) < (1ull << 40);
-}
-
-// No two elements of the tensor share an address: with the dimensions of size > 1 ordered
-// by stride (features innermost, stride 1, extent D), each stride covers the extent of the
-// dimension inside it.
-bool no_self_overlap(long long B, long long H, long long L, int D, const long long* st) {
-  std::pair<long long, long long> dims[4] = {{1, D}};   // (stride, extent)
-  int n = 1;
-  const long long size[3] = {B, H, L};
-  for (int i = 0; i < 3; ++i)
-    if (size[i] > 1) dims[n++] = {st[i], size[i]};
-  std::sort(dims, dims + n);
-  for (int i = 1; i < n; ++i)
-    if (dims[i].first < dims[i - 1].first * dims[i - 1].second) return false;
-  return true;
-}
-
-}  // namespace
+using fa_layout::no_self_overlap;
+using fa_layout::span_bytes;
+using fa_layout::strides_ok;
 
 extern "C" fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K,
                                     const long long* k_stride, const void* V,

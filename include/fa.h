@@ -272,6 +272,25 @@ fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void*
                         int H, int Lq, int Lk, int D, int window_left, int window_right,
                         float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * fa_bwd_strided -- fa_bwd_masked on strided tensors, in bf16 or fp16: the backward
+ * counterpart of fa_fwd_strided.  Each of Q, K, V, O, dO, dQ, dK, dV comes with three
+ * element strides {batch, head, row} (features contiguous), under the rules of
+ * fa_fwd_strided: 16-byte strides, no two elements of an output at one address, and
+ * the outputs and the workspace meeting neither an input nor each other (inputs may
+ * share memory).  dtype (FA_DTYPE_BF16 or FA_DTYPE_FP16) is the type of all eight
+ * tensors; LSE stays fp32 [B,H,Lq] contiguous.  Results equal fa_bwd_masked's on the
+ * same values laid out contiguously (bf16).
+ */
+fa_status fa_bwd_strided(const void* Q, const long long* q_stride, const void* K,
+                         const long long* k_stride, const void* V, const long long* v_stride,
+                         const void* O, const long long* o_stride, const void* dO,
+                         const long long* do_stride, const float* LSE, void* dQ,
+                         const long long* dq_stride, void* dK, const long long* dk_stride, void* dV,
+                         const long long* dv_stride, const int* kv_len, int B, int H, int Lq,
+                         int Lk, int D, int window_left, int window_right, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(fa_status s);
 

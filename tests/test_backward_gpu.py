@@ -271,3 +271,62 @@ def test_autograd_with_window_and_padding(oracle_mod):
                                                   40, 0, kvb, 0.125)
             for g_, r in zip((qg.grad, kg.grad, vg.grad), ref):
                 assert np.abs(g_[b, h].float().cpu().numpy() - r).max() < 5e-2
+
+
+# ---------------------------------------------------------------- strided layouts and fp16
+def _packed(B, H, L, D, dtype, seed):
+    q, k, v = make_qkv(B, H, L, L, D, seed)
+    dev = torch.device("cuda:0")
+    packed = torch.empty((B, L, 3, H, D), dtype=dtype, device=dev)
+    for i, t in enumerate((q, k, v)):
+        packed[:, :, i] = t.to(dtype).to(dev).transpose(1, 2)
+    return tuple(packed[:, :, i].transpose(1, 2) for i in range(3)), (q, k, v)
+
+
+@pytest.mark.parametrize("causal,D", [(True, 128), (False, 64)])
+def test_backward_strided_equals_contiguous(causal, D):
+    """Q, K, V from a packed [B, L, 3, H, D] projection, gradients written into a
+    [B, L, H, D] buffer: the bits of the contiguous call."""
+    dev = torch.device("cuda:0")
+    (qv, kv, vv), (q, k, v) = _packed(2, 3, 400, D, torch.bfloat16, seed=81 + D)
+    qc, kc, vc = (t.to(dev) for t in (q, k, v))
+    do = make_do(2, 3, 400, D, seed=81).to(dev)
+    o, lse = fa.attention(qc, kc, vc, causal=causal, split=False)
+    ref = fa.attention_backward(qc, kc, vc, o, lse, do, causal=causal)
+    bufs = [torch.full((2, 400, 3, D), 9.0, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    outs = [b.transpose(1, 2) for b in bufs]
+    got = fa.attention_backward(qv, kv, vv, o, lse, do, causal=causal, dq=outs[0], dk=outs[1], dv=outs[2])
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for g_, r in zip(got, ref):
+        assert torch.equal(g_, r)
+
+
+@pytest.mark.parametrize("causal,D,window", [(True, 128, None), (False, 64, None), (False, 128, (100, 20))])
+def test_backward_fp16_against_oracle(oracle_mod, causal, D, window):
+    dev = torch.device("cuda:0")
+    q, k, v = make_qkv(1, 2, 300, 300, D, seed=91 + D)
+    do = make_do(1, 2, 300, D, seed=91)
+    q16, k16, v16, do16 = (t.to(torch.float16).to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention(q16, k16, v16, causal=causal, window=window)
+    dq, dk, dv = fa.attention_backward(q16, k16, v16, o, lse, do16, causal=causal, window=window)
+    assert dq.dtype == torch.float16 and fa.fa_last_device_status() == fa.FA_OK
+    left, right = window if window is not None else (-1, 0 if causal else -1)
+    for h in range(2):
+        ref = oracle_mod.attn_bwd_head_masked(q[0, h].double().numpy(), k[0, h].double().numpy(),
+                                              v[0, h].double().numpy(), do[0, h].double().numpy(),
+                                              left, right, 300, 1.0 / math.sqrt(D))
+        for g_, r in zip((dq, dk, dv), ref):
+            err = np.abs(g_[0, h].float().cpu().numpy() - r).max()
+            assert err <= 2e-2 * max(1.0, np.abs(r).max()), err
+
+
+def test_fp16_autograd_through_packed_views():
+    dev = torch.device("cuda:0")
+    (qv, kv, vv), _ = _packed(1, 2, 256, 64, torch.float16, seed=97)
+    leaf = qv._base if qv._base is not None else qv
+    leaf.requires_grad_(True)
+    q, k, v = (leaf[:, :, i].transpose(1, 2) for i in range(3))
+    o = fa.flash_attention(q, k, v, causal=True)
+    o.float().sum().backward()
+    assert leaf.grad is not None and torch.isfinite(leaf.grad.float()).all()
+    assert leaf.grad.abs().sum() > 0
