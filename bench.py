@@ -470,12 +470,15 @@ def time_oracle_bwd(w, q, k, v, budget_s: float):
     L = min(w.Lq, w.Lk, 1024)
     qq, kk, vv = (np.ascontiguousarray(t[0, 0, :L].float().numpy(), dtype=np.float64) for t in (q, k, v))
     g = np.random.default_rng(0).standard_normal(qq.shape)
-    pairs = L * (L + 1) // 2 if w.causal else L * L
-    flops = 2.5 * 4 * w.D * pairs
+    left, right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
+    i = np.arange(L)
+    lo = np.zeros_like(i) if left < 0 else np.maximum(0, i - left)
+    hi = np.full_like(i, L - 1) if right < 0 else np.minimum(L - 1, i + right)
+    flops = 2.5 * 4 * w.D * int((hi - lo + 1).sum())
     spent, calls = 0.0, 0
     while spent < budget_s or calls == 0:
         t0 = time.perf_counter()
-        oracle.attn_bwd_head(qq, kk, vv, g, w.causal, w.scale)
+        oracle.attn_bwd_head_masked(qq, kk, vv, g, left, right, L, w.scale)
         spent += time.perf_counter() - t0
         calls += 1
     return flops * calls, spent, calls, oracle.max_threads(), L
@@ -494,26 +497,46 @@ def run_backward(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    if w.window is not None:
-        raise SystemExit("the backward pass covers the full and causal masks")
-    q_h, k_h, v_h = make_workload_inputs(w)
+    io_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    variant = args.dtype != "bf16" or args.layout != "bhld" or args.kv_pad > 0 or w.window is not None
+    q_h, k_h, v_h = (t.to(io_dtype) for t in make_workload_inputs(w))
     g = torch.Generator().manual_seed(w.seed + 99)
-    do_h = torch.randn(q_h.shape, generator=g).to(torch.bfloat16)
+    do_h = torch.randn(q_h.shape, generator=g).to(io_dtype)
+    kv_len_h = None
+    if args.kv_pad > 0:
+        rng = np.random.default_rng(0xCAFE + w.index)
+        lo_k = max(1, int(round(w.Lk * (1.0 - 2.0 * args.kv_pad))))
+        kv_len_h = rng.integers(lo_k, w.Lk + 1, size=w.B).astype(np.int32)
+    kv_len = torch.from_numpy(kv_len_h).to(dev) if kv_len_h is not None else None
+    left, right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
+
+    def place(t):   # [B, H, L, D] values, stored [B, L, H, D] with --layout bshd
+        t = t.to(dev)
+        return t.transpose(1, 2).contiguous().transpose(1, 2) if args.layout == "bshd" else t
+
     per_copy = 2 * (3 * q_h.numel() + 4 * k_h.numel()) + 8 * w.B * w.H * w.Lq
     n_copies = max(2, math.ceil(2 * L2_BYTES / per_copy) + 1)
     bufs = []
     for c in range(n_copies):
-        q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
-        o, lse = fa.attention(q, k, v, causal=w.causal, scale=w.scale)
-        bufs.append((q, k, v, o, do, lse, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)))
+        q, k, v, do = (place(t) for t in (q_h, k_h, v_h, do_h))
+        o, lse = fa.attention(q, k, v, causal=w.causal, scale=w.scale, window=w.window, kv_len=kv_len)
+        grads = tuple(place(torch.empty(t.shape, dtype=io_dtype)) for t in (q_h, k_h, v_h))
+        bufs.append((q, k, v, o, do, lse, *grads))
     st, ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize(dev)
+    code = fa.FA_DTYPE_FP16 if args.dtype == "fp16" else fa.FA_DTYPE_BF16
 
     def launch(i):
         q, k, v, o, do, lse, dq, dk, dv = bufs[i % n_copies]
-        st = fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.B, w.H, w.Lq, w.Lk, w.D, w.causal,
-                       w.scale, ws, ws_bytes, stream)
+        if variant:
+            st = fa.fa_bwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], o,
+                                   o.stride()[:3], do, do.stride()[:3], lse, dq, dq.stride()[:3], dk,
+                                   dk.stride()[:3], dv, dv.stride()[:3], kv_len, w.B, w.H, w.Lq, w.Lk,
+                                   w.D, left, right, w.scale, code, ws, ws_bytes, stream)
+        else:
+            st = fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.B, w.H, w.Lq, w.Lk, w.D, w.causal,
+                           w.scale, ws, ws_bytes, stream)
         if st != fa.FA_OK:
             raise RuntimeError(fa.fa_status_string(st))
 
@@ -539,7 +562,14 @@ def run_backward(args, w):
     if fa.fa_last_device_status(stream) != fa.FA_OK:
         raise RuntimeError("timed region reported a device error")
     max_ms = reduce_max(dist, ev[0].elapsed_time(ev[1]), dev)
-    flops = 2.5 * w.flops()   # five GEMMs of the forward's size (dV, dP, dS K, dS^T Q, and S)
+    pairs_flops = w.flops()
+    if kv_len_h is not None:   # only the unpadded pairs count
+        i = np.arange(w.Lq, dtype=np.int64)
+        lo = np.zeros_like(i) if left < 0 else np.maximum(0, i - left)
+        hi_band = np.full_like(i, w.Lk - 1) if right < 0 else np.minimum(w.Lk - 1, i + right)
+        pairs = sum(int(np.maximum(0, np.minimum(hi_band, kl - 1) - lo + 1).sum()) for kl in kv_len_h)
+        pairs_flops = 4 * w.D * w.H * pairs
+    flops = 2.5 * pairs_flops   # five GEMMs of the forward's size (dV, dP, dS K, dS^T Q, and S)
     value = aggregate_tflops(world, flops, args.steps, max_ms)
     per_gpu = flops / (max_ms / args.steps / 1e3) / 1e12
     peaks, peak_src = load_peaks()
@@ -554,9 +584,11 @@ def run_backward(args, w):
         line = {
             "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic",
             "config": {"workload": w.name, "shape": w.describe(), "pass": "backward",
+                       "io_dtype": args.dtype, "layout": args.layout,
+                       "kv_len": None if kv_len_h is None else [int(x) for x in kv_len_h],
                        "flops_per_step": flops, "flop_count": "2.5x forward (five GEMMs); the "
                        "kernels execute seven (dQ is computed apart from dK, dV)",
                        "l2": f"inputs rotate over {n_copies} copies (> 2x L2)",
