@@ -164,6 +164,8 @@ struct BwdParams {
   int nq;              // query tiles: ceil(Lq / 128)
   int nk;              // key tiles:   ceil(Lk / 128)
   int n_units;
+  int group_heads;     // causal-like orders: heads per group (a group's streamed tiles stay in L2)
+  int* unit_ctr;       // units drawn after each CTA's first, zeroed by the Delta kernel
   float scale;
   float scale_log2;    // scale * log2(e)
   uint32_t flags;      // test hooks (fa_debug_set): bit 0 withholds the first V tile of dK/dV
@@ -208,29 +210,72 @@ __device__ __forceinline__ void dq_range(const BwdParams& p, int qt, int kvl, in
   *n = static_cast<int>((lim - 1) / kBlk) - *ka + 1;
 }
 
-// Unit r of this CTA (boustrophedon over the grid), heaviest first.
-__device__ __forceinline__ bool unit_index(const BwdParams& p, int r, int& idx) {
-  const int G = static_cast<int>(gridDim.x), g = static_cast<int>(blockIdx.x);
-  idx = r * G + ((r & 1) ? (G - 1 - g) : g);
-  return idx < p.n_units;
+// Unit order.  Causal-like masks (the first key tiles are seen by the most queries, the
+// last query tiles see the most keys) go heaviest first within groups of group_heads
+// heads, one group after another: the units in flight then share a group's streamed
+// tiles in L2 instead of every head's at once.  Other masks go head by head.  Units are
+// handed out dynamically (below), so the heavy-first order also balances the CTAs.
+__device__ __forceinline__ void grouped_unit(const BwdParams& p, int idx, int n_tiles, int& bh, int& t) {
+  const int per_group = p.group_heads * n_tiles;
+  const int grp = idx / per_group;
+  const int i = idx - grp * per_group;
+  const int h0 = grp * p.group_heads;
+  const int hc = min(p.group_heads, p.bh_count - h0);   // the last group may be smaller
+  t = i / hc;
+  bh = h0 + (i - t * hc);
 }
 __device__ __forceinline__ void dkdv_unit(const BwdParams& p, int idx, int& bh, int& kt) {
-  if (p.win_left < 0 && p.win_right >= 0) {   // causal-like: the first key tiles are seen by the most queries
-    kt = idx / p.bh_count;
-    bh = idx % p.bh_count;
-  } else {          // a head's tiles run together and share its query tiles in L2
+  if (p.win_left < 0 && p.win_right >= 0) {
+    grouped_unit(p, idx, p.nk, bh, kt);
+  } else {
     bh = idx / p.nk;
     kt = idx % p.nk;
   }
 }
 __device__ __forceinline__ void dq_unit(const BwdParams& p, int idx, int& bh, int& qt) {
-  if (p.win_left < 0 && p.win_right >= 0) {   // causal-like: the last query tiles see the most keys
-    qt = p.nq - 1 - idx / p.bh_count;
-    bh = idx % p.bh_count;
+  if (p.win_left < 0 && p.win_right >= 0) {
+    int i;
+    grouped_unit(p, idx, p.nq, bh, i);
+    qt = p.nq - 1 - i;
   } else {
     bh = idx / p.nq;
     qt = idx % p.nq;
   }
+}
+
+// Dynamic unit hand-out.  Each CTA's first unit is its block index; the load warp draws
+// every later one from a global counter and passes it to the MMA warp and the compute
+// warps through a ring of shared-memory slots (full: count 1, the load warp; empty:
+// count 9, the eight compute warps and the MMA warp).  A drawn index >= n_units ends
+// every role's loop.  Both functions are warp-uniform.
+constexpr int kUnitRing = 4;
+constexpr int kUnitConsumers = 9;
+constexpr int kCtrStride = 32;   // the two counters sit 128 bytes apart in the workspace's last 256
+
+__device__ __forceinline__ bool unit_produce(const BwdParams& p, uint32_t full0, uint32_t empty0,
+                                             volatile int* slots, int r, int& idx, volatile int* abort_flag,
+                                             unsigned long long limit, uint32_t site) {
+  const int s = r % kUnitRing;
+  if (!wait_warp(empty0 + 8u * s, ((r / kUnitRing) & 1) ^ 1u, abort_flag, limit, site)) return false;
+  int v = 0;
+  if ((threadIdx.x & 31) == 0) {
+    v = r == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.unit_ctr, 1);
+    slots[s] = v;
+    ptx::mbar_arrive(full0 + 8u * s);   // release: the slot's value is visible to the waiters
+  }
+  idx = __shfl_sync(0xffffffffu, v, 0);
+  return true;
+}
+
+__device__ __forceinline__ bool unit_consume(uint32_t full0, uint32_t empty0, const volatile int* slots, int r,
+                                             int& idx, volatile int* abort_flag, unsigned long long limit,
+                                             uint32_t site) {
+  const int s = r % kUnitRing;
+  if (!wait_warp(full0 + 8u * s, (r / kUnitRing) & 1, abort_flag, limit, site)) return false;
+  idx = slots[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(empty0 + 8u * s);
+  return true;
 }
 
 // ------------------------------------------------------------------ Delta = rowsum(dO * O)
@@ -247,6 +292,7 @@ struct DeltaArgs {
   float* lse2;
   long long o_s[3], do_s[3];
   long long rows_pad;
+  int* unit_ctr;   // the dK/dV and dQ kernels' unit counters, zeroed here
   int Lq, Lpad, H;
 };
 
@@ -259,6 +305,10 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __grid_constant
   const int bh = static_cast<int>(row / a.Lpad);
   const int q = static_cast<int>(row - static_cast<long long>(bh) * a.Lpad);
   const bool valid = row < a.rows_pad && q < a.Lq;
+  if (tid == 0) {
+    a.unit_ctr[0] = 0;
+    a.unit_ctr[kCtrStride] = 0;
+  }
   float acc = 0.0f;
   if (valid) {
     const uint4 x4 = __ldg(reinterpret_cast<const uint4*>(a.O + row_offset(a.o_s, a.H, bh, q)) + part);
@@ -299,10 +349,13 @@ struct DkdvLayout {
   static constexpr int kBarAccFull = kBarDsFull + 1;
   static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 256 (compute threads)
   static constexpr int kBarDrain = kBarAccEmpty + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarUnitFull = kBarDrain + 1;                // [kUnitRing]
+  static constexpr int kBarUnitEmpty = kBarUnitFull + kUnitRing;    // [kUnitRing]
+  static constexpr int kNumBars = kBarUnitEmpty + kUnitRing;
   static constexpr int kOffAbort = kOffBar + kNumBars * 8;
   static constexpr int kOffTmemSlot = kOffAbort + 4;
-  static constexpr int kBytes = kOffTmemSlot + 4;
+  static constexpr int kOffUnits = kOffTmemSlot + 4;                // int[kUnitRing]
+  static constexpr int kBytes = kOffUnits + 4 * kUnitRing;
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns: S^T | dP^T | dV | dK (P^T and dS^T as bf16 over the first 64 columns of S^T / dP^T)
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 256 + HD;
@@ -321,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   const uint32_t sbase = ptx::smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  volatile int* unit_slots = reinterpret_cast<volatile int*>(smem + L::kOffUnits);
   auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
   auto stage_off = [&](int s) -> uint32_t { return L::kOffStage + s * L::kStageBytes; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -339,6 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     ptx::mbar_init(bar(L::kBarAccFull), 1);
     ptx::mbar_init(bar(L::kBarAccEmpty), kComputeThreads);
     ptx::mbar_init(bar(L::kBarDrain), 1);
+    for (int s = 0; s < kUnitRing; ++s) {
+      ptx::mbar_init(bar(L::kBarUnitFull + s), 1);
+      ptx::mbar_init(bar(L::kBarUnitEmpty + s), kUnitConsumers);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -365,7 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     uint32_t acc_count = 0;   // units whose accumulators were read
     bool ok = true;
     int idx;
-    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      ok = unit_consume(bar(L::kBarUnitFull), bar(L::kBarUnitEmpty), unit_slots, r, idx, abort_flag,
+                        limit, kSiteCompute);
+      if (!ok || idx >= p.n_units) break;
       int bh, kt;
       dkdv_unit(p, idx, bh, kt);
       const int kvl = batch_keys(p, bh);
@@ -484,7 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     for (int s = 0; s < L::kStages; ++s) last_fill[s] = -1;
     bool ok = true;
     int idx;
-    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      ok = unit_produce(p, bar(L::kBarUnitFull), bar(L::kBarUnitEmpty), unit_slots, r, idx, abort_flag,
+                        limit, kSiteLoad);
+      if (!ok || idx >= p.n_units) break;
       int bh, kt;
       dkdv_unit(p, idx, bh, kt);
       int q_first, n;
@@ -555,7 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     uint32_t it = 0, units = 0, acc_units = 0;
     bool ok = true;
     int idx;
-    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      ok = unit_consume(bar(L::kBarUnitFull), bar(L::kBarUnitEmpty), unit_slots, r, idx, abort_flag,
+                        limit, kSiteMma);
+      if (!ok || idx >= p.n_units) break;
       int bh, kt;
       dkdv_unit(p, idx, bh, kt);
       int qa_unused, n;
@@ -649,10 +716,13 @@ struct DqLayout {
   static constexpr int kBarAccFull = kBarDsFull + 1;
   static constexpr int kBarAccEmpty = kBarAccFull + 1;          // count 256 (compute threads)
   static constexpr int kBarDrain = kBarAccEmpty + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarUnitFull = kBarDrain + 1;                // [kUnitRing]
+  static constexpr int kBarUnitEmpty = kBarUnitFull + kUnitRing;    // [kUnitRing]
+  static constexpr int kNumBars = kBarUnitEmpty + kUnitRing;
   static constexpr int kOffAbort = kOffBar + kNumBars * 8;
   static constexpr int kOffTmemSlot = kOffAbort + 4;
-  static constexpr int kBytes = kOffTmemSlot + 4;
+  static constexpr int kOffUnits = kOffTmemSlot + 4;                // int[kUnitRing]
+  static constexpr int kBytes = kOffUnits + 4 * kUnitRing;
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns: S | dP | dQ (dS as bf16 over the first 64 columns of dP)
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDq = 256;
@@ -671,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   const uint32_t sbase = ptx::smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  volatile int* unit_slots = reinterpret_cast<volatile int*>(smem + L::kOffUnits);
   auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
   auto k_off = [&](int s) -> uint32_t { return L::kOffK + s * T::kTileBytes; };
   auto v_off = [&](int s) -> uint32_t { return L::kOffV + s * T::kTileBytes; };
@@ -694,6 +765,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     ptx::mbar_init(bar(L::kBarAccFull), 1);
     ptx::mbar_init(bar(L::kBarAccEmpty), kComputeThreads);
     ptx::mbar_init(bar(L::kBarDrain), 1);
+    for (int s = 0; s < kUnitRing; ++s) {
+      ptx::mbar_init(bar(L::kBarUnitFull + s), 1);
+      ptx::mbar_init(bar(L::kBarUnitEmpty + s), kUnitConsumers);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -719,7 +794,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     uint32_t it = 0, acc_count = 0;
     bool ok = true;
     int idx;
-    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      ok = unit_consume(bar(L::kBarUnitFull), bar(L::kBarUnitEmpty), unit_slots, r, idx, abort_flag,
+                        limit, kSiteCompute);
+      if (!ok || idx >= p.n_units) break;
       int bh, qt;
       dq_unit(p, idx, bh, qt);
       const int kvl = batch_keys(p, bh);
@@ -827,7 +905,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     for (int s = 0; s < L::kVStages; ++s) last_v[s] = -1;
     bool ok = true;
     int idx;
-    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      ok = unit_produce(p, bar(L::kBarUnitFull), bar(L::kBarUnitEmpty), unit_slots, r, idx, abort_flag,
+                        limit, kSiteLoad);
+      if (!ok || idx >= p.n_units) break;
       int bh, qt;
       dq_unit(p, idx, bh, qt);
       int ka, n;
@@ -897,7 +978,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     uint32_t it = 0, units = 0, acc_units = 0;
     bool ok = true;
     int idx;
-    for (int r = 0; ok && unit_index(p, r, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      ok = unit_consume(bar(L::kBarUnitFull), bar(L::kBarUnitEmpty), unit_slots, r, idx, abort_flag,
+                        limit, kSiteMma);
+      if (!ok || idx >= p.n_units) break;
       int bh, qt;
       dq_unit(p, idx, bh, qt);
       int ka_unused, n;
@@ -1036,6 +1120,14 @@ bool bwd_overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 size_t bwd_round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+constexpr size_t kBwdCounterBytes = 256;   // the kernels' two unit counters
+
+// Heads per unit group: as many as keep a group's streamed tensors (bytes_per_head each)
+// within 32 MiB of L2, at least one.
+int bwd_group_heads(long long bytes_per_head, long long bh) {
+  const long long g = (32ll << 20) / std::max(1ll, bytes_per_head);
+  return static_cast<int>(std::max(1ll, std::min(g, bh)));
+}
 
 fa_status bwd_prepare(int D, bool f16, int* sm_count) {
   int dev = -1;
@@ -1129,7 +1221,7 @@ extern "C" fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, 
   const fa_status st = bwd_check_sizes(B, H, Lq, Lk, D, &rows, &bh);
   if (st != FA_OK) return st;
   const size_t rows_pad = static_cast<size_t>(bh) * ((Lq + 127) / 128) * 128;
-  *bytes = 2 * bwd_round256(rows_pad * sizeof(float));
+  *bytes = 2 * bwd_round256(rows_pad * sizeof(float)) + kBwdCounterBytes;
   return FA_OK;
 }
 
@@ -1190,7 +1282,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   const long long nq_ll = (Lq + 127) / 128;
   const size_t rows_pad = static_cast<size_t>(bh) * nq_ll * 128;
   const size_t half_ws = bwd_round256(rows_pad * sizeof(float));
-  const size_t need_ws = 2 * half_ws;
+  const size_t need_ws = 2 * half_ws + kBwdCounterBytes;
   if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return FA_ERR_INVALID_ARG;
   // Inputs may share memory (they are only read); outputs and the workspace meet nothing.
@@ -1216,6 +1308,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
     return FA_ERR_CUDA;
   float* delta = static_cast<float*>(workspace);
   float* lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + half_ws);
+  int* unit_ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 2 * half_ws);
   p.delta = delta;
   p.lse2 = lse2;
   p.dq = static_cast<uint16_t*>(dQ);
@@ -1257,6 +1350,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
       da.do_s[i] = sd.dO[i];
     }
     da.rows_pad = static_cast<long long>(rows_pad);
+    da.unit_ctr = unit_ctr;
     da.Lq = Lq;
     da.Lpad = static_cast<int>(nq_ll * 128);
     da.H = H;
@@ -1272,10 +1366,14 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   cfg.blockDim = dim3(fab::kThreads);
   cfg.stream = stream;
   p.n_units = static_cast<int>(bh * p.nk);
+  p.unit_ctr = unit_ctr;
+  p.group_heads = bwd_group_heads(4ll * Lq * D, bh);   // dK/dV streams Q and dO
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.dynamicSmemBytes = (D == 128) ? fab::DkdvLayout<128>::kAlloc : fab::DkdvLayout<64>::kAlloc;
   if (cudaLaunchKernelEx(&cfg, dkdv_kernel(D, f16), p) != cudaSuccess) return FA_ERR_CUDA;
   p.n_units = static_cast<int>(bh * p.nq);
+  p.unit_ctr = unit_ctr + fab::kCtrStride;
+  p.group_heads = bwd_group_heads(4ll * Lk * D, bh);   // dQ streams K and V
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.dynamicSmemBytes = (D == 128) ? fab::DqLayout<128>::kAlloc : fab::DqLayout<64>::kAlloc;
   if (cudaLaunchKernelEx(&cfg, dq_kernel(D, f16), p) != cudaSuccess) return FA_ERR_CUDA;

@@ -220,7 +220,8 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, f
 /*
  * fa_bwd_workspace_size -- device workspace fa_bwd needs, in *bytes: two fp32 arrays
  * (Delta_i = dO_i.O_i and LSE_i * log2(e)) over the query rows padded to whole
- * 128-row tiles, B*H*ceil(Lq/128)*128 entries each, each rounded up to 256 bytes.  Argument errors as fa_bwd's
+ * 128-row tiles, B*H*ceil(Lq/128)*128 entries each, each rounded up to 256 bytes, then
+ * 256 bytes for the two kernels' work counters.  Argument errors as fa_bwd's
  * size checks (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED; bytes == NULL is invalid).
  */
 fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal, size_t* bytes);
@@ -244,7 +245,8 @@ fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
  *   LSE      : const fp32 [B,H,Lq] as written by fa_fwd for the same arguments;
  *   dQ       : bf16 [B,H,Lq,D], written;  dK, dV : bf16 [B,H,Lk,D], written;
  *   workspace: device memory of at least fa_bwd_workspace_size bytes, 256-byte
- *              aligned, contents ignored and left as scratch (Delta and LSE*log2e);
+ *              aligned, contents ignored and left as scratch (Delta, LSE*log2e and
+ *              the counters from which the dK/dV and dQ kernels draw their work units);
  *   B, H, Lq, Lk, D, causal, scale, stream: as fa_fwd.
  * All pointers are device pointers, 16-byte aligned; dQ, dK, dV and the workspace
  * must not overlap each other or any input.  Three kernels are queued on `stream`

@@ -173,14 +173,16 @@ def test_bwd_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(dQ=7 * A + 8) == fa.FA_ERR_INVALID_ARG          # misaligned
     assert call(ws=0) == fa.FA_ERR_INVALID_ARG                  # workspace missing
     assert call(wsb=16) == fa.FA_ERR_INVALID_ARG                # workspace too small
+    assert call(wsb=2 * 128 * 4) == fa.FA_ERR_INVALID_ARG       # no room for the work counters
     assert call(ws=10 * A + 16) == fa.FA_ERR_INVALID_ARG        # workspace not 256-byte aligned
     assert call(dK=A) == fa.FA_ERR_INVALID_ARG                  # dK overlaps Q
     assert call(dV=8 * A) == fa.FA_ERR_INVALID_ARG              # dV overlaps dK
     assert call(ws=5 * A) == fa.FA_ERR_INVALID_ARG              # workspace overlaps dO
     assert call(B=0, Lk=0) == fa.FA_OK                           # nothing to do
     st, n = fa.fa_bwd_workspace_size(2, 3, 100, 50, 128, 1)
-    # Delta and LSE * log2(e), each over whole 128-row tiles (2*3 heads x 1 tile x 128 rows)
-    assert st == fa.FA_OK and n == 2 * (2 * 3 * 128 * 4)
+    # Delta and LSE * log2(e), each over whole 128-row tiles (2*3 heads x 1 tile x 128 rows),
+    # then 256 bytes of work counters
+    assert st == fa.FA_OK and n == 2 * (2 * 3 * 128 * 4) + 256
     assert fa.fa_bwd_workspace_size(1, 1, 16, 16, 96, 0)[0] == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_bwd_workspace_size(1, 1, 16, 16, 64, 0, None) == fa.FA_ERR_INVALID_ARG
 

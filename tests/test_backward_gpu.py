@@ -112,6 +112,29 @@ def test_backward_workload_sampled_heads(oracle_mod, name):
     check(oracle_mod, q, k, v, do, w.causal, w.scale, heads=heads)
 
 
+@pytest.mark.parametrize("H,L", [(20, 4096), (10, 8192)])
+def test_backward_grouped_units_cover_every_head(H, L):
+    """Causal problems hand their units out by groups of heads sized to L2 (Q and dO, or K
+    and V, of 16 heads at L = 4096, D = 128; of 8 heads at L = 8192), so H = 20 and H = 10 end
+    on a partial group.  Every head, written into NaN-filled gradients, must equal the same
+    head computed as a one-head problem."""
+    dev = torch.device("cuda:0")
+    D = 128
+    q, k, v = (t.to(dev) for t in make_qkv(1, H, L, L, D, seed=91 + H))
+    do = make_do(1, H, L, D, seed=91 + H).to(dev)
+    o, lse = fa.attention(q, k, v, causal=True)
+    grads = [torch.full_like(t, float("nan")) for t in (q, k, v)]
+    fa.attention_backward(q, k, v, o, lse, do, causal=True, dq=grads[0], dk=grads[1], dv=grads[2])
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for g in grads:
+        assert torch.isfinite(g).all()
+    for h in sorted({0, H // 2, H - 2, H - 1}):
+        sl = lambda t: t[:, h:h + 1].contiguous()
+        one = fa.attention_backward(sl(q), sl(k), sl(v), sl(o), sl(lse), sl(do), causal=True)
+        for a, b in zip(grads, one):
+            assert torch.equal(a[:, h:h + 1], b), h
+
+
 def test_backward_unattended_keys_are_zero():
     """Causal with Lq < Lk: keys j >= Lq are seen by no query; their gradients are 0."""
     dev = torch.device("cuda:0")
