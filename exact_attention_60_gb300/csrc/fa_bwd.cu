@@ -453,9 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
                                          wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t sr[2][32];
-        ptx::tmem_ld32x32b_x32(t_s, sr[0]);
-        ptx::tmem_ld32x32b_x32(t_s + 32, sr[1]);
+        uint32_t sr[64];
+        ptx::tmem_ld32x32b_x64(t_s, sr);   // one load, one wait for the warpgroup's 64 columns
         // P^T_kq = exp2(sl2 * S - lse_q * log2e); padded queries carry lse2 = +inf (P = 0).
         // Key k is seen by query q iff k - right <= q <= k + left and k < kvl; only tiles the
         // band or the padding cuts are masked (a query without keys, LSE = -inf, is always in
@@ -469,16 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         const int c_hi = (p.win_left < 0 ? INT_MAX / 2 : k + p.win_left) - base;
         const bool key_ok = k < kvl;
         float pr[64];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {   // LSE * log2e of four queries per shared-memory load
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+          pr[c] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l4.x));
+          pr[c + 1] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -l4.y));
+          pr[c + 2] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + 2]), sl2, -l4.z));
+          pr[c + 3] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + 3]), sl2, -l4.w));
+        }
         if (cut) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
-            pr[c] = (key_ok && c >= c_lo && c <= c_hi) ? x : 0.0f;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            pr[c] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
+          for (int c = 0; c < 64; ++c) pr[c] = (key_ok && c >= c_lo && c <= c_hi) ? pr[c] : 0.0f;
         }
         uint32_t pk[32];
 #pragma unroll
@@ -492,13 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
-        ptx::tmem_ld32x32b_x32(t_dp, sr[0]);
-        ptx::tmem_ld32x32b_x32(t_dp + 32, sr[1]);
+        ptx::tmem_ld32x32b_x64(t_dp, sr);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float a = pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt[2 * c]);
-          const float b = pr[2 * c + 1] * (__uint_as_float(sr[c >> 4][(2 * c + 1) & 31]) - dlt[2 * c + 1]);
-          pk[c] = pack2<kF16>(a, b);
+        for (int c = 0; c < 32; c += 2) {   // Delta of four queries per shared-memory load
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt + 2 * c);
+          pk[c] = pack2<kF16>(pr[2 * c] * (__uint_as_float(sr[2 * c]) - d4.x),
+                              pr[2 * c + 1] * (__uint_as_float(sr[2 * c + 1]) - d4.y));
+          pk[c + 1] = pack2<kF16>(pr[2 * c + 2] * (__uint_as_float(sr[2 * c + 2]) - d4.z),
+                                  pr[2 * c + 3] * (__uint_as_float(sr[2 * c + 3]) - d4.w));
         }
         ptx::tmem_st32x32b_x32(t_dp, pk);
         ptx::tmem_st_wait();
@@ -831,9 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t sr[2][32];
-        ptx::tmem_ld32x32b_x32(t_s, sr[0]);
-        ptx::tmem_ld32x32b_x32(t_s + 32, sr[1]);
+        uint32_t sr[64];
+        ptx::tmem_ld32x32b_x64(t_s, sr);   // one load, one wait for the warpgroup's 64 columns
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarSFree));   // S is in registers: the next S may overwrite it
         const int kb = (ka + t) * kBlk;
@@ -841,27 +841,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         const int base = kb + 64 * g;   // key of this warpgroup's column 0
         const int lo_c = key_lo - base, lim_c = key_lim - base;   // columns lo_c <= c < lim_c are allowed
         float pr[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pr[c] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
         if (cut) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float x = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
-            pr[c] = (c >= lo_c && c < lim_c) ? x : 0.0f;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            pr[c] = ptx::ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2));
+          for (int c = 0; c < 64; ++c) pr[c] = (c >= lo_c && c < lim_c) ? pr[c] : 0.0f;
         }
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
-        ptx::tmem_ld32x32b_x32(t_dp, sr[0]);
-        ptx::tmem_ld32x32b_x32(t_dp + 32, sr[1]);
+        ptx::tmem_ld32x32b_x64(t_dp, sr);
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          pk[c] = pack2<kF16>(pr[2 * c] * (__uint_as_float(sr[c >> 4][(2 * c) & 31]) - dlt),
-                                   pr[2 * c + 1] * (__uint_as_float(sr[c >> 4][(2 * c + 1) & 31]) - dlt));
+          pk[c] = pack2<kF16>(pr[2 * c] * (__uint_as_float(sr[2 * c]) - dlt),
+                              pr[2 * c + 1] * (__uint_as_float(sr[2 * c + 1]) - dlt));
         ptx::tmem_st32x32b_x32(t_dp, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
