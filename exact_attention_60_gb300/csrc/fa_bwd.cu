@@ -668,7 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         if (!ok) break;
         ptx::tc_fence_after();
         issue_acc(L::kColDk, L::kColDp, mnmaj(stage_off(s)), t > 0);                   // dK += dS^T Q
-        ptx::mma_commit_warp(bar(L::kBarQdEmpty + s));   // Q, dO (and LSE, Delta) of stage s read
+        // Q, dO (and LSE, Delta) of stage s read.  Released by this commit, not by a compute
+        // thread once dP^T(t + 1) is done (as the dQ kernel's rings are): with two stages the
+        // later release leaves the next query tile unloaded when S^T(t + 2) is due.
+        ptx::mma_commit_warp(bar(L::kBarQdEmpty + s));
         if (t + 1 < n) {
           issue_rows(L::kColDp, desc_v, kmaj(stage_off(s1) + T::kTileBytes));
           ptx::mma_commit_warp(bar(L::kBarDpFull));
@@ -851,6 +854,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (!ok) break;
         ptx::tc_fence_after();
         ptx::tmem_ld32x32b_x64(t_dp, sr);
+        // Ring slots are released here rather than by MMA commits (each commit costs the
+        // tensor pipe about 90 cycles): dP(t) was V(t)'s only reader, and dP(t) was issued
+        // after dQ(t - 1), K(t - 1)'s last reader.
+        if (threadIdx.x == 0) {
+          ptx::mbar_arrive(bar(L::kBarVEmpty + static_cast<int>(it % L::kVStages)));
+          if (t > 0) ptx::mbar_arrive(bar(L::kBarKEmpty + static_cast<int>((it - 1) % L::kKStages)));
+        }
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c)
@@ -866,6 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (!ok) break;
       ++acc_count;
       ptx::tc_fence_after();
+      // every MMA of the unit is complete: the K slot of its last key tile is free
+      if (threadIdx.x == 0) ptx::mbar_arrive(bar(L::kBarKEmpty + static_cast<int>((it - 1) % L::kKStages)));
       // Epilogue: each warpgroup writes its half of the row's columns.
       uint16_t* dst = p.dq + row_offset(p.dq_s, p.H, bh, valid ? q : 0) + (HD / 2) * g;
 #pragma unroll
@@ -994,7 +1006,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ptx::mma_commit_warp(bar(L::kBarSFull));
         issue_rows(L::kColDp, desc_do, kmaj(v_off(v0)));
         ptx::mma_commit_warp(bar(L::kBarDpFull));
-        ptx::mma_commit_warp(bar(L::kBarVEmpty + v0));   // V read only by dP
       }
       for (int t = 0; t < n && ok; ++t, ++it) {
         const int sk = static_cast<int>(it % L::kKStages);
@@ -1015,14 +1026,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (!ok) break;
         ptx::tc_fence_after();
         issue_acc(mnmaj(k_off(sk)), t > 0);
-        ptx::mma_commit_warp(bar(L::kBarKEmpty + sk));   // K of this key tile read for the last time
         if (t + 1 < n) {   // next dP overwrites dS: issued after the MMA that reads it
           ok = wait_warp(bar(L::kBarVFull + v1), ((it + 1) / L::kVStages) & 1, abort_flag, limit, kSiteMma);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_rows(L::kColDp, desc_do, kmaj(v_off(v1)));
           ptx::mma_commit_warp(bar(L::kBarDpFull));
-          ptx::mma_commit_warp(bar(L::kBarVEmpty + v1));
         }
       }
       if (!ok) break;
