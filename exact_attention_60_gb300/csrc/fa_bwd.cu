@@ -340,8 +340,9 @@ struct DkdvLayout {
   static constexpr int kStageBytes = 2 * T::kTileBytes + 1024;   // Q | dO | lse2[128] | delta[128]
   static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
   static constexpr int kBarKvFull = 0, kBarKvEmpty = 1;
-  static constexpr int kBarQdFull = 2;                          // [kStages]
-  static constexpr int kBarQdEmpty = kBarQdFull + kStages;      // [kStages]
+  static constexpr int kBarQFull = 2;                           // [kStages] Q and LSE*log2e
+  static constexpr int kBarDoFull = kBarQFull + kStages;        // [kStages] dO and Delta
+  static constexpr int kBarQdEmpty = kBarDoFull + kStages;      // [kStages]
   static constexpr int kBarSFull = kBarQdEmpty + kStages;
   static constexpr int kBarDpFull = kBarSFull + 1;
   static constexpr int kBarPFull = kBarDpFull + 1;              // count 256 (compute threads)
@@ -383,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     ptx::mbar_init(bar(L::kBarKvFull), 1);
     ptx::mbar_init(bar(L::kBarKvEmpty), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::kBarQdFull + s), 1);
+      ptx::mbar_init(bar(L::kBarQFull + s), 1);
+      ptx::mbar_init(bar(L::kBarDoFull + s), 1);
       ptx::mbar_init(bar(L::kBarQdEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kBarSFull), 1);
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         const float* dlt = lse2 + kBlk;
         // the stage's LSE and Delta (bulk copies) are read here: wait for the stage
         // itself, and for S^T, which the MMA warp commits
-        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarQdFull + s), (it / L::kStages) & 1, abort_flag,
+        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarQFull + s), (it / L::kStages) & 1, abort_flag,
                                                 limit, kSiteCompute) &&
                                          wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
@@ -488,8 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarPFull));
         // dS^T_kq = P^T_kq (dP^T_kq - Delta_q); the packed result lands over this warpgroup's
-        // first 32 dP^T columns, after both halves have been read.
-        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
+        // first 32 dP^T columns, after both halves have been read.  Delta came with dO.
+        ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarDoFull + s), (it / L::kStages) & 1, abort_flag, limit,
+                                                kSiteCompute) &&
+                                         wait_phase(bar(L::kBarDpFull), it & 1, abort_flag, limit, kSiteCompute));
         if (!ok) break;
         ptx::tc_fence_after();
         ptx::tmem_ld32x32b_x64(t_dp, sr);
@@ -576,15 +580,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         ok = wait_warp(bar(L::kBarQdEmpty + s), ((it / L::kStages) & 1) ^ 1u, abort_flag, limit, kSiteLoad);
         if (!ok) break;
         if (lane == 0) {
-          const uint32_t full = bar(L::kBarQdFull + s);
+          // Q and LSE first (S^T of the tile needs them), then dO and Delta (needed from
+          // dP^T on), each half on its own barrier
+          const uint32_t qfull = bar(L::kBarQFull + s), dofull = bar(L::kBarDoFull + s);
           const size_t rowp = (static_cast<size_t>(bh) * p.nq + qt) * kBlk;   // padded row of the tile
-          ptx::mbar_arrive_expect_tx(full, 2 * T::kTileBytes + 2 * kBlk * 4);
-          for (int rg = 0; rg < T::kRegions; ++rg) {
-            ptx::tma_load_4d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, full, 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
-            ptx::tma_load_4d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, full, 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
-          }
-          ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes, p.lse2 + rowp, kBlk * 4, full);
-          ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes + kBlk * 4, p.delta + rowp, kBlk * 4, full);
+          ptx::mbar_arrive_expect_tx(qfull, T::kTileBytes + kBlk * 4);
+          for (int rg = 0; rg < T::kRegions; ++rg)
+            ptx::tma_load_4d(sbase + stage_off(s) + rg * T::kRegionBytes, &p.tm_q, qfull, 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
+          ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes, p.lse2 + rowp, kBlk * 4, qfull);
+          ptx::mbar_arrive_expect_tx(dofull, T::kTileBytes + kBlk * 4);
+          for (int rg = 0; rg < T::kRegions; ++rg)
+            ptx::tma_load_4d(sbase + stage_off(s) + T::kTileBytes + rg * T::kRegionBytes, &p.tm_do, dofull, 64 * rg, qt * kBlk, bh - (bh / p.H) * p.H, bh / p.H);
+          ptx::bulk_load(sbase + stage_off(s) + 2 * T::kTileBytes + kBlk * 4, p.delta + rowp, kBlk * 4, dofull);
         }
         last_fill[s] = static_cast<int>(it);
       }
@@ -592,7 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     // Drain: every copy this warp started has landed before the CTA exits.
     if (units > 0) drain_phase(bar(L::kBarKvFull), (units - 1) & 1, limit);
     for (int s = 0; s < L::kStages; ++s)
-      if (last_fill[s] >= 0) drain_phase(bar(L::kBarQdFull + s), (last_fill[s] / L::kStages) & 1, limit);
+      if (last_fill[s] >= 0) {
+        drain_phase(bar(L::kBarQFull + s), (last_fill[s] / L::kStages) & 1, limit);
+        drain_phase(bar(L::kBarDoFull + s), (last_fill[s] / L::kStages) & 1, limit);
+      }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA warp (warp-uniform, elected issue)
@@ -638,11 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       ptx::tc_fence_after();
       {
         const int s0 = static_cast<int>(it % L::kStages);
-        ok = wait_warp(bar(L::kBarQdFull + s0), (it / L::kStages) & 1, abort_flag, limit, kSiteMma);
+        ok = wait_warp(bar(L::kBarQFull + s0), (it / L::kStages) & 1, abort_flag, limit, kSiteMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_rows(L::kColS, desc_k, kmaj(stage_off(s0)));
         ptx::mma_commit_warp(bar(L::kBarSFull));
+        ok = wait_warp(bar(L::kBarDoFull + s0), (it / L::kStages) & 1, abort_flag, limit, kSiteMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
         issue_rows(L::kColDp, desc_v, kmaj(stage_off(s0) + T::kTileBytes));
         ptx::mma_commit_warp(bar(L::kBarDpFull));
       }
@@ -658,9 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         ptx::tc_fence_after();
         issue_acc(L::kColDv, L::kColS, mnmaj(stage_off(s) + T::kTileBytes), t > 0);   // dV += P^T dO
         if (t + 1 < n) {   // next S^T overwrites P^T: issued after the MMA that reads it
-          ok = wait_warp(bar(L::kBarQdFull + s1), ((it + 1) / L::kStages) & 1, abort_flag, limit, kSiteMma);
+          // A tile that TMA landed in shared memory needs no tcgen05 fence after its wait
+          // (that fence, which orders MMAs after TMEM hand-offs between threads, costs the
+          // tensor pipe about 80 cycles)
+          ok = wait_warp(bar(L::kBarQFull + s1), ((it + 1) / L::kStages) & 1, abort_flag, limit, kSiteMma);
           if (!ok) break;
-          ptx::tc_fence_after();
           issue_rows(L::kColS, desc_k, kmaj(stage_off(s1)));
           ptx::mma_commit_warp(bar(L::kBarSFull));
         }
@@ -673,6 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         // later release leaves the next query tile unloaded when S^T(t + 2) is due.
         ptx::mma_commit_warp(bar(L::kBarQdEmpty + s));
         if (t + 1 < n) {
+          ok = wait_warp(bar(L::kBarDoFull + s1), ((it + 1) / L::kStages) & 1, abort_flag, limit, kSiteMma);
+          if (!ok) break;   // TMA data: no fence (above)
           issue_rows(L::kColDp, desc_v, kmaj(stage_off(s1) + T::kTileBytes));
           ptx::mma_commit_warp(bar(L::kBarDpFull));
         }
@@ -1027,9 +1044,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ptx::tc_fence_after();
         issue_acc(mnmaj(k_off(sk)), t > 0);
         if (t + 1 < n) {   // next dP overwrites dS: issued after the MMA that reads it
+          // V landed by TMA: no tcgen05 fence after its wait (the fence orders MMAs after
+          // TMEM hand-offs between threads and costs the tensor pipe about 80 cycles)
           ok = wait_warp(bar(L::kBarVFull + v1), ((it + 1) / L::kVStages) & 1, abort_flag, limit, kSiteMma);
           if (!ok) break;
-          ptx::tc_fence_after();
           issue_rows(L::kColDp, desc_do, kmaj(v_off(v1)));
           ptx::mma_commit_warp(bar(L::kBarDpFull));
         }
