@@ -105,7 +105,10 @@ struct Layout {
   // the last P_i V MMA issued so far done (P_i columns free, O_i stable).
   static constexpr int kBarSFree = kBarDrain + 1;           // [2]
   static constexpr int kBarPVDone = kBarSFree + 2;          // [2]
-  static constexpr int kNumBars = kBarPVDone + 2;
+  // D = 128 only: P_i is handed over in halves, p_full for its first 32 packed columns
+  // (K-slices 0-3 of the P V MMA) and p_half for the other 32.
+  static constexpr int kBarPHalf = kBarPVDone + 2;          // [2]
+  static constexpr int kNumBars = kBarPHalf + 2;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
@@ -385,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       ptx::mbar_init(bar(L::kBarQEmpty + i), 1);
       ptx::mbar_init(bar(L::kBarSFull + i), 1);
       ptx::mbar_init(bar(L::kBarPFull + i), 4 * 32);
+      ptx::mbar_init(bar(L::kBarPHalf + i), 4 * 32);
       ptx::mbar_init(bar(L::kBarOFull + i), 1);
       ptx::mbar_init(bar(L::kBarOEmpty + i), 4 * 32);
     }
@@ -545,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
           l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
         } else {
+          // P_i in halves: the MMA warp starts P V on the first while the second is computed.
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t pk[32];
@@ -552,24 +557,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int c = 0; c < 32; ++c)
               pk[c] = exp2_pair<kF16>(s[64 * h + 2 * c], s[64 * h + 2 * c + 1], k2, c2, acc[c & 3]);
             ptx::tmem_st32x32b_x32(t_s + 32 * h, pk);
+            // O_i was last written by P_i(j-1) V, complete since S_i(j) is: rescale it
+            // before the first half is handed over, as that half's MMAs accumulate into O_i.
+            if (h == 0 && j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+              for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t o[32];
+                ptx::tmem_ld32x32b_x32(t_o + c0, o);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                ptx::tmem_st32x32b_x32(t_o + c0, o);
+              }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar((h == 0 ? L::kBarPFull : L::kBarPHalf) + wg));
           }
           float2 a0 = ptx::unpack_f32x2(acc[0]), a1 = ptx::unpack_f32x2(acc[1]);
           float2 a2 = ptx::unpack_f32x2(acc[2]), a3 = ptx::unpack_f32x2(acc[3]);
           l = l * alpha + (((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y)));
-          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-              uint32_t o[32];
-              ptx::tmem_ld32x32b_x32(t_o + c0, o);
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              ptx::tmem_st32x32b_x32(t_o + c0, o);
-            }
-          }
         }
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarPFull + wg));
+        if constexpr (L::kDecoupled) {
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::kBarPFull + wg));
+        }
       }
       if (!ok) break;
       s_base += n_blocks;
@@ -712,14 +724,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ptx::mma_ss_warp(tmem + L::col_s(i), a + off, b + off, kIdescS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int i, int slot, bool accumulate) {
+      // P_i V over K-slices [k0, k1) (16 keys each)
+      auto issue_pv_part = [&](int i, int slot, bool accumulate, int k0, int k1) {
         const uint64_t b = desc_v0 + ((slot * L::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        for (int kk = k0; kk < k1; ++kk) {
           ptx::mma_ts_warp(tmem + L::col_o(i), tmem + L::col_p(i) + kk * 8, b + ((kk * 16 * 128) >> 4),
                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
+      auto issue_pv = [&](int i, int slot, bool accumulate) { issue_pv_part(i, slot, accumulate, 0, kBlockN / 16); };
       uint32_t q_count[2] = {0, 0};   // units in which tile i was present (q_full / o_empty phase)
       uint32_t p_base[2] = {0, 0};    // S_i tiles of earlier units (p_full phase)
       uint32_t it_base = 0;           // K/V ring position of this unit's K_0
@@ -877,7 +891,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               break;
             }
             ptx::tc_fence_after();
-            issue_pv(i, slot_v, jl > 0);
+            issue_pv_part(i, slot_v, jl > 0, 0, kBlockN / 32);   // first half of P_i
+            if (!wait_warp(bar(L::kBarPHalf + i), (p_base[i] + jl) & 1, abort_flag, limit,
+                            kSiteMmaP)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv_part(i, slot_v, true, kBlockN / 32, kBlockN / 16);
             if (jl == nblk[i] - 1) {
               ptx::mma_commit_warp(bar(L::kBarOFull + i));
               if (nblk[i] > 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));   // Q_i no longer read
