@@ -448,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         const int s = static_cast<int>(it % L::kStages);
         const float* lse2 = reinterpret_cast<const float*>(smem + stage_off(s) + 2 * T::kTileBytes) + 64 * g;
         const float* dlt = lse2 + kBlk;
-        // the stage's LSE and Delta (bulk copies) are read here: wait for the stage
-        // itself, and for S^T, which the MMA warp commits
+        // LSE (a bulk copy that lands with Q, the stage's first half) is read here: wait
+        // for that half and for S^T, which the MMA warp commits; Delta comes with dO
         ok = __all_sync(0xffffffffu, wait_phase(bar(L::kBarQFull + s), (it / L::kStages) & 1, abort_flag,
                                                 limit, kSiteCompute) &&
                                          wait_phase(bar(L::kBarSFull), it & 1, abort_flag, limit, kSiteCompute));
