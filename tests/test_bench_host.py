@@ -1,0 +1,98 @@
+"""Host logic of the benchmark: work counts, the DRAM-traffic record and the peak lookup.
+
+The pair counts that every TFLOP/s figure divides by are checked against masks built
+element by element from the mask definitions (top-left causal j <= i; band
+i - left <= j <= i + right; keys past Lk excluded), and the large workloads against the
+closed forms quoted with the measurements.
+"""
+import json
+
+import numpy as np
+import pytest
+
+import bench
+from exact_attention_60_gb300.workloads import WORKLOADS, Workload
+
+
+def brute_pairs(Lq, Lk, causal, window):
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lk)[None, :]
+    keep = np.ones((Lq, Lk), dtype=bool)
+    if window is not None:
+        left, right = window
+        if left >= 0:
+            keep &= j >= i - left
+        if right >= 0:
+            keep &= j <= i + right
+    elif causal:
+        keep &= j <= i
+    return int(keep.sum())
+
+
+@pytest.mark.parametrize("Lq,Lk,causal,window", [
+    (1, 1, False, None), (1, 1, True, None), (130, 130, True, None), (300, 129, True, None),
+    (129, 300, True, None), (500, 257, False, None), (257, 257, False, (100, 0)),
+    (257, 257, False, (64, 64)), (257, 400, False, (-1, 3)), (257, 400, False, (200, -1)),
+    (257, 257, False, (0, 0)), (64, 500, False, (10, 600)),
+])
+def test_pairs_per_head_equal_the_mask(Lq, Lk, causal, window):
+    w = Workload("t", 1, 1, Lq, Lk, 64, causal, window=window)
+    assert w.pairs_per_head() == brute_pairs(Lq, Lk, causal, window)
+    # the per-row ranges the CPU baseline's sampled rows use cover the same pairs
+    assert sum(hi - lo + 1 for lo, hi in (w.key_range(r) for r in range(Lq))) == w.pairs_per_head()
+    assert bench.row_flops(w, range(Lq)) == 4 * w.D * w.pairs_per_head()
+
+
+def test_workload_flops_closed_forms():
+    w = WORKLOADS["seq16k_d128_causal"]
+    assert w.flops() == 4 * 128 * 16 * (16384 * 16385 // 2) == 1_099_578_736_640
+    w = WORKLOADS["seq4k_d128_causal"]
+    assert w.flops() == 4 * 128 * 2 * 32 * (4096 * 4097 // 2)
+    w = WORKLOADS["cross_q500_k8191_d128"]
+    assert w.flops() == 4 * 128 * 8 * 16 * 500 * 8191
+    w = WORKLOADS["seq1k_d64"]
+    assert w.flops() == 4 * 64 * 4 * 16 * 1024 * 1024 == 17_179_869_184
+    w = WORKLOADS["seq16k_d128_window4k"]   # keys i-4095 .. i
+    per_head = sum(min(i, 4095) + 1 for i in range(16384))
+    assert w.flops() == 4 * 128 * 16 * per_head
+
+
+def test_algorithmic_bytes_closed_form():
+    # Q, K, V read and O written once in bf16, LSE written once in fp32
+    w = WORKLOADS["seq16k_d128_causal"]
+    assert w.algorithmic_bytes() == 4 * 16384 * 128 * 2 * 16 + 16 * 16384 * 4 == 269_484_032
+    w = WORKLOADS["cross_q500_k8191_d128"]
+    bh = 8 * 16
+    assert w.algorithmic_bytes() == bh * (2 * 500 + 2 * 8191) * 128 * 2 + bh * 500 * 4
+
+
+def test_measured_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    record = {"kernel_source_sha256": "abc", "workloads": {"seq16k_d128_causal": {"bytes_per_launch": 5.0e8}}}
+    (prof / "dram_traffic.json").write_text(json.dumps(record))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    assert bench.measured_traffic("seq16k_d128_causal") == 5.0e8
+    assert bench.measured_traffic("seq4k_d128_causal") is None       # never captured
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    assert bench.measured_traffic("seq16k_d128_causal") is None      # kernel changed since
+
+
+def test_committed_traffic_record_matches_the_kernel_source():
+    """The committed record must belong to the committed kernel (else the bench reports null)."""
+    data = json.load(open(bench.os.path.join(bench.ROOT, "profiles", "dram_traffic.json")))
+    assert data["kernel_source_sha256"] == bench.kernel_source_hash()
+    for name, entry in data["workloads"].items():
+        assert entry["bytes_per_launch"] == entry["dram_bytes_read"] + entry["dram_bytes_write"]
+        assert entry["algorithmic_bytes"] == WORKLOADS[name].algorithmic_bytes()
+
+
+def test_peak_lookup():
+    assert bench.peak_value({"bf16_tflops": 1911.6}, "bf16_tflops", 1.0) == 1911.6
+    assert bench.peak_value({"bf16_tflops": {"value": "1800"}}, "bf16_tflops", 1.0) == 1800.0
+    assert bench.peak_value({"bf16_tflops": None}, "bf16_tflops", 7.0) == 7.0
+    assert bench.peak_value({}, "hbm_gbs", 6800.0) == 6800.0
+    peaks, source = bench.load_peaks()
+    assert source in ("measured", "fallback")
+    assert bench.peak_value(peaks, "bf16_tflops", 0.0) > 0
