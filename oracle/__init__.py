@@ -88,6 +88,11 @@ class OracleLib:
         lib.oracle_attn_bwd_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
                                              ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                              dp, dp, dp, ctypes.c_int]
+        lib.oracle_attn_bwd_rows.restype = ctypes.c_int
+        lib.oracle_attn_bwd_rows.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                             ctypes.c_long, ctypes.c_int, ctypes.c_double,
+                                             lp, ctypes.c_long, lp, ctypes.c_long, dp, dp, dp,
+                                             dp, dp, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self.lib = lib
@@ -216,6 +221,32 @@ class OracleLib:
             raise ValueError(f"oracle_attn_bwd_head failed with code {rc}")
         return dq, dk, dv
 
+    def attn_bwd_rows(self, q, k, v, do, causal: bool, scale: float, qrows, krows,
+                      nthreads: int = 0):
+        """Gradients of one (batch, head) slice at sampled outputs: dQ at query rows
+        ``qrows``, dK and dV at key rows ``krows``.  Returns (dQ_rows, dK_rows, dV_rows,
+        LSE, Delta), the last two over every query row."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        Lq, D = q.shape
+        Lk = k.shape[0]
+        if k.shape != (Lk, D) or v.shape != (Lk, D) or do.shape != (Lq, D):
+            raise ValueError("k, v must be [Lk, D] and do [Lq, D] with the same D as q")
+        qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int64)).astype(ctypes.c_long)
+        kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int64)).astype(ctypes.c_long)
+        if (qr.size and (qr.min() < 0 or qr.max() >= Lq)) or (kr.size and (kr.min() < 0 or kr.max() >= Lk)):
+            raise ValueError("sampled rows out of range")
+        dq, dk, dv = np.empty((qr.size, D)), np.empty((kr.size, D)), np.empty((kr.size, D))
+        lse, delta = np.empty(Lq), np.empty(Lq)
+        lp = ctypes.POINTER(ctypes.c_long)
+        rc = self.lib.oracle_attn_bwd_rows(_dptr(q), _dptr(k), _dptr(v), _dptr(do), Lq, Lk, D,
+                                           int(bool(causal)), float(scale),
+                                           qr.ctypes.data_as(lp), qr.size, kr.ctypes.data_as(lp),
+                                           kr.size, _dptr(dq), _dptr(dk), _dptr(dv), _dptr(lse),
+                                           _dptr(delta), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_rows failed with code {rc}")
+        return dq, dk, dv, lse, delta
+
     def attn_bwd_head_masked(self, q, k, v, do, left: int, right: int, kv_len: int,
                              scale: float, nthreads: int = 0):
         """Gradients (dQ, dK, dV) under the band and key-padding mask of attn_head_keypad."""
@@ -311,3 +342,7 @@ def attn_bwd_full(*args, **kwargs):
 
 def attn_bwd_head_masked(*args, **kwargs):
     return _get().attn_bwd_head_masked(*args, **kwargs)
+
+
+def attn_bwd_rows(*args, **kwargs):
+    return _get().attn_bwd_rows(*args, **kwargs)

@@ -371,6 +371,137 @@ int oracle_attn_bwd_head(const double *Q, const double *K, const double *V, cons
 }
 
 /*
+ * Gradients of one head at sampled outputs only, for heads too long for the Lq x Lk
+ * matrices of oracle_attn_bwd_head: dQ at the query rows qrows[0..nq) and dK, dV at the
+ * key rows krows[0..nk), by the same chain rule (P_ij = exp(scale Q_i.K_j - LSE_i),
+ * dP_ij = dO_i.V_j, Delta_i = sum_j P_ij dP_ij, dS_ij = P_ij (dP_ij - Delta_i),
+ * dQ_i = scale sum_j dS_ij K_j, dK_j = scale sum_i dS_ij Q_i, dV_j = sum_i P_ij dO_i)
+ * over the allowed pairs of the causal or full mask.  First every query row's LSE_i and
+ * Delta_i are computed from the definition (O(Lq Lk D) work, one score row of scratch per
+ * thread); then each sampled output is a sum over its row (dQ) or its column (dK, dV).
+ * LSE_all and Delta_all (Lq values each) receive the row statistics when not NULL.
+ */
+int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, const double *dO,
+                         long Lq, long Lk, long D, int causal, double scale,
+                         const long *qrows, long nq, const long *krows, long nk,
+                         double *dQ_rows, double *dK_rows, double *dV_rows,
+                         double *LSE_all, double *Delta_all, int nthreads)
+{
+    if (!Q || !K || !V || !dO) return ORACLE_BAD_ARG;
+    if (Lq < 1 || Lk < 1 || D < 1 || nq < 0 || nk < 0) return ORACLE_BAD_ARG;
+    if ((nq > 0 && (!qrows || !dQ_rows)) || (nk > 0 && (!krows || !dK_rows || !dV_rows)))
+        return ORACLE_BAD_ARG;
+    for (long r = 0; r < nq; ++r)
+        if (qrows[r] < 0 || qrows[r] >= Lq) return ORACLE_BAD_ARG;
+    for (long r = 0; r < nk; ++r)
+        if (krows[r] < 0 || krows[r] >= Lk) return ORACLE_BAD_ARG;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)Lq);
+    double *delta = (double *)malloc(sizeof(double) * (size_t)Lq);
+    if (!lse || !delta) {
+        free(lse);
+        free(delta);
+        return ORACLE_NO_MEMORY;
+    }
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *srow = (double *)malloc(sizeof(double) * (size_t)Lk);
+        if (!srow) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            bad = 1;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 8)
+#endif
+        for (long i = 0; i < Lq; ++i) {
+            if (!srow) continue;
+            const long n = allowed_keys(i, Lk, causal);
+            double m = -INFINITY;
+            for (long j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (long d = 0; d < D; ++d) dot += Q[i * D + d] * K[j * D + d];
+                srow[j] = scale * dot;
+                if (srow[j] > m) m = srow[j];
+            }
+            double l = 0.0;
+            for (long j = 0; j < n; ++j) l += exp(srow[j] - m);
+            const double lse_i = m + log(l);
+            double pdp = 0.0;
+            for (long j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (long d = 0; d < D; ++d) dot += dO[i * D + d] * V[j * D + d];
+                pdp += exp(srow[j] - lse_i) * dot;
+            }
+            lse[i] = lse_i;
+            delta[i] = pdp;
+        }
+        free(srow);
+    }
+    if (bad) {
+        free(lse);
+        free(delta);
+        return ORACLE_NO_MEMORY;
+    }
+    /* dQ at the sampled query rows: sums over the row's allowed keys */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long r = 0; r < nq; ++r) {
+        const long i = qrows[r];
+        const long n = allowed_keys(i, Lk, causal);
+        double *out = dQ_rows + r * D;
+        for (long d = 0; d < D; ++d) out[d] = 0.0;
+        for (long j = 0; j < n; ++j) {
+            double s = 0.0, dp = 0.0;
+            for (long d = 0; d < D; ++d) {
+                s += Q[i * D + d] * K[j * D + d];
+                dp += dO[i * D + d] * V[j * D + d];
+            }
+            const double p = exp(scale * s - lse[i]);
+            const double ds = p * (dp - delta[i]);
+            for (long d = 0; d < D; ++d) out[d] += ds * K[j * D + d];
+        }
+        for (long d = 0; d < D; ++d) out[d] *= scale;
+    }
+    /* dK, dV at the sampled key rows: sums over the queries that see the key */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long r = 0; r < nk; ++r) {
+        const long j = krows[r];
+        double *ok = dK_rows + r * D, *ov = dV_rows + r * D;
+        for (long d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
+        for (long i = 0; i < Lq; ++i) {
+            if (j >= allowed_keys(i, Lk, causal)) continue;
+            double s = 0.0, dp = 0.0;
+            for (long d = 0; d < D; ++d) {
+                s += Q[i * D + d] * K[j * D + d];
+                dp += dO[i * D + d] * V[j * D + d];
+            }
+            const double p = exp(scale * s - lse[i]);
+            const double ds = p * (dp - delta[i]);
+            for (long d = 0; d < D; ++d) {
+                ov[d] += p * dO[i * D + d];
+                ok[d] += ds * Q[i * D + d];
+            }
+        }
+        for (long d = 0; d < D; ++d) ok[d] *= scale;
+    }
+    if (LSE_all)
+        for (long i = 0; i < Lq; ++i) LSE_all[i] = lse[i];
+    if (Delta_all)
+        for (long i = 0; i < Lq; ++i) Delta_all[i] = delta[i];
+    free(lse);
+    free(delta);
+    return ORACLE_OK;
+}
+
+/*
  * Gradients under the band and key-padding mask of oracle_attn_head_keypad: the same
  * chain rule as oracle_attn_bwd_head, with row i's allowed keys the contiguous range
  * [lo_i, hi_i] (i - left <= j <= i + right, j < kv_len; -1 = unbounded side) instead of

@@ -332,7 +332,37 @@ def pin_bwd_single_key(lib):
     assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0
 
 
-BWD_PINS = [pin_bwd_finite_differences, pin_bwd_constant_v, pin_bwd_sums, pin_bwd_single_key]
+def pin_bwd_rows_finite_differences(lib):
+    """The row-sampled backward at its sampled rows equals central differences of
+    sum(G * O) (to 1e-7), and its LSE equals the forward's."""
+    for (Lq, Lk, D, causal) in [(5, 6, 3, False), (6, 6, 3, True), (7, 4, 2, True), (3, 8, 4, False)]:
+        q, k, v = _rand((Lq, D), 90 + Lq, 1.5), _rand((Lk, D), 91 + Lk, 1.5), _rand((Lk, D), 92)
+        g = _rand((Lq, D), 93)
+        qr, kr = [0, Lq - 1, Lq // 2], [0, Lk - 1, Lk // 2]
+        dq, dk, dv, lse, _ = lib.attn_bwd_rows(q, k, v, g, causal, 0.7, qr, kr)
+        fq, fk, fv = _fd_grads(lib, q, k, v, g, causal, 0.7)
+        for got, fd in ((dq, fq[qr]), (dk, fk[kr]), (dv, fv[kr])):
+            np.testing.assert_allclose(got, fd, rtol=0, atol=1e-7)
+        np.testing.assert_allclose(lse, lib.attn_head(q, k, v, causal, 0.7)[1], rtol=0, atol=1e-12)
+
+
+def pin_bwd_rows_match_full_head(lib):
+    """On heads small enough for both: the row-sampled backward equals the full-head one at
+    the sampled rows, and Delta_i = sum_j P_ij dP_ij equals dO_i . O_i (the identity the
+    kernels' Delta uses)."""
+    for (Lq, Lk, D, causal) in [(37, 53, 8, True), (37, 53, 8, False), (60, 20, 5, True), (1, 1, 4, False)]:
+        q, k, v, g = (_rand(sh, 100 + Lq + i) for i, sh in enumerate(((Lq, D), (Lk, D), (Lk, D), (Lq, D))))
+        qr, kr = sorted({0, Lq - 1, Lq // 2, Lq // 3}), sorted({0, Lk - 1, Lk // 2, Lk // 5})
+        dq, dk, dv, _, delta = lib.attn_bwd_rows(q, k, v, g, causal, 0.6, qr, kr)
+        fq, fk, fv = lib.attn_bwd_head(q, k, v, g, causal, 0.6)
+        for got, ref in ((dq, fq[qr]), (dk, fk[kr]), (dv, fv[kr])):
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+        o, _ = lib.attn_head(q, k, v, causal, 0.6)
+        np.testing.assert_allclose(delta, (g * o).sum(axis=1), rtol=0, atol=1e-12)
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_constant_v, pin_bwd_sums, pin_bwd_single_key,
+            pin_bwd_rows_finite_differences, pin_bwd_rows_match_full_head]
 PINS.extend(BWD_PINS)
 
 
@@ -478,6 +508,11 @@ MUTATIONS = {
     "bwd_masked_dk_missing_scale": ("dK[j * D + d] = scale * ak;", "dK[j * D + d] = ak;", 1),
     "bwd_masked_padding_ignored": ("if (hi > kv - 1) hi = kv - 1;", ";", 1),
     "keypad_last_key_kept": ("if (hi > kv - 1) hi = kv - 1;", "if (hi > kv) hi = kv;", 0),
+    "bwd_rows_dq_without_row_term": ("const double ds = p * (dp - delta[i]);", "const double ds = p * dp;", 0),
+    "bwd_rows_dk_without_row_term": ("const double ds = p * (dp - delta[i]);", "const double ds = p * dp;", 1),
+    "bwd_rows_dk_missing_scale": ("for (long d = 0; d < D; ++d) ok[d] *= scale;", ";"),
+    "bwd_rows_dv_from_queries": ("ov[d] += p * dO[i * D + d];", "ov[d] += p * Q[i * D + d];"),
+    "bwd_rows_delta_unnormalised": ("pdp += exp(srow[j] - lse_i) * dot;", "pdp += exp(srow[j] - m) * dot;"),
     "window_shifted_values": ("double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D,",
                               "double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
 }
