@@ -93,6 +93,11 @@ class OracleLib:
                                              ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                              lp, ctypes.c_long, lp, ctypes.c_long, dp, dp, dp,
                                              dp, dp, ctypes.c_int]
+        lib.oracle_attn_bwd_rows_masked.restype = ctypes.c_int
+        lib.oracle_attn_bwd_rows_masked.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                                    ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                    ctypes.c_long, ctypes.c_double, lp, ctypes.c_long,
+                                                    lp, ctypes.c_long, dp, dp, dp, dp, dp, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self.lib = lib
@@ -226,6 +231,14 @@ class OracleLib:
         """Gradients of one (batch, head) slice at sampled outputs: dQ at query rows
         ``qrows``, dK and dV at key rows ``krows``.  Returns (dQ_rows, dK_rows, dV_rows,
         LSE, Delta), the last two over every query row."""
+        return self._bwd_rows(q, k, v, do, scale, qrows, krows, nthreads, causal=causal)
+
+    def attn_bwd_rows_masked(self, q, k, v, do, left: int, right: int, kv_len: int,
+                             scale: float, qrows, krows, nthreads: int = 0):
+        """attn_bwd_rows under the band and key-padding mask of attn_bwd_head_masked."""
+        return self._bwd_rows(q, k, v, do, scale, qrows, krows, nthreads, band=(left, right, kv_len))
+
+    def _bwd_rows(self, q, k, v, do, scale, qrows, krows, nthreads, causal=None, band=None):
         q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
         Lq, D = q.shape
         Lk = k.shape[0]
@@ -238,11 +251,14 @@ class OracleLib:
         dq, dk, dv = np.empty((qr.size, D)), np.empty((kr.size, D)), np.empty((kr.size, D))
         lse, delta = np.empty(Lq), np.empty(Lq)
         lp = ctypes.POINTER(ctypes.c_long)
-        rc = self.lib.oracle_attn_bwd_rows(_dptr(q), _dptr(k), _dptr(v), _dptr(do), Lq, Lk, D,
-                                           int(bool(causal)), float(scale),
-                                           qr.ctypes.data_as(lp), qr.size, kr.ctypes.data_as(lp),
-                                           kr.size, _dptr(dq), _dptr(dk), _dptr(dv), _dptr(lse),
-                                           _dptr(delta), int(nthreads))
+        head = (_dptr(q), _dptr(k), _dptr(v), _dptr(do), Lq, Lk, D)
+        tail = (qr.ctypes.data_as(lp), qr.size, kr.ctypes.data_as(lp), kr.size, _dptr(dq), _dptr(dk),
+                _dptr(dv), _dptr(lse), _dptr(delta), int(nthreads))
+        if band is None:
+            rc = self.lib.oracle_attn_bwd_rows(*head, int(bool(causal)), float(scale), *tail)
+        else:
+            left, right, kv_len = (int(x) for x in band)
+            rc = self.lib.oracle_attn_bwd_rows_masked(*head, left, right, kv_len, float(scale), *tail)
         if rc != 0:
             raise ValueError(f"oracle_attn_bwd_rows failed with code {rc}")
         return dq, dk, dv, lse, delta
@@ -346,3 +362,7 @@ def attn_bwd_head_masked(*args, **kwargs):
 
 def attn_bwd_rows(*args, **kwargs):
     return _get().attn_bwd_rows(*args, **kwargs)
+
+
+def attn_bwd_rows_masked(*args, **kwargs):
+    return _get().attn_bwd_rows_masked(*args, **kwargs)

@@ -370,31 +370,47 @@ int oracle_attn_bwd_head(const double *Q, const double *K, const double *V, cons
     return ORACLE_OK;
 }
 
+/* Allowed keys of query row i under the band (left, right; -1 = unbounded side) and the
+ * key count kv: the contiguous range [*lo, *hi], empty when *lo > *hi. */
+static void band_keys(long i, long Lk, long left, long right, long kv, long *lo, long *hi)
+{
+    *lo = (left < 0 || i - left < 0) ? 0 : i - left;
+    long h = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;
+    if (h > kv - 1) h = kv - 1;
+    *hi = h;
+}
+
 /*
  * Gradients of one head at sampled outputs only, for heads too long for the Lq x Lk
- * matrices of oracle_attn_bwd_head: dQ at the query rows qrows[0..nq) and dK, dV at the
- * key rows krows[0..nk), by the same chain rule (P_ij = exp(scale Q_i.K_j - LSE_i),
+ * matrices of oracle_attn_bwd_head(_masked): dQ at the query rows qrows[0..nq) and dK, dV
+ * at the key rows krows[0..nk), by the same chain rule (P_ij = exp(scale Q_i.K_j - LSE_i),
  * dP_ij = dO_i.V_j, Delta_i = sum_j P_ij dP_ij, dS_ij = P_ij (dP_ij - Delta_i),
- * dQ_i = scale sum_j dS_ij K_j, dK_j = scale sum_i dS_ij Q_i, dV_j = sum_i P_ij dO_i)
- * over the allowed pairs of the causal or full mask.  First every query row's LSE_i and
- * Delta_i are computed from the definition (O(Lq Lk D) work, one score row of scratch per
- * thread); then each sampled output is a sum over its row (dQ) or its column (dK, dV).
- * LSE_all and Delta_all (Lq values each) receive the row statistics when not NULL.
+ * dQ_i = scale sum_j dS_ij K_j, dK_j = scale sum_i dS_ij Q_i, dV_j = sum_i P_ij dO_i) over
+ * the allowed pairs of the band and key-padding mask of oracle_attn_bwd_head_masked (query
+ * i sees keys i - left .. i + right below kv_len; -1 = unbounded side).  A row without
+ * allowed keys has LSE = -inf, Delta = 0, dQ = 0 and adds nothing to dK, dV.  First every
+ * query row's LSE_i and Delta_i are computed from the definition (O(Lq Lk D) work, one
+ * score row of scratch per thread); then each sampled output is a sum over its row (dQ)
+ * or its column (dK, dV).  LSE_all and Delta_all (Lq values each) receive the row
+ * statistics when not NULL.
  */
-int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, const double *dO,
-                         long Lq, long Lk, long D, int causal, double scale,
-                         const long *qrows, long nq, const long *krows, long nk,
-                         double *dQ_rows, double *dK_rows, double *dV_rows,
-                         double *LSE_all, double *Delta_all, int nthreads)
+int oracle_attn_bwd_rows_masked(const double *Q, const double *K, const double *V,
+                                const double *dO, long Lq, long Lk, long D, long left,
+                                long right, long kv_len, double scale, const long *qrows,
+                                long nq, const long *krows, long nk, double *dQ_rows,
+                                double *dK_rows, double *dV_rows, double *LSE_all,
+                                double *Delta_all, int nthreads)
 {
     if (!Q || !K || !V || !dO) return ORACLE_BAD_ARG;
-    if (Lq < 1 || Lk < 1 || D < 1 || nq < 0 || nk < 0) return ORACLE_BAD_ARG;
+    if (Lq < 1 || Lk < 1 || D < 1 || nq < 0 || nk < 0 || left < -1 || right < -1)
+        return ORACLE_BAD_ARG;
     if ((nq > 0 && (!qrows || !dQ_rows)) || (nk > 0 && (!krows || !dK_rows || !dV_rows)))
         return ORACLE_BAD_ARG;
     for (long r = 0; r < nq; ++r)
         if (qrows[r] < 0 || qrows[r] >= Lq) return ORACLE_BAD_ARG;
     for (long r = 0; r < nk; ++r)
         if (krows[r] < 0 || krows[r] >= Lk) return ORACLE_BAD_ARG;
+    const long kv = kv_len < 0 ? 0 : (kv_len > Lk ? Lk : kv_len);
     double *lse = (double *)malloc(sizeof(double) * (size_t)Lq);
     double *delta = (double *)malloc(sizeof(double) * (size_t)Lq);
     if (!lse || !delta) {
@@ -420,19 +436,25 @@ int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, cons
 #endif
         for (long i = 0; i < Lq; ++i) {
             if (!srow) continue;
-            const long n = allowed_keys(i, Lk, causal);
+            long lo, hi;
+            band_keys(i, Lk, left, right, kv, &lo, &hi);
+            if (lo > hi) {   /* no allowed key */
+                lse[i] = -INFINITY;
+                delta[i] = 0.0;
+                continue;
+            }
             double m = -INFINITY;
-            for (long j = 0; j < n; ++j) {
+            for (long j = lo; j <= hi; ++j) {
                 double dot = 0.0;
                 for (long d = 0; d < D; ++d) dot += Q[i * D + d] * K[j * D + d];
                 srow[j] = scale * dot;
                 if (srow[j] > m) m = srow[j];
             }
             double l = 0.0;
-            for (long j = 0; j < n; ++j) l += exp(srow[j] - m);
+            for (long j = lo; j <= hi; ++j) l += exp(srow[j] - m);
             const double lse_i = m + log(l);
             double pdp = 0.0;
-            for (long j = 0; j < n; ++j) {
+            for (long j = lo; j <= hi; ++j) {
                 double dot = 0.0;
                 for (long d = 0; d < D; ++d) dot += dO[i * D + d] * V[j * D + d];
                 pdp += exp(srow[j] - lse_i) * dot;
@@ -453,10 +475,11 @@ int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, cons
 #endif
     for (long r = 0; r < nq; ++r) {
         const long i = qrows[r];
-        const long n = allowed_keys(i, Lk, causal);
+        long lo, hi;
+        band_keys(i, Lk, left, right, kv, &lo, &hi);
         double *out = dQ_rows + r * D;
         for (long d = 0; d < D; ++d) out[d] = 0.0;
-        for (long j = 0; j < n; ++j) {
+        for (long j = lo; j <= hi; ++j) {
             double s = 0.0, dp = 0.0;
             for (long d = 0; d < D; ++d) {
                 s += Q[i * D + d] * K[j * D + d];
@@ -477,7 +500,9 @@ int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, cons
         double *ok = dK_rows + r * D, *ov = dV_rows + r * D;
         for (long d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
         for (long i = 0; i < Lq; ++i) {
-            if (j >= allowed_keys(i, Lk, causal)) continue;
+            long lo, hi;
+            band_keys(i, Lk, left, right, kv, &lo, &hi);
+            if (j < lo || j > hi) continue;
             double s = 0.0, dp = 0.0;
             for (long d = 0; d < D; ++d) {
                 s += Q[i * D + d] * K[j * D + d];
@@ -499,6 +524,19 @@ int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, cons
     free(lse);
     free(delta);
     return ORACLE_OK;
+}
+
+/* oracle_attn_bwd_rows_masked for the causal mask (band (-1, 0): key j <= i) or the full
+ * mask (band (-1, -1)), no key padding. */
+int oracle_attn_bwd_rows(const double *Q, const double *K, const double *V, const double *dO,
+                         long Lq, long Lk, long D, int causal, double scale,
+                         const long *qrows, long nq, const long *krows, long nk,
+                         double *dQ_rows, double *dK_rows, double *dV_rows,
+                         double *LSE_all, double *Delta_all, int nthreads)
+{
+    return oracle_attn_bwd_rows_masked(Q, K, V, dO, Lq, Lk, D, -1, causal ? 0 : -1, Lk, scale,
+                                       qrows, nq, krows, nk, dQ_rows, dK_rows, dV_rows, LSE_all,
+                                       Delta_all, nthreads);
 }
 
 /*

@@ -136,38 +136,55 @@ def test_backward_grouped_units_cover_every_head(H, L):
             assert torch.equal(a[:, h:h + 1], b), h
 
 
-def test_backward_seq16k_causal_sampled_rows(oracle_mod):
-    """The backward benchmark's workload (16K causal) at sampled outputs of two heads: dQ
-    at sampled query rows and dK, dV at sampled key rows against the oracle's row-sampled
-    backward, under the element-wise bound of ``check`` computed for those rows and
-    columns only (the full-head matrices would take 2 GB each)."""
-    w = WORKLOADS["seq16k_d128_causal"]
+@pytest.mark.parametrize("name", ["seq16k_d128_causal", "seq16k_d128_window4k", "seq4k_d64_local256"])
+def test_backward_workload_sampled_rows(oracle_mod, name):
+    """Long workloads of the backward benchmark at sampled outputs of two heads: dQ at
+    sampled query rows and dK, dV at sampled key rows against the oracle's row-sampled
+    backward (band masks through its masked form), under the element-wise bound of
+    ``check`` computed for those rows and columns only (the full-head matrices would take
+    up to 2 GB each)."""
+    w = WORKLOADS[name]
+    dev = torch.device("cuda:0")
     q, k, v = make_workload_inputs(w)
     do = make_do(w.B, w.H, w.Lq, w.D, seed=w.seed)
-    o_g, dq_g, dk_g, dv_g = gpu_grads(q, k, v, do, True, w.scale)
-    rng = np.random.default_rng(0x5EED + 3)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse_g = fa.attention(qd, kd, vd, causal=w.causal, scale=w.scale, window=w.window)
+    dq_g, dk_g, dv_g = (t.float().cpu().numpy() for t in
+                        fa.attention_backward(qd, kd, vd, o, lse_g, dod, causal=w.causal, scale=w.scale,
+                                              window=w.window))
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o_g = o.float().cpu().numpy()
+    left, right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
+    rng = np.random.default_rng(0x5EED + w.index)
     rows = sorted({0, 1, 127, 128, 129, w.Lq // 2, w.Lq - 1} | set(rng.integers(0, w.Lq, 9).tolist()))
     keys = sorted({0, 1, 127, 128, w.Lk // 2, w.Lk - 1} | set(rng.integers(0, w.Lk, 9).tolist()))
+    i_all = np.arange(w.Lq)
+    lo_all = np.array([w.key_range(int(i))[0] for i in i_all])
+    hi_all = np.array([w.key_range(int(i))[1] for i in i_all])
     sc = w.scale
     for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
         qh, kh, vh, doh = (t[b, h].double().numpy() for t in (q, k, v, do))
-        rq, rk, rv, lse, delta = oracle_mod.attn_bwd_rows(qh, kh, vh, doh, True, sc, rows, keys)
+        rq, rk, rv, lse, delta = oracle_mod.attn_bwd_rows_masked(qh, kh, vh, doh, left, right, w.Lk, sc,
+                                                                 rows, keys)
         e = 2 * U * np.abs(doh * o_g[b, h].astype(np.float64)).sum(axis=1)   # Delta from bf16 O
-        for r, i in enumerate(rows):          # query row i sees keys 0..i
-            p = np.exp(sc * (kh[:i + 1] @ qh[i]) - lse[i])
-            ds = p * (vh[:i + 1] @ doh[i] - delta[i])
-            bq = sc * (p * e[i] + U * np.abs(ds)) @ np.abs(kh[:i + 1])
+        for r, i in enumerate(rows):          # query row i sees keys lo..hi
+            lo, hi = lo_all[i], hi_all[i]
+            p = np.exp(sc * (kh[lo:hi + 1] @ qh[i]) - lse[i])
+            ds = p * (vh[lo:hi + 1] @ doh[i] - delta[i])
+            bq = sc * (p * e[i] + U * np.abs(ds)) @ np.abs(kh[lo:hi + 1])
             err = np.abs(dq_g[b, h, i] - rq[r])
             assert (err <= 2 * (bq + U * np.abs(rq[r])) + 1e-3).all(), (b, h, i, err.max())
-        for r, j in enumerate(keys):          # key j is seen by queries j..L-1
-            p = np.exp(sc * (qh[j:] @ kh[j]) - lse[j:])
-            ds = p * (doh[j:] @ vh[j] - delta[j:])
-            wgt = p * e[j:] + U * np.abs(ds)
-            bk = sc * wgt @ np.abs(qh[j:])
-            bv = U * p @ np.abs(doh[j:])
-            for name, got, ref, bnd in (("dK", dk_g[b, h, j], rk[r], bk), ("dV", dv_g[b, h, j], rv[r], bv)):
+        for r, j in enumerate(keys):          # key j is seen by the queries whose range holds it
+            sel = (lo_all <= j) & (j <= hi_all)
+            qs, dos = qh[sel], doh[sel]
+            p = np.exp(sc * (qs @ kh[j]) - lse[sel])
+            ds = p * (dos @ vh[j] - delta[sel])
+            wgt = p * e[sel] + U * np.abs(ds)
+            bk = sc * wgt @ np.abs(qs)
+            bv = U * p @ np.abs(dos)
+            for nm, got, ref, bnd in (("dK", dk_g[b, h, j], rk[r], bk), ("dV", dv_g[b, h, j], rv[r], bv)):
                 err = np.abs(got - ref)
-                assert (err <= 2 * (bnd + U * np.abs(ref)) + 1e-3).all(), (name, b, h, j, err.max())
+                assert (err <= 2 * (bnd + U * np.abs(ref)) + 1e-3).all(), (nm, b, h, j, err.max())
 
 
 def test_backward_unattended_keys_are_zero():

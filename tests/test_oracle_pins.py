@@ -451,6 +451,24 @@ def pin_bwd_masked_finite_differences(lib):
             np.testing.assert_allclose(got, fd, rtol=0, atol=1e-7)
 
 
+def pin_bwd_rows_masked_match_full_head(lib):
+    """The row-sampled backward under band and key padding equals the masked full-head
+    backward at the sampled rows (rows without keys included: dQ = 0, LSE = -inf,
+    Delta = 0), and Delta_i = dO_i . O_i with the masked forward's O."""
+    for n, (Lq, Lk, left, right, kv) in enumerate(KEYPAD_CASES):
+        D = 4
+        q, k, v, g = (_rand(sh, 140 + 7 * n + i) for i, sh in enumerate(((Lq, D), (Lk, D), (Lk, D), (Lq, D))))
+        qr, kr = list(range(Lq)), list(range(Lk))
+        dq, dk, dv, lse, delta = lib.attn_bwd_rows_masked(q, k, v, g, left, right, kv, 0.8, qr, kr)
+        fq, fk, fv = lib.attn_bwd_head_masked(q, k, v, g, left, right, kv, 0.8)
+        for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+        o, l = lib.attn_head_keypad(q, k, v, left, right, kv, 0.8)
+        assert np.array_equal(np.isinf(lse), np.isinf(l))
+        np.testing.assert_allclose(lse[np.isfinite(l)], l[np.isfinite(l)], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(delta, (g * o).sum(axis=1), rtol=0, atol=1e-12)
+
+
 def pin_bwd_masked_reduces_to_causal_and_full(lib):
     q, k, v, g = _rand((9, 4), 99), _rand((11, 4), 100), _rand((11, 4), 101), _rand((9, 4), 102)
     for causal, (left, right) in ((False, (-1, -1)), (True, (-1, 0))):
@@ -460,8 +478,10 @@ def pin_bwd_masked_reduces_to_causal_and_full(lib):
             np.testing.assert_allclose(x, y, rtol=0, atol=1e-13)
 
 
-BWD_PINS.extend([pin_bwd_masked_finite_differences, pin_bwd_masked_reduces_to_causal_and_full])
-PINS.extend([pin_bwd_masked_finite_differences, pin_bwd_masked_reduces_to_causal_and_full])
+BWD_PINS.extend([pin_bwd_masked_finite_differences, pin_bwd_masked_reduces_to_causal_and_full,
+                 pin_bwd_rows_masked_match_full_head])
+PINS.extend([pin_bwd_masked_finite_differences, pin_bwd_masked_reduces_to_causal_and_full,
+             pin_bwd_rows_masked_match_full_head])
 
 
 def test_window_rejects_empty_rows(oracle_mod):
@@ -513,6 +533,7 @@ MUTATIONS = {
     "bwd_rows_dk_missing_scale": ("for (long d = 0; d < D; ++d) ok[d] *= scale;", ";"),
     "bwd_rows_dv_from_queries": ("ov[d] += p * dO[i * D + d];", "ov[d] += p * Q[i * D + d];"),
     "bwd_rows_delta_unnormalised": ("pdp += exp(srow[j] - lse_i) * dot;", "pdp += exp(srow[j] - m) * dot;"),
+    "bwd_rows_padding_ignored": ("if (h > kv - 1) h = kv - 1;", ";"),
     "window_shifted_values": ("double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + lo * D,",
                               "double *p_row = P ? P + r * Lk : NULL;\n                attend_row(Q + i * D, K + lo * D, V + (lo > 0 ? lo - 1 : 0) * D,"),
 }
