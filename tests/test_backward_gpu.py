@@ -136,22 +136,29 @@ def test_backward_grouped_units_cover_every_head(H, L):
             assert torch.equal(a[:, h:h + 1], b), h
 
 
-@pytest.mark.parametrize("name", ["seq16k_d128_causal", "seq16k_d128_window4k", "seq4k_d64_local256"])
-def test_backward_workload_sampled_rows(oracle_mod, name):
+@pytest.mark.parametrize("name,kv_pad", [("seq16k_d128_causal", 0.0), ("seq16k_d128_window4k", 0.0),
+                                         ("seq4k_d64_local256", 0.0), ("seq16k_d128_causal", 0.25)])
+def test_backward_workload_sampled_rows(oracle_mod, name, kv_pad):
     """Long workloads of the backward benchmark at sampled outputs of two heads: dQ at
     sampled query rows and dK, dV at sampled key rows against the oracle's row-sampled
     backward (band masks through its masked form), under the element-wise bound of
     ``check`` computed for those rows and columns only (the full-head matrices would take
-    up to 2 GB each)."""
+    up to 2 GB each).  With kv_pad > 0 the keys past each batch's count (drawn as
+    ``bench.py --kv-pad`` draws them) are masked too; their dK and dV must be zero."""
     w = WORKLOADS[name]
     dev = torch.device("cuda:0")
     q, k, v = make_workload_inputs(w)
     do = make_do(w.B, w.H, w.Lq, w.D, seed=w.seed)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    o, lse_g = fa.attention(qd, kd, vd, causal=w.causal, scale=w.scale, window=w.window)
+    kv_len = np.full(w.B, w.Lk, dtype=np.int32)
+    if kv_pad > 0:
+        g = np.random.default_rng(0xCAFE + w.index)
+        kv_len = g.integers(max(1, int(round(w.Lk * (1.0 - 2.0 * kv_pad)))), w.Lk + 1, size=w.B).astype(np.int32)
+    kl = torch.from_numpy(kv_len).to(dev) if kv_pad > 0 else None
+    o, lse_g = fa.attention(qd, kd, vd, causal=w.causal, scale=w.scale, window=w.window, kv_len=kl)
     dq_g, dk_g, dv_g = (t.float().cpu().numpy() for t in
                         fa.attention_backward(qd, kd, vd, o, lse_g, dod, causal=w.causal, scale=w.scale,
-                                              window=w.window))
+                                              window=w.window, kv_len=kl))
     assert fa.fa_last_device_status() == fa.FA_OK
     o_g = o.float().cpu().numpy()
     left, right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
@@ -160,12 +167,18 @@ def test_backward_workload_sampled_rows(oracle_mod, name):
     keys = sorted({0, 1, 127, 128, w.Lk // 2, w.Lk - 1} | set(rng.integers(0, w.Lk, 9).tolist()))
     i_all = np.arange(w.Lq)
     lo_all = np.array([w.key_range(int(i))[0] for i in i_all])
-    hi_all = np.array([w.key_range(int(i))[1] for i in i_all])
+    hi_band = np.array([w.key_range(int(i))[1] for i in i_all])
     sc = w.scale
     for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
+        kv = int(kv_len[b])
+        if kv_pad > 0:
+            keys_b = sorted(set(keys) | {kv - 1, kv} & set(range(w.Lk)))
+        else:
+            keys_b = keys
+        hi_all = np.minimum(hi_band, kv - 1)
         qh, kh, vh, doh = (t[b, h].double().numpy() for t in (q, k, v, do))
-        rq, rk, rv, lse, delta = oracle_mod.attn_bwd_rows_masked(qh, kh, vh, doh, left, right, w.Lk, sc,
-                                                                 rows, keys)
+        rq, rk, rv, lse, delta = oracle_mod.attn_bwd_rows_masked(qh, kh, vh, doh, left, right, kv, sc,
+                                                                 rows, keys_b)
         e = 2 * U * np.abs(doh * o_g[b, h].astype(np.float64)).sum(axis=1)   # Delta from bf16 O
         for r, i in enumerate(rows):          # query row i sees keys lo..hi
             lo, hi = lo_all[i], hi_all[i]
@@ -174,7 +187,7 @@ def test_backward_workload_sampled_rows(oracle_mod, name):
             bq = sc * (p * e[i] + U * np.abs(ds)) @ np.abs(kh[lo:hi + 1])
             err = np.abs(dq_g[b, h, i] - rq[r])
             assert (err <= 2 * (bq + U * np.abs(rq[r])) + 1e-3).all(), (b, h, i, err.max())
-        for r, j in enumerate(keys):          # key j is seen by the queries whose range holds it
+        for r, j in enumerate(keys_b):        # key j is seen by the queries whose range holds it
             sel = (lo_all <= j) & (j <= hi_all)
             qs, dos = qh[sel], doh[sel]
             p = np.exp(sc * (qs @ kh[j]) - lse[sel])

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import exact_attention_60_gb300 as fa
-from exact_attention_60_gb300.workloads import make_qkv
+from exact_attention_60_gb300.workloads import WORKLOADS, make_qkv, make_workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -84,3 +84,29 @@ def test_keypad_out_of_range_lengths_are_clamped(oracle_mod):
     a = run_keypad(q, k, v, [-5, 10_000, 256], (-1, -1))
     b = run_keypad(q, k, v, [0, 256, 256], (-1, -1))
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def bench_kv_len(w, pad):
+    """The per-batch key counts ``bench.py --kv-pad pad`` draws for workload w."""
+    g = np.random.default_rng(0xCAFE + w.index)
+    lo = max(1, int(round(w.Lk * (1.0 - 2.0 * pad))))
+    return g.integers(lo, w.Lk + 1, size=w.B).astype(np.int32)
+
+
+def test_keypad_workload_sampled(oracle_mod):
+    """The key-padding benchmark variant (16K causal, a quarter of the keys padded on
+    average) at sampled rows of every head, rows at the padding edge included."""
+    w = WORKLOADS["seq16k_d128_causal"]
+    kv_len = bench_kv_len(w, 0.25)
+    q, k, v = make_workload_inputs(w)
+    o, lse = run_keypad(q, k, v, kv_len.tolist(), (-1, 0))
+    rng = np.random.default_rng(0x5EED + 99)
+    for b in range(w.B):
+        kv = int(kv_len[b])
+        rows = sorted({0, 1, 127, 128, kv - 2, kv - 1, kv, kv + 1, w.Lq - 1} & set(range(w.Lq))
+                      | set(rng.integers(0, w.Lq, 24).tolist()))
+        for h in (0, w.H // 2, w.H - 1):
+            ref_o, ref_l = oracle_mod.attn_head_keypad(q[b, h], k[b, h], v[b, h], -1, 0, kv, w.scale,
+                                                       rows=rows)
+            assert np.abs(o[b, h][rows] - ref_o).max() <= TOL_O
+            assert np.abs(lse[b, h][rows] - ref_l).max() <= TOL_LSE
