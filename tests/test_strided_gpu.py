@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import exact_attention_60_gb300 as fa
-from exact_attention_60_gb300.workloads import make_qkv
+from exact_attention_60_gb300.workloads import WORKLOADS, make_qkv, make_workload_inputs, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -132,3 +132,45 @@ def test_strided_guard_band_untouched():
     assert (buf[..., 64:] == 5.0).all()
     o_ref, _ = fa.attention(q, k, v, causal=True, split=False)
     assert torch.equal(out, o_ref)
+
+
+def bshd(t):
+    """The same [B, H, L, D] values stored [B, L, H, D] (a strided view)."""
+    return t.transpose(1, 2).contiguous().transpose(1, 2)
+
+
+def test_workload_bshd_equals_contiguous_both_passes():
+    """The benchmark's [B, L, H, D] variant of the 16K causal workload: forward and backward
+    results identical to the contiguous calls, bit for bit (only addressing changes)."""
+    w = WORKLOADS["seq16k_d128_causal"]
+    q, k, v = (t.to(DEV) for t in make_workload_inputs(w))
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(w.seed + 99)).to(torch.bfloat16).to(DEV)
+    o, lse = fa.attention(q, k, v, causal=True)
+    grads = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    qb, kb, vb, dob = (bshd(t) for t in (q, k, v, do))
+    assert not qb.is_contiguous()
+    o_b, lse_b = fa.attention(qb, kb, vb, causal=True)
+    dq_b, dk_b, dv_b = (bshd(torch.empty_like(t)) for t in (q, k, v))
+    fa.attention_backward(qb, kb, vb, o_b, lse_b, dob, causal=True, dq=dq_b, dk=dk_b, dv=dv_b)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert torch.equal(o_b, o) and torch.equal(lse_b, lse)
+    for a, b in zip(grads, (dq_b, dk_b, dv_b)):
+        assert torch.equal(a, b)
+
+
+def test_workload_fp16_sampled(oracle_mod):
+    """The benchmark's fp16 variant of the 16K causal workload against the oracle at
+    sampled rows (the bf16 draws are exact in fp16)."""
+    w = WORKLOADS["seq16k_d128_causal"]
+    q, k, v = (t.to(torch.float16) for t in make_workload_inputs(w))
+    o, lse = fa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    assert o.dtype == torch.float16 and fa.fa_last_device_status() == fa.FA_OK
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    pairs = sample_rows(w, 256)
+    for bh in np.unique(pairs[:, 0]):
+        rows = pairs[pairs[:, 0] == bh, 1]
+        b, h = divmod(int(bh), w.H)
+        ref_o, ref_l = oracle_mod.attn_head(q[b, h].float(), k[b, h].float(), v[b, h].float(), True,
+                                            w.scale, rows=rows)
+        assert np.abs(o[b, h][rows] - ref_o).max() <= TOL_O
+        assert np.abs(lse[b, h][rows] - ref_l).max() <= TOL_LSE
