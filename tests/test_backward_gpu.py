@@ -136,20 +136,25 @@ def test_backward_grouped_units_cover_every_head(H, L):
             assert torch.equal(a[:, h:h + 1], b), h
 
 
-@pytest.mark.parametrize("name,kv_pad", [("seq16k_d128_causal", 0.0), ("seq16k_d128_window4k", 0.0),
-                                         ("seq4k_d64_local256", 0.0), ("seq16k_d128_causal", 0.25)])
-def test_backward_workload_sampled_rows(oracle_mod, name, kv_pad):
+@pytest.mark.parametrize("name,kv_pad,dtype", [("seq16k_d128_causal", 0.0, torch.bfloat16),
+                                               ("seq16k_d128_window4k", 0.0, torch.bfloat16),
+                                               ("seq4k_d64_local256", 0.0, torch.bfloat16),
+                                               ("seq16k_d128_causal", 0.25, torch.bfloat16),
+                                               ("seq16k_d128_causal", 0.0, torch.float16)])
+def test_backward_workload_sampled_rows(oracle_mod, name, kv_pad, dtype):
     """Long workloads of the backward benchmark at sampled outputs of two heads: dQ at
     sampled query rows and dK, dV at sampled key rows against the oracle's row-sampled
     backward (band masks through its masked form), under the element-wise bound of
     ``check`` computed for those rows and columns only (the full-head matrices would take
     up to 2 GB each).  With kv_pad > 0 the keys past each batch's count (drawn as
-    ``bench.py --kv-pad`` draws them) are masked too; their dK and dV must be zero."""
+    ``bench.py --kv-pad`` draws them) are masked too; their dK and dV must be zero.  fp16
+    runs on the same values (the bf16 draws are exact in fp16) under the same bound, which
+    assumes bf16 rounding and so holds for fp16 too."""
     w = WORKLOADS[name]
     dev = torch.device("cuda:0")
     q, k, v = make_workload_inputs(w)
     do = make_do(w.B, w.H, w.Lq, w.D, seed=w.seed)
-    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    qd, kd, vd, dod = (t.to(dtype).to(dev) for t in (q, k, v, do))
     kv_len = np.full(w.B, w.Lk, dtype=np.int32)
     if kv_pad > 0:
         g = np.random.default_rng(0xCAFE + w.index)
