@@ -173,13 +173,21 @@ def test_backward_workload_sampled_rows(oracle_mod, name, kv_pad, dtype):
     i_all = np.arange(w.Lq)
     lo_all = np.array([w.key_range(int(i))[0] for i in i_all])
     hi_band = np.array([w.key_range(int(i))[1] for i in i_all])
-    sc = w.scale
-    for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
-        kv = int(kv_len[b])
-        if kv_pad > 0:
-            keys_b = sorted(set(keys) | {kv - 1, kv} & set(range(w.Lk)))
-        else:
-            keys_b = keys
+    check_sampled(oracle_mod, q, k, v, do, o_g, (dq_g, dk_g, dv_g), [(0, 0), (w.B - 1, w.H - 1)],
+                  (left, right), kv_len if kv_pad > 0 else None, w.scale, rows, keys, lo_all, hi_band)
+
+
+def check_sampled(oracle_mod, q, k, v, do, o_g, grads, heads, band, kv_len, sc, rows, keys, lo_all, hi_band):
+    """dQ at query rows ``rows`` and dK, dV at key rows ``keys`` of the given heads against
+    the oracle's row-sampled backward, under the element-wise bound of ``check`` computed
+    for those rows and columns.  Query row i may see keys lo_all[i]..hi_band[i] below the
+    batch's key count (``kv_len``, None for all keys); padded keys' gradients must be 0."""
+    dq_g, dk_g, dv_g = grads
+    left, right = band
+    Lk = k.shape[2]
+    for (b, h) in heads:
+        kv = Lk if kv_len is None else int(kv_len[b])
+        keys_b = keys if kv_len is None else sorted(set(keys) | {kv - 1, kv} & set(range(Lk)))
         hi_all = np.minimum(hi_band, kv - 1)
         qh, kh, vh, doh = (t[b, h].double().numpy() for t in (q, k, v, do))
         rq, rk, rv, lse, delta = oracle_mod.attn_bwd_rows_masked(qh, kh, vh, doh, left, right, kv, sc,
@@ -203,6 +211,30 @@ def test_backward_workload_sampled_rows(oracle_mod, name, kv_pad, dtype):
             for nm, got, ref, bnd in (("dK", dk_g[b, h, j], rk[r], bk), ("dV", dv_g[b, h, j], rv[r], bv)):
                 err = np.abs(got - ref)
                 assert (err <= 2 * (bnd + U * np.abs(ref)) + 1e-3).all(), (nm, b, h, j, err.max())
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,D,causal", [(1, 2, 8191, 8191, 128, True), (2, 1, 5000, 12345, 64, False),
+                                                (1, 1, 12000, 3000, 128, True)])
+def test_backward_large_ragged_sampled(oracle_mod, B, H, Lq, Lk, D, causal):
+    """Large problems whose lengths are not tile multiples (causal with Lq > Lk included:
+    query rows past Lk see every key), at sampled outputs of the first and last head."""
+    dev = torch.device("cuda:0")
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed=Lq + Lk + D)
+    do = make_do(B, H, Lq, D, seed=Lq + D)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention(qd, kd, vd, causal=causal, scale=scale)
+    grads = tuple(t.float().cpu().numpy() for t in fa.attention_backward(qd, kd, vd, o, lse, dod,
+                                                                         causal=causal, scale=scale))
+    assert fa.fa_last_device_status() == fa.FA_OK
+    rng = np.random.default_rng(Lq * 7 + Lk)
+    edges = lambda L: {0, 1, 127, 128, 129, L // 2, L - 2, L - 1, (L - 1) // 128 * 128, (L - 1) // 128 * 128 - 1}
+    rows = sorted({i for i in edges(Lq) | {Lk - 1, Lk} if 0 <= i < Lq} | set(rng.integers(0, Lq, 8).tolist()))
+    keys = sorted({j for j in edges(Lk) if 0 <= j < Lk} | set(rng.integers(0, Lk, 8).tolist()))
+    i_all = np.arange(Lq)
+    hi_band = np.minimum(i_all, Lk - 1) if causal else np.full(Lq, Lk - 1)
+    check_sampled(oracle_mod, q, k, v, do, o.float().cpu().numpy(), grads, [(0, 0), (B - 1, H - 1)],
+                  (-1, 0 if causal else -1), None, scale, rows, keys, np.zeros(Lq, dtype=np.int64), hi_band)
 
 
 def test_backward_unattended_keys_are_zero():
