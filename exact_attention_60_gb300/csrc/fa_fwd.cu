@@ -1620,7 +1620,7 @@ extern "C" fa_status fa_fwd_strided(const void* Q, const long long* q_stride, co
 // Scratch for fa_fwd_noalloc: the split schedule's workspace, held in device
 // memory that the CUDA runtime reserves when this library's module is loaded on a
 // GPU, so the call itself never allocates.  42 MiB covers the split schedule at
-// D = 128 on up to 165 SMs (GB300 has 152) and at D = 64 on up to 326 SMs.
+// D = 128 on up to 165 SMs (GB300 has 152) and at D = 64 on up to 325 SMs.
 constexpr size_t kNoAllocScratchBytes = 42ull << 20;
 static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -201,13 +201,17 @@ fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K
  * The split schedule's workspace lives in a 42 MiB device array inside this
  * library, reserved on every GPU that loads the library and held until the
  * process exits.  That covers the split schedule at D = 128 on GPUs with up to
- * 165 SMs (D = 64: 326 SMs); on larger GPUs a problem that would need more
+ * 165 SMs (D = 64: 325 SMs); on larger GPUs a problem that would need more
  * returns FA_ERR_UNSUPPORTED before anything is launched.  Problems that run on
  * whole units (all causal ones, and non-causal ones that keep the SMs busy) use
  * no scratch at all.  Nothing is allocated by the call itself.
  *
  * The first call on each device looks up the array's device address (once, with
- * that device current); make that first call before any stream capture.  Every
+ * that device current); make that first call before any stream capture.  The
+ * address is kept for the life of the process: a cudaDeviceReset (or anything
+ * else that destroys the device's primary context) makes it, like the library's
+ * other per-device settings, stale, so after a reset no entry point of this
+ * library may be called on that device again in the same process.  Every
  * call shares the one array and leaves scratch in it (it needs no clearing):
  * calls whose kernels can overlap on the GPU -- on different streams, or from
  * different host threads -- race on it and must be ordered by the caller.

@@ -93,7 +93,8 @@ static void attend_row(const double *q, const double *K, const double *V,
  *         (then nrows must equal Lq).
  *   O: [nrows, D] out; LSE: [nrows] out; P: [nrows, Lk] out or NULL.
  *   nthreads: OpenMP threads to use (<= 0: the runtime default).
- * Returns ORACLE_OK, or an error code with no output written.
+ * Returns ORACLE_OK, or an error code (argument errors before any output is written;
+ * ORACLE_NO_MEMORY with the outputs incomplete).
  */
 int oracle_attn_head(const double *Q, const double *K, const double *V,
                      long Lq, long Lk, long D, int causal, double scale,
@@ -114,16 +115,21 @@ int oracle_attn_head(const double *Q, const double *K, const double *V,
     {
         double *S = (double *)malloc(sizeof(double) * (size_t)Lk);
         double *Pr = (double *)malloc(sizeof(double) * (size_t)Lk);
-        if (!S || !Pr) {
+        const int have = S && Pr;
+        if (!have) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
             status = ORACLE_NO_MEMORY;
-        } else {
+        }
+        /* Every thread of the team meets the worksharing loop; one without its row
+         * buffers takes its share of rows and skips them (the call then fails). */
+        {
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 4)
 #endif
             for (long r = 0; r < nrows; ++r) {
+                if (!have) continue;
                 const long i = rows ? rows[r] : r;
                 attend_row(Q + i * D, K, V, Lk, D, allowed_keys(i, Lk, causal), scale,
                            S, Pr, O + r * D, LSE + r, P ? P + r * Lk : NULL);
@@ -189,16 +195,21 @@ int oracle_attn_head_window(const double *Q, const double *K, const double *V,
     {
         double *S = (double *)malloc(sizeof(double) * (size_t)Lk);
         double *Pr = (double *)malloc(sizeof(double) * (size_t)Lk);
-        if (!S || !Pr) {
+        const int have = S && Pr;
+        if (!have) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
             status = ORACLE_NO_MEMORY;
-        } else {
+        }
+        /* Every thread of the team meets the worksharing loop; one without its row
+         * buffers takes its share of rows and skips them (the call then fails). */
+        {
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 4)
 #endif
             for (long r = 0; r < nrows; ++r) {
+                if (!have) continue;
                 const long i = rows ? rows[r] : r;
                 const long lo = (left < 0 || i - left < 0) ? 0 : i - left;
                 const long hi = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;
@@ -247,16 +258,21 @@ int oracle_attn_head_keypad(const double *Q, const double *K, const double *V,
     {
         double *S = (double *)malloc(sizeof(double) * (size_t)Lk);
         double *Pr = (double *)malloc(sizeof(double) * (size_t)Lk);
-        if (!S || !Pr) {
+        const int have = S && Pr;
+        if (!have) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
             status = ORACLE_NO_MEMORY;
-        } else {
+        }
+        /* Every thread of the team meets the worksharing loop; one without its row
+         * buffers takes its share of rows and skips them (the call then fails). */
+        {
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 4)
 #endif
             for (long r = 0; r < nrows; ++r) {
+                if (!have) continue;
                 const long i = rows ? rows[r] : r;
                 const long lo = (left < 0 || i - left < 0) ? 0 : i - left;
                 long hi = (right < 0 || i + right > Lk - 1) ? Lk - 1 : i + right;

@@ -222,3 +222,32 @@ def test_fwd_strided_accepts_shared_inputs_and_empty(lib):
                              64, -1, -1, 0.125, 0, None, 0, 0) == fa.FA_OK
     # a missing stride array with work to do is an argument error
     assert call_strided(qs=None) == fa.FA_ERR_INVALID_ARG
+
+
+def split_workspace_bytes(grid: int, D: int) -> int:
+    """The split schedule's workspace as fa_fwd_workspace_size documents it: 2 slots x
+    2 query tiles x 128 rows per CTA of D partial-O floats, then (m, l) per row, each
+    array rounded up to 256 bytes."""
+    r256 = lambda x: (x + 255) & ~255
+    rows = grid * 2 * 2 * 128
+    return r256(rows * D * 4) + r256(rows * 2 * 4)
+
+
+def test_noalloc_documented_limits_follow_from_the_scratch_size():
+    """The largest grid whose split workspace fits fa_fwd_noalloc's built-in scratch,
+    for each head dimension, is the SM count that the header and the source state."""
+    src = open(os.path.join(ROOT, "exact_attention_60_gb300", "csrc", "fa_fwd.cu")).read()
+    m = re.search(r"kNoAllocScratchBytes = (\d+)ull << (\d+);", src)
+    assert m, "scratch size constant not found"
+    cap = int(m.group(1)) << int(m.group(2))
+    limits = {}
+    for D in (128, 64):
+        g = 1
+        while split_workspace_bytes(g + 1, D) <= cap:
+            g += 1
+        limits[D] = g
+    header = open(os.path.join(ROOT, "include", "fa.h")).read()
+    stated = f"{limits[128]} SMs (D = 64: {limits[64]} SMs)"
+    assert stated in " ".join(header.split()), stated
+    assert (f"D = 128 on up to {limits[128]} SMs" in src
+            and f"at D = 64 on up to {limits[64]} SMs" in src)

@@ -9,8 +9,12 @@ memory built into the library instead of a caller-provided workspace.
 Each test calls it through the C ABI twice in a row (the second call finds the
 scratch as the first call left it) and compares the results with the existing
 entry points -- fa_fwd_ws given its own workspace, or fa_fwd when no scratch is
-involved -- within the same tolerances as the other parity tests.  The file is
-named so that pytest collects it after every other test file.
+involved.  The results must lie within the tolerances of the other parity tests
+and, since both calls run the same kernels on the same schedule and inputs, be
+bit-identical: a stale or partly overwritten scratch slot would show there.  One
+test also checks the property the entry point exists for: a call changes the
+device's free memory by nothing.  The file is named so that pytest collects it
+after every other test file.
 """
 import math
 
@@ -50,6 +54,28 @@ def test_noalloc_matches_workspace_entry_point(B, H, Lq, Lk, D):
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
         assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O
         assert (lse - l_ref).abs().max().item() <= TOL_LSE
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    """After a first call (which looks up the scratch address), a call on a split
+    shape leaves the device's free memory exactly as it was."""
+    B, H, Lq, Lk, D = 1, 4, 2048, 32768, 128
+    # The workspace it replaces: 2 slots x 2 tiles x 128 rows per CTA (one CTA per SM
+    # here) of D partial-O floats, then (m, l) per row, each rounded up to 256 bytes.
+    rows = torch.cuda.get_device_properties(0).multi_processor_count * 2 * 2 * 128
+    r256 = lambda x: (x + 255) & ~255
+    assert fa.fa_fwd_workspace_size(B, H, Lq, Lk, D, False) == (
+        fa.FA_OK, r256(rows * D * 4) + r256(rows * 2 * 4))
+    q, k, v, o, lse = _buffers(B, H, Lq, Lk, D, seed=3)
+    scale = 1.0 / math.sqrt(D)
+    assert fa.fa_fwd_noalloc(q, k, v, o, lse, B, H, Lq, Lk, D, 0, scale) == fa.FA_OK
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    assert fa.fa_fwd_noalloc(q, k, v, o, lse, B, H, Lq, Lk, D, 0, scale) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert fa.fa_last_device_status() == fa.FA_OK
 
 
 def test_noalloc_without_scratch_matches_fa_fwd():
@@ -66,6 +92,7 @@ def test_noalloc_without_scratch_matches_fa_fwd():
         assert fa.fa_last_device_status() == fa.FA_OK
         assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O
         assert (lse - l_ref).abs().max().item() <= TOL_LSE
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
 
 
 def test_noalloc_rejects_bad_arguments():
