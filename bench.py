@@ -9,13 +9,17 @@ unmasked (query, key) pair.  Between timed steps the inputs rotate over enough
 copies that their total exceeds twice the L2 cache.
 
 Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
-  e2e          the same metric through the public host-buffer call
-               (attention_from_host: pinned host Q, K, V in, host O, LSE out; the
-               copies and kernels overlap by chunks of heads) with every copy inside
-               the timed region;
-  roofline     achieved TFLOP/s of the kernel against the measured bf16 peak;
+  e2e          the same metric through the C host-buffer call fa_fwd_host (pinned
+               host Q, K, V in, host O, LSE out; the library overlaps the copies and
+               kernels by chunks of heads) with every copy inside the timed region,
+               beside the time one plain upload of the inputs takes;
+  roofline     achieved TFLOP/s of the kernel against the measured bf16 peak (or GB/s
+               against the measured copy rate, whichever roof the workload meets first);
   cpu_baseline the fp64 oracle timed on the host cores on a bounded row sample;
-  clocks       SM clocks and throttle reasons sampled during the timed region.
+  clocks       SM clocks, power and throttle reasons sampled during the timed region;
+  per_config   every configuration of the specification (C1-C5, C2 with both masks),
+               each timed over at least --per-config-seconds of back-to-back launches
+               with its own roofline and the clock samples taken inside that window.
 With --impl reference the fp64 CPU oracle is the measured arm (bounded row
 samples of the same workload per step), printed with "impl": "reference".
 
@@ -75,13 +79,18 @@ def peak_value(peaks: dict, key: str, default: float) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks, power and throttle reasons while running.
+
+    Every sample carries nvidia-smi's own timestamp, so ``summary(t0, t1)`` can keep only
+    the samples taken inside a timed window (host wall-clock seconds, time.time())."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 100):
         self.gpu_index = gpu_index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
         self.error = None
@@ -90,7 +99,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -101,33 +110,53 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def _samples(self):
+        import datetime
+        out = []
+        for line in list(self.lines):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax = float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            try:
+                power = float(parts[4])
+            except ValueError:
+                power = None
+            reasons = {n for n, v in zip(self.REASONS, parts[6:10]) if v.lower() == "active"}
+            out.append((t, sm, smax, power, reasons))
+        return out
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock, throttle reasons and power over the samples taken in
+        [t0, t1] (all samples when no window is given or none falls inside it)."""
+        samples = self._samples()
+        if not samples:
+            return {"error": self.error or "no clock samples"}
+        inside = [x for x in samples if t0 is not None and t0 <= x[0] <= t1]
+        use = inside if inside else samples
+        power = [x[3] for x in use if x[3] is not None]
+        res = {"sm_mhz": statistics.median(x[1] for x in use),
+               "sm_max_mhz": max(x[2] for x in use),
+               "reasons": sorted(set().union(*(x[4] for x in use))),
+               "samples": len(use), "samples_in_window": len(inside),
+               "power_w_max": max(power) if power else None}
+        if t0 is not None:
+            res["window_s"] = t1 - t0
+        return res
+
     def stop(self):
         if self.proc is None:
-            return {"error": self.error or "nvidia-smi unavailable"}
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"error": "no clock samples"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def dist_setup(n_gpus: int):
@@ -266,6 +295,223 @@ def run_reference(args, w):
     return 0
 
 
+class ForwardSetup:
+    """Device buffers of one forward workload, rotated over enough copies that their
+    total exceeds twice the L2 cache, and ``launch(i)`` for step i (a public C call)."""
+
+    def __init__(self, fa, w, dev, stream, dtype="bf16", layout="bhld", kv_pad=0.0):
+        import torch
+        self.fa, self.w, self.dev, self.stream = fa, w, dev, stream
+        q_h, k_h, v_h = make_workload_inputs(w)
+        # Variants of the same workload (fa_fwd_strided): fp16 values, Q/K/V read in place
+        # from [B, L, H, D] memory, per-batch key padding.
+        self.variant = dtype != "bf16" or layout != "bhld" or kv_pad > 0
+        io_dtype = torch.float16 if dtype == "fp16" else torch.bfloat16
+        if dtype == "fp16":
+            q_h, k_h, v_h = (t.to(torch.float16) for t in (q_h, k_h, v_h))
+        self.host = (q_h, k_h, v_h)
+        self.kv_len_h = None
+        if kv_pad > 0:
+            g = np.random.default_rng(0xCAFE + w.index)
+            lo = max(1, int(round(w.Lk * (1.0 - 2.0 * kv_pad))))
+            self.kv_len_h = g.integers(lo, w.Lk + 1, size=w.B).astype(np.int32)
+        self.in_bytes = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+        self.out_bytes = q_h.numel() * 2 + w.B * w.H * w.Lq * 4
+        self.n_copies = max(2, math.ceil(2 * L2_BYTES / (self.in_bytes + self.out_bytes)) + 1)
+
+        def place(t):   # [B, H, L, D] values, stored [B, L, H, D] with layout bshd
+            t = t.to(dev)
+            return t.transpose(1, 2).contiguous().transpose(1, 2) if layout == "bshd" else t
+
+        base = tuple(place(t) for t in (q_h, k_h, v_h))
+        self.bufs = []
+        for c in range(self.n_copies):
+            qkv = base if c == 0 else tuple(place(t) for t in (q_h, k_h, v_h))
+            o = torch.empty((w.B, w.H, w.Lq, w.D), device=dev, dtype=io_dtype)
+            lse = torch.empty((w.B, w.H, w.Lq), device=dev, dtype=torch.float32)
+            self.bufs.append((*qkv, o, lse))
+        self.kv_len = torch.from_numpy(self.kv_len_h).to(dev) if self.kv_len_h is not None else None
+        # Workspace for the split-key schedule, allocated once outside the timed region
+        # (zero bytes, and plain fa_fwd semantics, for causal workloads).  Local-window
+        # workloads run fa_fwd_window (whole units, no workspace).
+        if w.window is None and self.kv_len is None:
+            st, self.ws_bytes = fa.fa_fwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
+            if st != fa.FA_OK:
+                raise RuntimeError(fa.fa_status_string(st))
+        else:
+            self.ws_bytes = 0
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev) if self.ws_bytes else None
+        self.left, self.right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
+        self.code = fa.FA_DTYPE_FP16 if dtype == "fp16" else fa.FA_DTYPE_BF16
+        torch.cuda.synchronize(dev)
+
+    def launch(self, i):
+        fa, w = self.fa, self.w
+        q, k, v, o, lse = self.bufs[i % self.n_copies]
+        if self.variant:
+            st = fa.fa_fwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], o,
+                                   o.stride()[:3], lse, self.kv_len, w.B, w.H, w.Lq, w.Lk, w.D,
+                                   self.left, self.right, w.scale, self.code, self.ws,
+                                   self.ws_bytes, self.stream)
+        elif w.window is not None:
+            st = fa.fa_fwd_window(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.window[0],
+                                  w.window[1], w.scale, self.stream)
+        else:
+            st = fa.fa_fwd_ws(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.causal, w.scale,
+                              self.ws, self.ws_bytes, self.stream)
+        if st != fa.FA_OK:
+            raise RuntimeError(fa.fa_status_string(st))
+
+    def flops(self):
+        w = self.w
+        if self.kv_len_h is None:
+            return w.flops()
+        i = np.arange(w.Lq, dtype=np.int64)   # only the unpadded pairs count
+        lo = np.zeros_like(i) if self.left < 0 else np.maximum(0, i - self.left)
+        hi_band = np.full_like(i, w.Lk - 1) if self.right < 0 else np.minimum(w.Lk - 1, i + self.right)
+        pairs = sum(int(np.maximum(0, np.minimum(hi_band, kl - 1) - lo + 1).sum()) for kl in self.kv_len_h)
+        return 4 * w.D * w.H * pairs
+
+    def algorithmic_bytes(self):
+        w = self.w
+        alg = w.algorithmic_bytes()
+        if self.kv_len_h is not None:   # padded keys are never read
+            alg = alg - 2 * 2 * w.B * w.H * w.Lk * w.D + 2 * 2 * w.H * w.D * int(self.kv_len_h.sum())
+        return alg
+
+    def free(self):
+        import torch
+        self.bufs = []
+        self.ws = None
+        self.kv_len = None
+        torch.cuda.empty_cache()
+
+
+def roofline_of(setup, flops, per_launch_s, peaks, peak_src, traffic, sustained=False):
+    """The roof the workload's algorithmic intensity (flops per algorithmic byte: Q, K, V
+    read once, O and LSE written once) meets first, and the achieved fraction of it; both
+    fractions are reported.  ``sustained``: the kernel ran back to back for a second or
+    more, under the power cap, so the sustained bf16 figure is the tensor roof."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = peak_value(peaks, key, FALLBACK_PEAKS[key])
+    hbm_peak = peak_value(peaks, "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    alg_bytes = setup.algorithmic_bytes()
+    kernel_tflops = flops / per_launch_s / 1e12
+    hbm_gbs = alg_bytes / per_launch_s / 1e9
+    if flops / alg_bytes >= peak * 1e12 / (hbm_peak * 1e9):
+        roof = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
+                "frac": kernel_tflops / peak,
+                "peak_source": f"{peak_src} bf16 dense ({'sustained' if sustained else 'burst'})"}
+    else:
+        roof = {"bound": "hbm", "achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": hbm_gbs / hbm_peak, "peak_source": f"{peak_src} HBM copy"}
+    roof.update({"traffic": traffic, "kernel": f"{KERNEL_NAME}<{setup.w.D}>",
+                 "algorithmic_bytes": alg_bytes, "flops_per_byte": flops / alg_bytes,
+                 "tensor_frac": kernel_tflops / peak, "hbm_achieved_gbs": hbm_gbs,
+                 "hbm_frac": hbm_gbs / hbm_peak})
+    return roof
+
+
+# The specification's configurations, one bench line each in ``per_config``.
+PER_CONFIG = [("C1", "tiny_d64"), ("C2", "seq1k_d64"), ("C2-causal", "seq1k_d64_causal"),
+              ("C3", "seq4k_d128_causal"), ("C4", "seq16k_d128_causal"),
+              ("C5", "cross_q500_k8191_d128")]
+
+
+def measure_config(fa, w, dev, stream, peaks, peak_src, seconds, no_clocks):
+    """One configuration timed over at least ``seconds`` of back-to-back launches (one CUDA
+    event pair on the launching stream), with the clocks sampled inside that window."""
+    import torch
+    setup = ForwardSetup(fa, w, dev, stream)
+    for i in range(5):
+        setup.launch(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(20):
+        setup.launch(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = max(e0.elapsed_time(e1) / 20, 1e-3)
+    steps = int(min(200000, max(50, math.ceil(seconds * 1000.0 / est_ms))))
+    # Host cost of one launch (the C call and its argument checks), over fewer launches
+    # than the stream's queue holds, so the host never waits for the GPU here.
+    torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
+    for i in range(100):
+        setup.launch(i)
+    host_us = (time.perf_counter() - h0) / 100 * 1e6
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index)
+    if not no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(steps):
+        setup.launch(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if not no_clocks:
+        time.sleep(0.15)
+        sampler.stop()
+    clocks = None if no_clocks else sampler.summary(t0, t1)
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"{w.name}: {fa.fa_status_string(st)}")
+    total_ms = e0.elapsed_time(e1)
+    per_launch_s = total_ms / steps / 1e3
+    flops = setup.flops()
+    entry = {"workload": w.name, "shape": w.describe(), "steps": steps,
+             "ms_per_step": total_ms / steps, "tflops": flops / per_launch_s / 1e12,
+             "us_per_step": total_ms / steps * 1e3, "host_us_per_launch": host_us,
+             "schedule": ("split key ranges" if setup.ws_bytes else "whole units"),
+             "roofline": roofline_of(setup, flops, per_launch_s, peaks, peak_src,
+                                     measured_traffic(w.name), sustained=True),
+             "clocks": clocks}
+    if host_us > 0.5 * total_ms / steps * 1e3:
+        # The host's launch rate may limit the stream: replay the same launches from a CUDA
+        # graph (captured once; no host work per launch) for the device-limited figure.
+        entry["graph"] = graph_replay(setup, stream, flops, seconds / 2, est_ms)
+    setup.free()
+    return entry
+
+
+def graph_replay(setup, stream, flops, seconds, est_ms):
+    import torch
+    n = 20
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(setup.dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            setup.stream = side
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    setup.launch(i)
+    except RuntimeError as e:
+        return {"error": str(e)[:200]}
+    finally:
+        setup.stream = stream
+    stream.wait_stream(side)
+    reps = int(max(10, math.ceil(seconds * 1000.0 / (n * est_ms))))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(setup.dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(torch.cuda.current_stream(setup.dev))
+    for _ in range(reps):
+        g.replay()
+    e1.record(torch.cuda.current_stream(setup.dev))
+    torch.cuda.synchronize(setup.dev)
+    per_step_ms = e0.elapsed_time(e1) / (reps * n)
+    return {"steps": reps * n, "us_per_step": per_step_ms * 1e3,
+            "tflops": flops / (per_step_ms / 1e3) / 1e12,
+            "how": f"{n} launches captured once in a CUDA graph, replayed {reps} times"}
+
+
 def run_ours(args, w):
     import torch
     import exact_attention_60_gb300 as fa
@@ -277,67 +523,11 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-
-    q_h, k_h, v_h = make_workload_inputs(w)
-    # Variants of the same workload (fa_fwd_strided): fp16 values, Q/K/V read in place
-    # from [B, L, H, D] memory, per-batch key padding.
-    variant = args.dtype != "bf16" or args.layout != "bhld" or args.kv_pad > 0
-    io_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
-    if args.dtype == "fp16":
-        q_h, k_h, v_h = (t.to(torch.float16) for t in (q_h, k_h, v_h))
-    kv_len_h = None
-    if args.kv_pad > 0:
-        g = np.random.default_rng(0xCAFE + w.index)
-        lo = max(1, int(round(w.Lk * (1.0 - 2.0 * args.kv_pad))))
-        kv_len_h = g.integers(lo, w.Lk + 1, size=w.B).astype(np.int32)
-    in_bytes = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
-    out_bytes = q_h.numel() * 2 + w.B * w.H * w.Lq * 4
-    n_copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)) + 1)
-    bufs = []
-
-    def place(t):   # [B, H, L, D] values, stored [B, L, H, D] with --layout bshd
-        t = t.to(dev)
-        return t.transpose(1, 2).contiguous().transpose(1, 2) if args.layout == "bshd" else t
-
-    base = tuple(place(t) for t in (q_h, k_h, v_h))
-    for c in range(n_copies):
-        qkv = base if c == 0 else tuple(place(t) for t in (q_h, k_h, v_h))
-        o = torch.empty((w.B, w.H, w.Lq, w.D), device=dev, dtype=io_dtype)
-        lse = torch.empty((w.B, w.H, w.Lq), device=dev, dtype=torch.float32)
-        bufs.append((*qkv, o, lse))
-    kv_len = torch.from_numpy(kv_len_h).to(dev) if kv_len_h is not None else None
-    torch.cuda.synchronize(dev)
-
-    # Workspace for the split-key schedule, allocated once outside the timed region
-    # (zero bytes, and plain fa_fwd semantics, for causal workloads).
-    # Local-window workloads run fa_fwd_window (whole units, no workspace).
-    if w.window is None and kv_len is None:
-        st, ws_bytes = fa.fa_fwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
-        if st != fa.FA_OK:
-            raise RuntimeError(fa.fa_status_string(st))
-    else:
-        ws_bytes = 0
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
-    left, right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
-    code = fa.FA_DTYPE_FP16 if args.dtype == "fp16" else fa.FA_DTYPE_BF16
-
-    def launch(i):
-        q, k, v, o, lse = bufs[i % n_copies]
-        if variant:
-            st = fa.fa_fwd_strided(q, q.stride()[:3], k, k.stride()[:3], v, v.stride()[:3], o,
-                                   o.stride()[:3], lse, kv_len, w.B, w.H, w.Lq, w.Lk, w.D, left,
-                                   right, w.scale, code, ws, ws_bytes, stream)
-        elif w.window is not None:
-            st = fa.fa_fwd_window(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.window[0],
-                                  w.window[1], w.scale, stream)
-        else:
-            st = fa.fa_fwd_ws(q, k, v, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, w.causal, w.scale, ws,
-                              ws_bytes, stream)
-        if st != fa.FA_OK:
-            raise RuntimeError(fa.fa_status_string(st))
+    setup = ForwardSetup(fa, w, dev, stream, args.dtype, args.layout, args.kv_pad)
+    variant = setup.variant
 
     for i in range(args.warmup):
-        launch(i)
+        setup.launch(i)
     torch.cuda.synchronize(dev)
     st = fa.fa_last_device_status(stream)
     if st != fa.FA_OK:
@@ -355,81 +545,89 @@ def run_ours(args, w):
     # attention kernel is the only kernel in the stream, so its mean launch duration is
     # total / K (a split step's combine kernel included).
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    t_begin = time.time()
     ev[0].record(stream)
     for i in range(args.steps):
-        launch(i)
+        setup.launch(i)
     ev[1].record(stream)
     torch.cuda.synchronize(dev)
+    t_end = time.time()
     barrier(dist, dev)
-    clocks = sampler.stop() if not args.no_clocks else None
+    if not args.no_clocks:
+        time.sleep(0.15)
+        sampler.stop()
+    clocks = None if args.no_clocks else sampler.summary(t_begin, t_end)
     total_ms = ev[0].elapsed_time(ev[1])
-    per_launch_ms = [total_ms / args.steps]
     st = fa.fa_last_device_status(stream)
     if st != fa.FA_OK:
         raise RuntimeError(f"timed region reported {fa.fa_status_string(st)}")
     max_ms = reduce_max(dist, total_ms, dev)
-    flops = w.flops()
-    if kv_len_h is not None:   # only the unpadded pairs count
-        i = np.arange(w.Lq, dtype=np.int64)
-        lo = np.zeros_like(i) if left < 0 else np.maximum(0, i - left)
-        hi_band = np.full_like(i, w.Lk - 1) if right < 0 else np.minimum(w.Lk - 1, i + right)
-        pairs = sum(int(np.maximum(0, np.minimum(hi_band, kl - 1) - lo + 1).sum()) for kl in kv_len_h)
-        flops = 4 * w.D * w.H * pairs
+    flops = setup.flops()
     value = aggregate_tflops(world, flops, args.steps, max_ms)
     ms_per_step = max_ms / args.steps
-    kernel_tflops = flops / (statistics.mean(per_launch_ms) / 1e3) / 1e12
+    per_launch_s = total_ms / args.steps / 1e3
+    kernel_tflops = flops / per_launch_s / 1e12
+    q_h, k_h, v_h = setup.host
+    in_bytes, out_bytes, ws_bytes, n_copies = (setup.in_bytes, setup.out_bytes, setup.ws_bytes,
+                                               setup.n_copies)
+    kv_len_h = setup.kv_len_h
+    peaks, peak_src = load_peaks()
+    traffic = measured_traffic(w.name) if not variant else None   # measured on bf16, [B,H,L,D]
+    roofline = roofline_of(setup, flops, per_launch_s, peaks, peak_src, traffic)
+    peak = roofline["peak"] if roofline["bound"] == "tensor" else peak_value(
+        peaks, "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    setup.free()
 
-    # ---------------- end to end: pinned host buffers through the public call
+    # ---------------- end to end: pinned host buffers through the C call fa_fwd_host
     e2e = None
     if not args.skip_e2e and not variant:
         q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
         o_p = torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory()
         l_p = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32).pin_memory()
+        left, right = setup.left, setup.right
+        st, host_ws_bytes = fa.fa_fwd_host_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, left, right)
+        if st != fa.FA_OK:
+            raise RuntimeError(fa.fa_status_string(st))
+        host_ws = torch.empty(max(host_ws_bytes, 256), dtype=torch.uint8, device=dev)   # once
 
         def e2e_step():
-            # the public host-buffer call: uploads, kernels and downloads overlapped by chunk
-            fa.attention_from_host(q_p, k_p, v_p, causal=w.causal, scale=w.scale, out=o_p,
-                                   lse=l_p, device=dev, window=w.window)
+            # uploads, kernels and downloads overlapped by chunks of heads inside the library
+            st = fa.fa_fwd_host(q_p, k_p, v_p, o_p, l_p, w.B, w.H, w.Lq, w.Lk, w.D, left, right,
+                                w.scale, host_ws, host_ws.numel(), stream)
+            if st != fa.FA_OK:
+                raise RuntimeError(fa.fa_status_string(st))
 
+        # The host link alone: one upload of the step's inputs, the floor of an e2e step.
+        scratch = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        flat = [t.view(-1).view(torch.uint8) for t in (q_p, k_p, v_p)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        off = 0
+        e0.record(stream)
+        for t in flat:
+            scratch[off:off + t.numel()].copy_(t, non_blocking=True)
+            off += t.numel()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        upload_ms = e0.elapsed_time(e1)
+        del scratch
         e2e_steps = max(1, min(args.steps, 10))
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize(dev)
         barrier(dist, dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
+        if fa.fa_last_device_status(stream) != fa.FA_OK:
+            raise RuntimeError("e2e steps reported a device error")
         e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
         e2e = {"value": aggregate_tflops(world, flops, e2e_steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-               "ms_per_step": e2e_ms / e2e_steps}
-
-    peaks, peak_src = load_peaks()
-    peak = peak_value(peaks, "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    hbm_peak = peak_value(peaks, "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    traffic = measured_traffic(w.name) if not variant else None   # measured on bf16, [B,H,L,D]
-    # The bound is the roof the workload's algorithmic intensity (flops per algorithmic
-    # byte: Q, K, V read once, O and LSE written once) meets first; both are reported.
-    alg_bytes = w.algorithmic_bytes()
-    if kv_len_h is not None:   # padded keys are never read
-        kv_bytes = 2 * 2 * w.H * w.D * int(kv_len_h.sum())
-        alg_bytes = alg_bytes - 2 * 2 * w.B * w.H * w.Lk * w.D + kv_bytes
-    launch_s = statistics.mean(per_launch_ms) / 1e3
-    hbm_gbs = alg_bytes / launch_s / 1e9
-    tensor_bound = flops / alg_bytes >= peak * 1e12 / (hbm_peak * 1e9)
-    if tensor_bound:
-        roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
-                    "frac": kernel_tflops / peak, "peak_source": f"{peak_src} bf16 dense (burst)"}
-    else:
-        roofline = {"bound": "hbm", "achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": hbm_gbs / hbm_peak, "peak_source": f"{peak_src} HBM copy"}
-    roofline.update({"traffic": traffic, "kernel": f"{KERNEL_NAME}<{w.D}>",
-                     "algorithmic_bytes": alg_bytes, "flops_per_byte": flops / alg_bytes,
-                     "tensor_frac": kernel_tflops / peak, "hbm_achieved_gbs": hbm_gbs,
-                     "hbm_frac": hbm_gbs / hbm_peak})
+               "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+               "call": "fa_fwd_host (C ABI, pinned host buffers, device workspace allocated once)",
+               "upload_only_ms": upload_ms, "upload_gbs": in_bytes / upload_ms / 1e6}
 
     cpu = None
     if rank == 0 and not args.skip_cpu_baseline:
@@ -437,6 +635,13 @@ def run_ours(args, w):
         cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n} query rows sampled uniformly from 2 heads of {w.name}, "
                          f"{t:.1f} s of fp64 oracle time"}
+
+    per_config = None
+    if rank == 0 and not args.skip_per_config and not variant:
+        per_config = {}
+        for label, name in PER_CONFIG:
+            per_config[label] = measure_config(fa, WORKLOADS[name], dev, stream, peaks, peak_src,
+                                               args.per_config_seconds, args.no_clocks)
 
     if rank == 0:
         line = {
@@ -455,7 +660,7 @@ def run_ours(args, w):
                        "workspace_bytes": ws_bytes},
             "pct_of_peak": 100.0 * kernel_tflops / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps, "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -552,13 +757,18 @@ def run_backward(args, w):
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    t_begin = time.time()
     ev[0].record(stream)
     for i in range(args.steps):
         launch(i)
     ev[1].record(stream)
     torch.cuda.synchronize(dev)
+    t_end = time.time()
     barrier(dist, dev)
-    clocks = sampler.stop() if not args.no_clocks else None
+    if not args.no_clocks:
+        time.sleep(0.15)
+        sampler.stop()
+    clocks = None if args.no_clocks else sampler.summary(t_begin, t_end)
     if fa.fa_last_device_status(stream) != fa.FA_OK:
         raise RuntimeError("timed region reported a device error")
     max_ms = reduce_max(dist, ev[0].elapsed_time(ev[1]), dev)
@@ -618,6 +828,9 @@ def main(argv=None):
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-per-config", action="store_true",
+                    help="skip the per-configuration lines (each timed over >= --per-config-seconds)")
+    ap.add_argument("--per-config-seconds", type=float, default=1.0)
     ap.add_argument("--ref-seconds-per-step", type=float, default=5.0)
     ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
                     help="forward (the headline metric) or backward (fa_bwd)")

@@ -10,8 +10,9 @@ import math
 from ._native import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,
                       FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, fa_bwd, fa_bwd_masked,
                       fa_bwd_strided, fa_bwd_workspace_size,
-                      fa_debug_set, fa_fwd, fa_fwd_noalloc, fa_fwd_strided, fa_fwd_window,
-                      fa_fwd_workspace_size, fa_fwd_ws, fa_last_device_status, fa_status_string)
+                      fa_debug_set, fa_fwd, fa_fwd_host, fa_fwd_host_workspace_size,
+                      fa_fwd_noalloc, fa_fwd_strided, fa_fwd_window, fa_fwd_workspace_size,
+                      fa_fwd_ws, fa_last_device_status, fa_status_string)
 
 
 class FaError(RuntimeError):
@@ -199,72 +200,56 @@ def flash_attention(q, k, v, causal: bool = False, scale: float | None = None, w
     return _Fn.apply(q, k, v)
 
 
+_host_workspaces = {}
+
+
 def attention_from_host(q, k, v, causal: bool = False, scale: float | None = None, out=None,
-                        lse=None, chunks: int | None = None, device=None, window=None):
-    """Exact attention of host tensors: copies in, computes, copies out, overlapped.
+                        lse=None, device=None, window=None, stream=None):
+    """Exact attention of host tensors through the C call fa_fwd_host.
 
     ``q`` [B,H,Lq,D], ``k``/``v`` [B,H,Lk,D] are contiguous bf16 CPU tensors (pinned for
-    the copies to overlap).  The (batch, head) slices are cut into ``chunks`` groups;
-    group i+1 travels to the GPU while group i is computed and group i-1 travels back,
-    on three streams ordered by events.  Returns host ``out`` (bf16) and ``lse`` (fp32),
-    allocated pinned if not given.  Device buffers are allocated per call.  ``window``
-    as for ``attention``.
+    the copies to overlap the kernels).  The library cuts the (batch, head) slices into
+    chunks and overlaps their uploads, kernels and downloads on three streams.  Returns
+    host ``out`` (bf16) and ``lse`` (fp32), allocated pinned if not given, complete once
+    ``stream`` (default: the device's current stream) has finished.  The device
+    workspace is cached per device, so calls on one device must be ordered on one
+    stream.  ``window`` as for ``attention``.
     """
     import torch
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
-    BH = B * H
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CPU tensors [B, H, L, D]")
+    if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
+        raise ValueError("k and v must be [B, H, Lk, D] matching q")
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
     if lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32).pin_memory()
-    if chunks is None:
-        chunks = default_chunks(BH, Lq, Lk, causal)
-    chunks = max(1, min(int(chunks), BH))
-    dq = torch.empty((BH, Lq, D), dtype=torch.bfloat16, device=dev)
-    dk = torch.empty((BH, Lk, D), dtype=torch.bfloat16, device=dev)
-    dv = torch.empty((BH, Lk, D), dtype=torch.bfloat16, device=dev)
-    do = torch.empty((BH, Lq, D), dtype=torch.bfloat16, device=dev)
-    dl = torch.empty((BH, Lq), dtype=torch.float32, device=dev)
-    hq, hk, hv = q.reshape(BH, Lq, D), k.reshape(BH, Lk, D), v.reshape(BH, Lk, D)
-    ho, hl = out.view(BH, Lq, D), lse.view(BH, Lq)
-    main = torch.cuda.current_stream(dev)
-    # uploads on one stream (parallel upload streams measured slower: they make the
-    # first chunk's tensors arrive later), kernels on a second, downloads on a third
-    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    for s in (s_in, s_cmp, s_out):
-        s.wait_stream(main)
-    bounds = [(BH * i // chunks, BH * (i + 1) // chunks) for i in range(chunks)]
-    for a, b in bounds:
-        if a == b:
-            continue
-        with torch.cuda.stream(s_in):
-            dq[a:b].copy_(hq[a:b], non_blocking=True)
-            dk[a:b].copy_(hk[a:b], non_blocking=True)
-            dv[a:b].copy_(hv[a:b], non_blocking=True)
-        s_cmp.wait_stream(s_in)
-        with torch.cuda.stream(s_cmp):
-            n = b - a
-            attention(dq[a:b].view(1, n, Lq, D), dk[a:b].view(1, n, Lk, D), dv[a:b].view(1, n, Lk, D),
-                      causal=causal, scale=scale, out=do[a:b].view(1, n, Lq, D),
-                      lse=dl[a:b].view(1, n, Lq), stream=s_cmp, window=window)
-        s_out.wait_stream(s_cmp)
-        with torch.cuda.stream(s_out):
-            ho[a:b].copy_(do[a:b], non_blocking=True)
-            hl[a:b].copy_(dl[a:b], non_blocking=True)
-    main.wait_stream(s_out)
-    for t in (dq, dk, dv, do, dl):
-        for s in (s_in, s_cmp, s_out):
-            t.record_stream(s)
+    if (out.dtype != torch.bfloat16 or out.is_cuda or tuple(out.shape) != tuple(q.shape)
+            or not out.is_contiguous() or lse.dtype != torch.float32 or lse.is_cuda
+            or tuple(lse.shape) != (B, H, Lq) or not lse.is_contiguous()):
+        raise ValueError("out and lse must be contiguous CPU tensors: bf16 like q, fp32 [B, H, Lq]")
+    if window is None:
+        left, right = -1, (0 if causal else -1)
+    else:
+        left, right = int(window[0]), (0 if causal else int(window[1]))
+    with torch.cuda.device(dev):
+        st, nbytes = fa_fwd_host_workspace_size(B, H, Lq, Lk, D, left, right)
+        if st != FA_OK:
+            raise FaError(st)
+        ws = _host_workspaces.get(dev.index)
+        if ws is None or ws.numel() < max(nbytes, 256):
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+            _host_workspaces[dev.index] = ws
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        st = fa_fwd_host(q, k, v, out, lse, B, H, Lq, Lk, D, left, right, scale, ws, ws.numel(),
+                         stream)
+    if st != FA_OK:
+        raise FaError(st)
     return out, lse
-
-
-def default_chunks(BH: int, Lq: int, Lk: int, causal: bool) -> int:
-    """Chunks for attention_from_host: enough to overlap the copies with the kernels,
-    few enough that each kernel still spreads over the GPU (at least 256 query-tile
-    pairs per chunk, at most 8 chunks)."""
-    units = BH * ((Lq + 255) // 256)
-    return max(1, min(8, units // 256, BH))

@@ -21,7 +21,7 @@ FA_DTYPE_FP16 = 1
 
 # Every symbol include/fa.h declares.
 EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_strided",
-            "fa_fwd_noalloc",
+            "fa_fwd_noalloc", "fa_fwd_host_workspace_size", "fa_fwd_host",
             "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_masked", "fa_bwd_strided", "fa_status_string",
             "fa_last_device_status",
             "fa_debug_set")
@@ -57,6 +57,11 @@ def load(path: str = LIB) -> ctypes.CDLL:
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
+    lib.fa_fwd_host_workspace_size.restype = ctypes.c_int
+    lib.fa_fwd_host_workspace_size.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_fwd_host.restype = ctypes.c_int
+    lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 7 + [ctypes.c_float, vp,
+                                                                          ctypes.c_size_t, vp]
     lib.fa_bwd_workspace_size.restype = ctypes.c_int
     lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_bwd.restype = ctypes.c_int
@@ -152,6 +157,24 @@ def fa_fwd_noalloc(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, stream=None)
     return load().fa_fwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
                                  int(Lq), int(Lk), int(D), int(bool(causal)), float(scale),
                                  _stream(stream))
+
+
+def fa_fwd_host_workspace_size(B, H, Lq, Lk, D, window_left, window_right):
+    """C ``fa_fwd_host_workspace_size``: returns (status, bytes)."""
+    n = ctypes.c_size_t(0)
+    st = load().fa_fwd_host_workspace_size(int(B), int(H), int(Lq), int(Lk), int(D),
+                                           int(window_left), int(window_right), ctypes.byref(n))
+    return st, int(n.value)
+
+
+def fa_fwd_host(Q, K, V, O, LSE, B, H, Lq, Lk, D, window_left, window_right, scale, workspace,
+                workspace_bytes, stream=None) -> int:
+    """C ``fa_fwd_host``: Q, K, V, O, LSE are HOST pointers (ints or CPU tensors, pinned for
+    overlap); ``workspace`` is device memory of fa_fwd_host_workspace_size bytes."""
+    return load().fa_fwd_host(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), int(B), int(H),
+                              int(Lq), int(Lk), int(D), int(window_left), int(window_right),
+                              float(scale), _ptr(workspace), int(workspace_bytes),
+                              _stream(stream))
 
 
 def fa_bwd_workspace_size(B, H, Lq, Lk, D, causal):

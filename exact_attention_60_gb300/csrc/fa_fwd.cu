@@ -1298,7 +1298,11 @@ Plan plan_schedule(const Problem& pr, int sm_count) {
   return pl;
 }
 
-fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cudaStream_t stream) {
+// allow_dependent = false keeps the kernel from starting before the operation ahead of it
+// in the stream has completed (needed when that operation is an event wait, which a
+// programmatic dependent launch does not order).
+fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cudaStream_t stream,
+                 bool allow_dependent = true) {
   Params p;
   if (!encode_map(&p.tm_q, pr.Q, pr.B, pr.H, pr.Lq, pr.D, pr.qs, pr.f16) ||
       !encode_map(&p.tm_k, pr.K, pr.B, pr.H, pr.Lk, pr.D, pr.ks, pr.f16) ||
@@ -1358,7 +1362,7 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
       static_cast<long long>(pr.n_units) * pr.nkv / std::max(1, pl.grid);
   const bool dependent_launch = steps_per_cta <= 256;
   cfg.attrs = attr;
-  cfg.numAttrs = dependent_launch ? 1 : 0;
+  cfg.numAttrs = (dependent_launch && allow_dependent) ? 1 : 0;
   const int sched = pl.band ? fa::kSchedBand : pl.split ? fa::kSchedSplit : fa::kSchedWhole;
   cudaError_t err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched, pr.f16), p);
   if (err != cudaSuccess) return FA_ERR_CUDA;
@@ -1664,6 +1668,265 @@ extern "C" fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V,
   const fa_status sa = scratch_address(dev, &scratch);
   if (sa != FA_OK) return sa;
   return launch(pr, sm_count, pl, scratch, stream);
+}
+
+// ---------------------------------------------------------------- host-buffer entry point
+// fa_fwd_host: Q, K, V in host memory, O and LSE back to host memory, with the copies and
+// the kernels overlapped.  The (batch, head) slices are cut into chunks of whole heads;
+// chunk c travels to the GPU on an upload stream while chunk c-1 is computed on the
+// caller's stream and chunk c-2 travels back on a download stream, ordered by events.
+// Every device buffer lives in the caller's workspace, so the call allocates nothing.
+namespace {
+
+constexpr int kHostMaxChunks = 8;
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t up = nullptr;
+  cudaStream_t down = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t end = nullptr;
+  cudaEvent_t up_done[kHostMaxChunks] = {};
+  cudaEvent_t cmp_done[kHostMaxChunks] = {};
+};
+
+std::mutex g_host_mutex[kMaxDevices];
+HostPipe g_host_pipe[kMaxDevices];
+
+// The device's upload/download streams and events, created on first use (the device's
+// mutex must be held).
+fa_status host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_host_pipe[dev];
+  if (!hp.ready) {
+    bool ok = cudaStreamCreateWithFlags(&hp.up, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; ok && c < kHostMaxChunks; ++c)
+      ok = cudaEventCreateWithFlags(&hp.up_done[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.cmp_done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      if (hp.up) cudaStreamDestroy(hp.up);
+      if (hp.down) cudaStreamDestroy(hp.down);
+      for (cudaEvent_t e : {hp.start, hp.end}) if (e) cudaEventDestroy(e);
+      for (int c = 0; c < kHostMaxChunks; ++c) {
+        if (hp.up_done[c]) cudaEventDestroy(hp.up_done[c]);
+        if (hp.cmp_done[c]) cudaEventDestroy(hp.cmp_done[c]);
+      }
+      hp = HostPipe{};
+      return FA_ERR_CUDA;
+    }
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+// A validated host-buffer problem and the layout of its device workspace.
+struct HostPlan {
+  Problem pr;          // sizes, mask and scale; the pointers are the caller's host buffers
+  int chunks = 1;
+  size_t off_q = 0, off_k = 0, off_v = 0, off_o = 0, off_lse = 0, off_split = 0;
+  size_t split_bytes = 0;
+  size_t total = 0;
+};
+
+// Heads of chunk c: [bh * c / chunks, bh * (c + 1) / chunks).
+long long chunk_lo(const HostPlan& hp, int c) { return hp.pr.bh * c / hp.chunks; }
+
+// The chunk of heads [a, b) as a problem of its own: B = 1, H = b - a, on the workspace copies.
+Problem chunk_problem(const HostPlan& hp, uint8_t* ws, long long a, long long b) {
+  Problem c = hp.pr;
+  const long long n = b - a;
+  const size_t q_row = static_cast<size_t>(hp.pr.Lq) * hp.pr.D * 2;
+  const size_t k_row = static_cast<size_t>(hp.pr.Lk) * hp.pr.D * 2;
+  c.Q = ws ? ws + hp.off_q + a * q_row : nullptr;
+  c.K = ws ? ws + hp.off_k + a * k_row : nullptr;
+  c.V = ws ? ws + hp.off_v + a * k_row : nullptr;
+  c.O = ws ? ws + hp.off_o + a * q_row : nullptr;
+  c.LSE = ws ? reinterpret_cast<float*>(ws + hp.off_lse) + a * hp.pr.Lq : nullptr;
+  c.B = 1;
+  c.H = static_cast<int>(n);
+  c.bh = n;
+  c.n_units = static_cast<int>(n * hp.pr.n_pairs);
+  c.bytes_q = n * q_row;
+  c.bytes_k = n * k_row;
+  c.bytes_lse = static_cast<size_t>(n) * hp.pr.Lq * 4;
+  contiguous_strides(c.H, c.Lq, c.D, c.qs);
+  contiguous_strides(c.H, c.Lk, c.D, c.ks);
+  contiguous_strides(c.H, c.Lk, c.D, c.vs);
+  contiguous_strides(c.H, c.Lq, c.D, c.os);
+  return c;
+}
+
+// Checks the arguments of fa_fwd_host / fa_fwd_host_workspace_size and lays out the
+// workspace.  *empty = true: nothing to compute.
+fa_status host_plan(int B, int H, int Lq, int Lk, int D, int window_left, int window_right,
+                    float scale, bool check_scale, HostPlan* hp, int* sm_count, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * Lq == 0) {
+    *empty = true;
+    return FA_OK;
+  }
+  if (Lk < 1) return FA_ERR_INVALID_ARG;
+  if (check_scale && (!(scale > 0.0f) || !isfinite(scale))) return FA_ERR_INVALID_ARG;
+  const long long n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  if (bh > INT_MAX || n_pairs * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  if (bh * Lq * D > (1ll << 40) || bh * Lk * D > (1ll << 40)) return FA_ERR_INVALID_ARG;
+  int left = window_left, right = window_right;
+  if (left >= Lq - 1) left = -1;
+  if (right >= Lk - 1) right = -1;
+  if (left >= 0 && Lq - 1 - left > Lk - 1) return FA_ERR_INVALID_ARG;   // a row without keys
+  const fa_status prep = current_device(D, sm_count);
+  if (prep != FA_OK) return prep;
+
+  Problem& pr = hp->pr;
+  pr = Problem{};
+  pr.Lq = Lq;
+  pr.Lk = Lk;
+  pr.D = D;
+  pr.scale = scale;
+  pr.bh = bh;
+  pr.n_pairs = static_cast<int>(n_pairs);
+  pr.n_units = static_cast<int>(n_pairs * bh);
+  pr.nkv = (Lk + fa::kBlockN - 1) / fa::kBlockN;
+  pr.B = B;
+  pr.H = H;
+  if (left < 0 && (right < 0 || right == 0)) {
+    pr.causal = right == 0 ? 1 : 0;   // the full or the causal mask: whole units or split
+  } else {
+    pr.band = true;
+    pr.win_left = left;
+    pr.win_right = right;
+  }
+  // Chunks: enough to overlap the copies with the kernels, few enough that each chunk's
+  // kernel still spreads over the GPU (at least 256 query-tile pairs per chunk).  Test
+  // hook (fa_debug_set bit 3): as many chunks as there are heads, up to the maximum.
+  const long long chunks = (g_debug_flags.load() & 8u)
+                               ? std::min<long long>(kHostMaxChunks, bh)
+                               : std::min<long long>({kHostMaxChunks, pr.n_units / 256, bh});
+  hp->chunks = static_cast<int>(std::max<long long>(1, chunks));
+  pr.bytes_q = static_cast<size_t>(bh) * Lq * D * 2;
+  pr.bytes_k = static_cast<size_t>(bh) * Lk * D * 2;
+  pr.bytes_lse = static_cast<size_t>(bh) * Lq * 4;
+  hp->off_q = 0;
+  hp->off_k = hp->off_q + round256(pr.bytes_q);
+  hp->off_v = hp->off_k + round256(pr.bytes_k);
+  hp->off_o = hp->off_v + round256(pr.bytes_k);
+  hp->off_lse = hp->off_o + round256(pr.bytes_q);
+  hp->off_split = hp->off_lse + round256(pr.bytes_lse);
+  hp->split_bytes = 0;
+  if (!pr.band) {   // the largest split-schedule workspace any chunk needs
+    for (int c = 0; c < hp->chunks; ++c) {
+      const Problem cp = chunk_problem(*hp, nullptr, chunk_lo(*hp, c), chunk_lo(*hp, c + 1));
+      const Plan pl = plan_schedule(cp, *sm_count);
+      if (pl.split) hp->split_bytes = std::max(hp->split_bytes, pl.ws_bytes);
+    }
+  }
+  hp->total = hp->off_split + hp->split_bytes;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_host_workspace_size(int B, int H, int Lq, int Lk, int D,
+                                                int window_left, int window_right, size_t* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  HostPlan hp;
+  int sm_count = 0;
+  bool empty = false;
+  const fa_status st = host_plan(B, H, Lq, Lk, D, window_left, window_right, 0.0f, false, &hp,
+                                 &sm_count, &empty);
+  if (st != FA_OK || empty) return st;
+  *bytes = hp.total;
+  return FA_OK;
+}
+
+extern "C" fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 int B, int H, int Lq, int Lk, int D, int window_left,
+                                 int window_right, float scale, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  HostPlan hp;
+  int sm_count = 0;
+  bool empty = false;
+  const fa_status st = host_plan(B, H, Lq, Lk, D, window_left, window_right, scale, true, &hp,
+                                 &sm_count, &empty);
+  if (st != FA_OK || empty) return st;
+  const Problem& pr = hp.pr;
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  // O and LSE are written while later chunks of Q, K, V are still being read.
+  if (overlaps(O, pr.bytes_q, Q, pr.bytes_q) || overlaps(O, pr.bytes_q, K, pr.bytes_k) ||
+      overlaps(O, pr.bytes_q, V, pr.bytes_k) || overlaps(O, pr.bytes_q, LSE, pr.bytes_lse) ||
+      overlaps(LSE, pr.bytes_lse, Q, pr.bytes_q) || overlaps(LSE, pr.bytes_lse, K, pr.bytes_k) ||
+      overlaps(LSE, pr.bytes_lse, V, pr.bytes_k))
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < hp.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_INVALID_ARG;
+  const void* host[5] = {Q, K, V, O, LSE};
+  const size_t host_bytes[5] = {pr.bytes_q, pr.bytes_k, pr.bytes_k, pr.bytes_q, pr.bytes_lse};
+  for (int i = 0; i < 5; ++i)
+    if (overlaps(workspace, hp.total, host[i], host_bytes[i])) return FA_ERR_INVALID_ARG;
+  if (g_debug_flags.load() & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_host_mutex[dev]);
+  HostPipe* pipe = nullptr;
+  const fa_status ps = host_pipe(dev, &pipe);
+  if (ps != FA_OK) return ps;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* hq = static_cast<const uint8_t*>(Q);
+  const uint8_t* hk = static_cast<const uint8_t*>(K);
+  const uint8_t* hv = static_cast<const uint8_t*>(V);
+  uint8_t* ho = static_cast<uint8_t*>(O);
+  const size_t q_row = static_cast<size_t>(pr.Lq) * pr.D * 2;
+  const size_t k_row = static_cast<size_t>(pr.Lk) * pr.D * 2;
+  const size_t l_row = static_cast<size_t>(pr.Lq) * 4;
+  // The copies start after the work queued on `stream` so far (the caller may still be
+  // producing the inputs or using the outputs there).
+  if (cudaEventRecord(pipe->start, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(pipe->up, pipe->start, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  auto copy = [](void* dst, const void* src, size_t n, cudaStream_t s) {
+    return cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, s) == cudaSuccess;
+  };
+  for (int c = 0; c < hp.chunks; ++c) {
+    const long long a = chunk_lo(hp, c), b = chunk_lo(hp, c + 1);
+    const size_t n = static_cast<size_t>(b - a);
+    if (!copy(ws + hp.off_q + a * q_row, hq + a * q_row, n * q_row, pipe->up) ||
+        !copy(ws + hp.off_k + a * k_row, hk + a * k_row, n * k_row, pipe->up) ||
+        !copy(ws + hp.off_v + a * k_row, hv + a * k_row, n * k_row, pipe->up) ||
+        cudaEventRecord(pipe->up_done[c], pipe->up) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, pipe->up_done[c], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    const Problem cp = chunk_problem(hp, ws, a, b);
+    Plan pl{};
+    if (cp.band) {
+      pl.band = true;
+      pl.grid = std::min(cp.n_units, sm_count);
+    } else {
+      pl = plan_schedule(cp, sm_count);
+    }
+    // Not a programmatic dependent launch: the operation ahead of it is the event wait.
+    const fa_status ls = launch(cp, sm_count, pl, pl.split ? ws + hp.off_split : nullptr, stream,
+                                /*allow_dependent=*/false);
+    if (ls != FA_OK) return ls;
+    if (cudaEventRecord(pipe->cmp_done[c], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(pipe->down, pipe->cmp_done[c], 0) != cudaSuccess ||
+        !copy(ho + a * q_row, ws + hp.off_o + a * q_row, n * q_row, pipe->down) ||
+        !copy(LSE + a * pr.Lq, ws + hp.off_lse + a * l_row, n * l_row, pipe->down))
+      return FA_ERR_CUDA;
+  }
+  // `stream` completes only after the last download.
+  if (cudaEventRecord(pipe->end, pipe->down) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, pipe->end, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 extern "C" const char* fa_status_string(fa_status s) {

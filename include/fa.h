@@ -222,6 +222,64 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, f
                          cudaStream_t stream);
 
 /*
+ * fa_fwd_host_workspace_size -- device workspace that fa_fwd_host needs for this
+ * problem on the current device, in *bytes (0 when B*H*Lq == 0): room for device
+ * copies of Q, K, V, O and LSE (each rounded up to 256 bytes) followed by the split
+ * schedule's workspace of the largest chunk that uses it (see fa_fwd_ws).
+ * window_left / window_right as for fa_fwd_host.  Returns the argument errors of
+ * fa_fwd_host that depend on sizes alone, FA_ERR_INVALID_ARG for bytes == NULL, and
+ * FA_ERR_CUDA if the device cannot be queried.
+ */
+fa_status fa_fwd_host_workspace_size(int B, int H, int Lq, int Lk, int D, int window_left,
+                                     int window_right, size_t* bytes);
+
+/*
+ * fa_fwd_host -- the forward pass on HOST buffers: Q, K, V are read from host memory,
+ * O and LSE are written to host memory.  This is the host wrapper of the wsisp.com
+ * post "FlashAttention-2 forward in Triton" (it takes the tensors, allocates O and
+ * the per-row statistic M, runs the kernel and returns O) for callers whose tensors
+ * live on the host, with the transfers made part of the call.
+ *
+ *   Q, K, V : host pointers, bf16, contiguous [B,H,Lq,D] / [B,H,Lk,D] / [B,H,Lk,D];
+ *             only read.  Any alignment.
+ *   O       : host pointer, bf16 [B,H,Lq,D], written;  LSE : host pointer, fp32
+ *             [B,H,Lq], written.  O and LSE must not overlap Q, K, V or each other.
+ *             Page-locked host memory (cudaHostAlloc / cudaHostRegister) lets the
+ *             copies run asynchronously and overlap the kernels; pageable memory also
+ *             works, with the copies then serialised by the CUDA runtime.
+ *   window_left, window_right : the band of fa_fwd_window; (-1, -1) is the full
+ *             softmax (fa_fwd with causal = 0, split schedule included) and (-1, 0)
+ *             the causal mask (fa_fwd with causal != 0).
+ *   workspace, workspace_bytes : DEVICE memory on the current device, 256-byte aligned,
+ *             at least fa_fwd_host_workspace_size bytes, overlapping none of the host
+ *             buffers; contents on entry do not matter, left as scratch (it holds the
+ *             device copies of all five tensors).  Calls sharing a workspace must not
+ *             run concurrently.
+ *   B, H, Lq, Lk, D, scale : as fa_fwd.
+ *   stream  : the call is ordered after the work already queued on `stream`, and
+ *             `stream` completes only once O and LSE are in host memory.
+ *
+ * How it runs: the B*H (batch, head) slices are cut into up to 8 chunks of whole heads
+ * (each large enough to keep the GPU busy).  Chunk c's Q, K, V travel to the device on
+ * an internal upload stream while chunk c-1 is computed on `stream` (the kernels of
+ * fa_fwd_ws / fa_fwd_window) and chunk c-2's O and LSE travel back on an internal
+ * download stream; events order the three.  One cudaMemcpyAsync per tensor and chunk.
+ * The call allocates no device memory; the two internal streams and their events are
+ * created on the first call on each device and kept until the process exits.
+ *
+ * Asynchronous: the call returns once everything is queued; the host buffers must stay
+ * valid and unmodified (Q, K, V) and unread (O, LSE) until `stream` has completed
+ * (cudaStreamSynchronize).  Calls from several host threads are safe: each holds a
+ * per-device lock while it queues its work.  B*H*Lq == 0 returns FA_OK with nothing
+ * queued.  Argument errors are returned before anything is queued; FA_ERR_CUDA from a
+ * failed copy or launch may leave part of the work queued (O and LSE are then
+ * undefined).  Pipeline-wait timeouts are reported by fa_last_device_status().
+ */
+fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                      int B, int H, int Lq, int Lk, int D, int window_left, int window_right,
+                      float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_bwd_workspace_size -- device workspace fa_bwd needs, in *bytes: two fp32 arrays
  * (Delta_i = dO_i.O_i and LSE_i * log2(e)) over the query rows padded to whole
  * 128-row tiles, B*H*ceil(Lq/128)*128 entries each, each rounded up to 256 bytes, then
@@ -318,7 +376,9 @@ fa_status fa_last_device_status(cudaStream_t stream);
  * instead of completing.  Bit 1 makes every
  * launch fail with FA_ERR_CUDA before anything is queued.  Bit 2 makes
  * fa_fwd_window run its band kernel also for the bands (-1, 0) and (-1, -1), so
- * that it can be compared with fa_fwd's kernels.  Not for production use;
+ * that it can be compared with fa_fwd's kernels.  Bit 3 makes fa_fwd_host (and
+ * fa_fwd_host_workspace_size) cut the heads into as many chunks as it can, so that
+ * small problems exercise the overlapped pipeline.  Not for production use;
  * returns FA_OK.
  */
 fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns);

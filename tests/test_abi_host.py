@@ -251,3 +251,26 @@ def test_noalloc_documented_limits_follow_from_the_scratch_size():
     assert stated in " ".join(header.split()), stated
     assert (f"D = 128 on up to {limits[128]} SMs" in src
             and f"at D = 64 on up to {limits[64]} SMs" in src)
+
+
+def test_host_entry_point_rejects_bad_arguments_before_cuda(lib):
+    """fa_fwd_host and its workspace query check sizes, masks and head dimensions before
+    they touch the device."""
+    host = dict(Q=ALIGNED, K=2 * ALIGNED, V=3 * ALIGNED, O=4 * ALIGNED, LSE=5 * ALIGNED)
+
+    def call(B=1, H=1, Lq=16, Lk=16, D=64, left=-1, right=-1, scale=0.125):
+        return fa.fa_fwd_host(host["Q"], host["K"], host["V"], host["O"], host["LSE"], B, H, Lq,
+                              Lk, D, left, right, scale, 6 * ALIGNED, 1 << 20, 0)
+
+    assert call(D=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(B=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(left=-2) == fa.FA_ERR_INVALID_ARG
+    assert call(right=-5) == fa.FA_ERR_INVALID_ARG
+    assert call(Lk=0) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(Lq=300, Lk=100, left=10, right=0) == fa.FA_ERR_INVALID_ARG   # rows without keys
+    assert call(B=0) == fa.FA_OK                                             # nothing to do
+    assert fa.fa_fwd_host_workspace_size(1, 1, 16, 16, 96, -1, -1)[0] == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_host_workspace_size(1, 1, 16, 16, 64, -3, -1)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_host_workspace_size(0, 1, 16, 16, 64, -1, -1) == (fa.FA_OK, 0)
+    assert lib.fa_fwd_host_workspace_size(1, 1, 16, 16, 64, -1, -1, None) == fa.FA_ERR_INVALID_ARG

@@ -98,3 +98,35 @@ def test_peak_lookup():
     peaks, source = bench.load_peaks()
     assert source in ("measured", "fallback")
     assert bench.peak_value(peaks, "bf16_tflops", 0.0) > 0
+
+
+def test_clock_sampler_keeps_samples_inside_the_window():
+    import datetime
+    s = bench.ClockSampler(0)
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    def line(dt_s, mhz, power, cap):
+        t = (base + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{t}, 0, {mhz}, 2070, {power}, 0x0, Not Active, Not Active, Not Active, {cap}"
+    s.lines = [line(0.0, 1000, 200.0, "Not Active"), line(0.5, 1900, 1300.0, "Active"),
+               line(0.6, 1700, 1350.0, "Active"), line(0.7, 1800, 1390.0, "Not Active"),
+               line(2.0, 900, 180.0, "Not Active"), "garbage line"]
+    t0 = (base + datetime.timedelta(seconds=0.45)).timestamp()
+    t1 = (base + datetime.timedelta(seconds=0.75)).timestamp()
+    r = s.summary(t0, t1)
+    assert r["samples_in_window"] == 3 and r["samples"] == 3
+    assert r["sm_mhz"] == 1800 and r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"] and r["power_w_max"] == 1390.0
+    # a window with no sample falls back to every sample, and says so
+    r = s.summary(t1 + 10, t1 + 11)
+    assert r["samples_in_window"] == 0 and r["samples"] == 5
+    assert bench.ClockSampler(0).summary()["error"]
+
+
+def test_per_config_covers_every_specified_configuration():
+    """C1, C2 (both masks), C3, C4 and C5 of the specification, each once."""
+    shapes = {(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
+              for w in (WORKLOADS[name] for _, name in bench.PER_CONFIG)}
+    assert shapes == {(1, 2, 128, 128, 64, False), (4, 16, 1024, 1024, 64, False),
+                      (4, 16, 1024, 1024, 64, True), (2, 32, 4096, 4096, 128, True),
+                      (1, 16, 16384, 16384, 128, True), (8, 16, 500, 8191, 128, False)}
+    assert len(bench.PER_CONFIG) == 6

@@ -285,22 +285,6 @@ def test_workspace_argument_errors():
     assert fa.fa_last_device_status() == fa.FA_OK
 
 
-@pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("chunks", [1, 3, None])
-def test_attention_from_host(oracle_mod, causal, chunks):
-    """Host buffers in and out, copies overlapped with the kernels by chunks of heads."""
-    B, H, Lq, Lk, D = 2, 5, 300, 520, 128
-    q, k, v = make_qkv(B, H, Lq, Lk, D, seed=41)
-    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    o, lse = fa.attention_from_host(qp, kp, vp, causal=causal, chunks=chunks)
-    torch.cuda.synchronize()
-    assert fa.fa_last_device_status() == fa.FA_OK
-    assert o.device.type == "cpu" and lse.device.type == "cpu"
-    ref_o, ref_l = oracle_mod.attn_full(q, k, v, causal, 1.0 / math.sqrt(D))
-    assert np.abs(o.float().numpy() - ref_o).max() <= TOL_O
-    assert np.abs(lse.numpy() - ref_l).max() <= TOL_LSE
-
-
 @pytest.mark.parametrize("shape,kw", [((4, 16, 1024, 1024, 64), dict(causal=True)),          # dependent launches
                                       ((1, 4, 512, 8192, 128), dict(causal=False)),          # split + combine
                                       ((2, 8, 700, 700, 128), dict(window=(100, 0)))])       # band
