@@ -48,6 +48,8 @@
 #include <climits>
 #include <mutex>
 #include <utility>
+#include <vector>
+#include <queue>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -76,7 +78,10 @@ constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // one second per 
 //   kSchedSplit: non-causal key ranges cut across CTAs, merged by fa_combine_kernel.
 //   kSchedBand : local (sliding-window) attention; each query tile covers its own band
 //                of key tiles, and only tiles cut by the band's edges are masked.
-enum Sched : int { kSchedWhole = 0, kSchedSplit = 1, kSchedBand = 2 };
+//   kSchedTable: whole units in an order computed on the host (causal problems whose K/V
+//                outgrow the L2 cache): heads in groups whose K/V fit in L2, each group's
+//                units dealt heaviest first to the least-loaded CTA.
+enum Sched : int { kSchedWhole = 0, kSchedSplit = 1, kSchedBand = 2, kSchedTable = 3 };
 
 enum WaitSite : uint32_t {
   kSiteLoadKV = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteSoftS, kSiteSoftO,
@@ -159,6 +164,17 @@ struct Params {
   unsigned long long wait_limit_ns;
 };
 
+// The host-computed order of kSchedTable, passed with the launch: CTA g takes the units
+// tab_units[tab_off[g] .. tab_off[g + 1]) in that order.
+constexpr int kTabMaxGrid = 256;
+constexpr int kTabMaxUnits = 4096;
+struct TableParams : Params {
+  uint16_t tab_off[kTabMaxGrid + 1];
+  uint32_t tab_units[kTabMaxUnits];   // (bh << 12) | index of the pair of query tiles
+};
+template <int kS> struct ParamsOf { using type = Params; };
+template <> struct ParamsOf<kSchedTable> { using type = TableParams; };
+
 // A unit of work: two consecutive 128-row query tiles of one (batch, head).
 // Units are numbered heaviest first (causal: the last query tiles attend to the
 // most keys); a CTA takes units in boustrophedon order over the grid (round r:
@@ -210,11 +226,27 @@ __device__ __forceinline__ int band_lim(const Params& p, int q, int kvl) {
                                     static_cast<long long>(q) + p.win_right + 1));
 }
 
-template <int kS>
-__device__ __forceinline__ bool unit_of(const Params& p, int r, Unit& u) {
+template <int kS, class P>
+__device__ __forceinline__ bool unit_of(const P& p, int r, Unit& u) {
   const int G = static_cast<int>(gridDim.x);
   const int g = static_cast<int>(blockIdx.x);
-  if constexpr (kS == kSchedBand) {
+  if constexpr (kS == kSchedTable) {
+    const int e = p.tab_off[g] + r;
+    if (e >= p.tab_off[g + 1]) return false;
+    const uint32_t t = p.tab_units[e];
+    u.bh = static_cast<int>(t >> 12);
+    u.q0 = static_cast<int>(t & 0xfffu) * 2 * kBlockM;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int qi = u.q0 + i * kBlockM;
+      u.nblk[i] = (qi >= p.Lq) ? 0 : (p.causal ? min(p.nkv, qi / kBlockN + 1) : p.nkv);
+    }
+    u.nmax = max(u.nblk[0], u.nblk[1]);
+    u.kv0 = 0;
+    u.first[0] = u.first[1] = 0;
+    u.partial = 0;
+    return true;
+  } else if constexpr (kS == kSchedBand) {
     // Units in the order that puts the heaviest first: descending query order
     // when the band is bounded on the right or open on the left (the last tiles
     // see the most keys), ascending when only the left side is bounded.
@@ -366,7 +398,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 template <int HD, int kS, bool kF16>
-__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
   using L = Layout<HD>;
   constexpr bool kSplit = kS == kSchedSplit;
   constexpr bool kBand = kS == kSchedBand;
@@ -687,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int rg = 0; rg < L::kRegions; ++rg)
               ptx::tma_load_4d(sbase + L::kOffKV + s * L::kTileBytes + rg * L::kRegionBytes,
                                t ? &p.tm_v : &p.tm_k, bar(L::kBarKVFull + s), 64 * rg,
-                               (kS != kSchedWhole ? u.kv0 + j : j) * kBlockN, uh, ub);
+                               (u.kv0 + j) * kBlockN, uh, ub);
             last_fill[s] = static_cast<int>(it);
           }
         }
@@ -1085,7 +1118,7 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
-  bool attr[2][3][2] = {};   // [D == 128][schedule][fp16]: shared-memory opt-in done
+  bool attr[2][4][2] = {};   // [D == 128][schedule][fp16]: shared-memory opt-in done
 };
 
 std::mutex g_mutex;
@@ -1115,11 +1148,18 @@ KernelFn attention_kernel_t(int D, int sched) {
 KernelFn attention_kernel(int D, int sched, bool f16) {
   return f16 ? attention_kernel_t<true>(D, sched) : attention_kernel_t<false>(D, sched);
 }
+using TableKernelFn = void (*)(const fa::TableParams);
+TableKernelFn table_kernel(int D, bool f16) {
+  if (D == 64)
+    return f16 ? fa::fa_fwd_kernel<64, fa::kSchedTable, true> : fa::fa_fwd_kernel<64, fa::kSchedTable, false>;
+  return f16 ? fa::fa_fwd_kernel<128, fa::kSchedTable, true> : fa::fa_fwd_kernel<128, fa::kSchedTable, false>;
+}
 
 // Shared-memory opt-in for one kernel instance, and a check that the registers it
 // is launched with cover the warpgroups' register split (setmaxnreg.inc would
 // otherwise wait forever for registers that do not exist).
-fa_status configure_kernel(void (*kernel)(const Params), int smem_bytes) {
+template <class Fn>
+fa_status configure_kernel(Fn kernel, int smem_bytes) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
       cudaSuccess)
     return FA_ERR_CUDA;
@@ -1159,10 +1199,11 @@ fa_status prepare_device(int dev, int D, int* sm_count, bool f16 = false) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   const int di = (D == 128) ? 1 : 0, ti = f16 ? 1 : 0;
-  for (int sc = 0; sc < 3; ++sc) {
+  for (int sc = 0; sc < 4; ++sc) {
     if (info.attr[di][sc][ti]) continue;
-    const fa_status st = configure_kernel(attention_kernel(D, sc, f16),
-                                          D == 64 ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc);
+    const int smem = D == 64 ? fa::Layout<64>::kAlloc : fa::Layout<128>::kAlloc;
+    const fa_status st = sc == fa::kSchedTable ? configure_kernel(table_kernel(D, f16), smem)
+                                               : configure_kernel(attention_kernel(D, sc, f16), smem);
     if (st != FA_OK) return st;
     info.attr[di][sc][ti] = true;
   }
@@ -1298,6 +1339,86 @@ Plan plan_schedule(const Problem& pr, int sm_count) {
   return pl;
 }
 
+// ---------------------------------------------------------------- schedule table (kSchedTable)
+// Causal units are dealt heaviest first so the CTAs finish together; with the formula order
+// (all heads' last query tiles first) every head's K/V is in flight at once, and K/V tiles
+// leave the L2 cache between the units of a head that read them (DRAM reads measured at
+// 2.6x the compulsory bytes at 4K tokens, 64 heads).  When the heads' K/V outgrow the L2,
+// the host orders the units instead: heads in groups whose K/V take about 32 MiB, group
+// after group, each group's units heaviest first, each unit to the CTA with the least work
+// so far (greedy longest-processing-time).  The per-CTA lists go to the kernel with the
+// launch.  A one-entry cache per device keeps the last table.
+constexpr long long kTableGroupBytes = 32ll << 20;   // K/V bytes of one head group
+constexpr long long kTableMinBytes = 48ll << 20;     // below this the heads' K/V stay in L2
+
+bool table_eligible(const Problem& pr, const Plan& pl) {
+  if (pl.split || pl.band || !pr.causal || (g_debug_flags.load() & 16u)) return false;
+  const long long kv_head = 4ll * pr.Lk * pr.D;   // K and V bytes of one head (16-bit elements)
+  return pr.n_units <= fa::kTabMaxUnits && pl.grid <= fa::kTabMaxGrid && pr.n_pairs <= 4096 &&
+         pr.bh < (1ll << 20) && pr.bh * kv_head > kTableMinBytes;
+}
+
+struct TableCache {
+  bool valid = false;
+  long long bh = 0;
+  int Lq = 0, Lk = 0, D = 0, grid = 0;
+  std::vector<uint16_t> off;
+  std::vector<uint32_t> units;
+};
+std::mutex g_table_mutex;
+TableCache g_table_cache[kMaxDevices];
+
+void build_table(const Problem& pr, int G, TableCache& tc) {
+  const long long kv_head = 4ll * pr.Lk * pr.D;
+  const long long group = std::max(1ll, kTableGroupBytes / kv_head);
+  std::vector<std::vector<uint32_t>> lists(G);
+  using Load = std::pair<long long, int>;   // (work so far, CTA): least work first, then lowest index
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int g = 0; g < G; ++g) heap.push({0, g});
+  for (long long h0 = 0; h0 < pr.bh; h0 += group) {
+    const long long h1 = std::min(pr.bh, h0 + group);
+    for (int pair = pr.n_pairs - 1; pair >= 0; --pair) {
+      // Cost: key tiles of the pair's two query tiles, plus two for the unit's fill and drain.
+      const int q0 = pair * 2 * fa::kBlockM;
+      const int n0 = std::min(pr.nkv, q0 / fa::kBlockN + 1);
+      const int n1 = q0 + fa::kBlockM >= pr.Lq ? 0 : std::min(pr.nkv, (q0 + fa::kBlockM) / fa::kBlockN + 1);
+      const long long cost = n0 + n1 + 2;
+      for (long long h = h0; h < h1; ++h) {
+        const Load least = heap.top();
+        heap.pop();
+        lists[least.second].push_back(static_cast<uint32_t>((h << 12) | pair));
+        heap.push({least.first + cost, least.second});
+      }
+    }
+  }
+  tc.off.assign(G + 1, 0);
+  tc.units.clear();
+  for (int g = 0; g < G; ++g) {
+    tc.off[g] = static_cast<uint16_t>(tc.units.size());
+    tc.units.insert(tc.units.end(), lists[g].begin(), lists[g].end());
+  }
+  tc.off[G] = static_cast<uint16_t>(tc.units.size());
+  tc.bh = pr.bh;
+  tc.Lq = pr.Lq;
+  tc.Lk = pr.Lk;
+  tc.D = pr.D;
+  tc.grid = G;
+  tc.valid = true;
+}
+
+// Fills the table part of *tp for this problem (from the cache when it matches).
+fa_status fill_table(const Problem& pr, int G, fa::TableParams* tp) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  TableCache& tc = g_table_cache[dev];
+  if (!tc.valid || tc.bh != pr.bh || tc.Lq != pr.Lq || tc.Lk != pr.Lk || tc.D != pr.D || tc.grid != G)
+    build_table(pr, G, tc);
+  std::copy(tc.off.begin(), tc.off.end(), tp->tab_off);
+  std::copy(tc.units.begin(), tc.units.end(), tp->tab_units);
+  return FA_OK;
+}
+
 // allow_dependent = false keeps the kernel from starting before the operation ahead of it
 // in the stream has completed (needed when that operation is an event wait, which a
 // programmatic dependent launch does not order).
@@ -1364,7 +1485,16 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   cfg.attrs = attr;
   cfg.numAttrs = (dependent_launch && allow_dependent) ? 1 : 0;
   const int sched = pl.band ? fa::kSchedBand : pl.split ? fa::kSchedSplit : fa::kSchedWhole;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched, pr.f16), p);
+  cudaError_t err;
+  if (table_eligible(pr, pl)) {
+    fa::TableParams tp;
+    static_cast<Params&>(tp) = p;
+    const fa_status ts = fill_table(pr, pl.grid, &tp);
+    if (ts != FA_OK) return ts;
+    err = cudaLaunchKernelEx(&cfg, table_kernel(pr.D, pr.f16), tp);
+  } else {
+    err = cudaLaunchKernelEx(&cfg, attention_kernel(pr.D, sched, pr.f16), p);
+  }
   if (err != cudaSuccess) return FA_ERR_CUDA;
   if (pl.split && pl.grid > 1) {
     // Merge the parts of every split unit (same stream: runs after the parts exist).

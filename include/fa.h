@@ -378,8 +378,10 @@ fa_status fa_last_device_status(cudaStream_t stream);
  * fa_fwd_window run its band kernel also for the bands (-1, 0) and (-1, -1), so
  * that it can be compared with fa_fwd's kernels.  Bit 3 makes fa_fwd_host (and
  * fa_fwd_host_workspace_size) cut the heads into as many chunks as it can, so that
- * small problems exercise the overlapped pipeline.  Not for production use;
- * returns FA_OK.
+ * small problems exercise the overlapped pipeline.  Bit 4 turns off the host-computed
+ * unit order that causal problems with more than 48 MiB of K/V use (heads grouped so
+ * their K/V stay in the L2 cache, units dealt to the least-loaded CTA), so that the two
+ * orders can be compared bit for bit.  Not for production use; returns FA_OK.
  */
 fa_status fa_debug_set(unsigned int flags, unsigned long long wait_limit_ns);
 
