@@ -44,6 +44,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <atomic>
 #include <climits>
 #include <mutex>
@@ -94,12 +95,18 @@ struct Layout {
   static constexpr int kRegionBytes = kBlockM * 128;     // 128 rows x 128 B (64 bf16): one swizzle column
   static constexpr int kRegions = HD / 64;
   static constexpr int kStages = (HD == 128) ? 4 : 8;    // K/V ring slots
-  static constexpr int kOffQ = 0;                        // two Q tiles
-  static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  static constexpr int kBarQFull = 0;                    // [2]  Q_i landed
-  static constexpr int kBarQEmpty = 2;                   // [2]  last S_i MMA of a unit done
-  static constexpr int kBarKVFull = 4;                   // [kStages]
+  // D = 64 has shared memory to spare: two Q buffers per tile (the next unit's Q loads
+  // while the current unit runs) and one O staging tile per query tile (the epilogue
+  // writes O / l there and one TMA store moves the tile to global memory).
+  static constexpr int kQBufs = (HD == 64) ? 2 : 1;
+  static constexpr bool kTmaStoreO = (HD == 64);
+  static constexpr int kOffQ = 0;                        // Q_i of buffer b: kOffQ + (2b + i) * kTileBytes
+  static constexpr int kOffKV = 2 * kQBufs * kTileBytes;
+  static constexpr int kOffStage = kOffKV + kStages * kTileBytes;   // [2] O staging (D = 64)
+  static constexpr int kOffBar = kOffStage + (kTmaStoreO ? 2 : 0) * kTileBytes;
+  static constexpr int kBarQFull = 0;                    // [2 kQBufs]  Q_i of buffer b landed (2b + i)
+  static constexpr int kBarQEmpty = 2 * kQBufs;          // [2 kQBufs]  last MMA reading it done
+  static constexpr int kBarKVFull = 4 * kQBufs;          // [kStages]
   static constexpr int kBarKVEmpty = kBarKVFull + kStages;
   static constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_i in TMEM
   static constexpr int kBarPFull = kBarSFull + 2;           // [2] P_i in TMEM, O_i rescaled
@@ -139,6 +146,7 @@ struct Params {
   CUtensorMap tm_q;   // 4-D views [B][H][L][D] of Q, K, V (caller's strides); box 64 x 128 x 1 x 1
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;   // D = 64: 4-D view of O for the epilogue's TMA stores (same box)
   uint16_t* o;        // bf16 or fp16 elements
   long long o_sb, o_sh, o_sl;   // O strides in elements (batch, head, row); features contiguous
   float* lse;         // contiguous [B*H][Lq]
@@ -416,9 +424,12 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2 * L::kQBufs; ++i) {
       ptx::mbar_init(bar(L::kBarQFull + i), 1);
       ptx::mbar_init(bar(L::kBarQEmpty + i), 1);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(L::kBarSFull + i), 1);
       ptx::mbar_init(bar(L::kBarPFull + i), 4 * 32);
       ptx::mbar_init(bar(L::kBarPHalf + i), 4 * 32);
@@ -649,6 +660,42 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       const float inv_l = kBand ? (l > 0.0f ? 1.0f / l : 0.0f) : 1.0f / l;
       const bool store = q < p.Lq;
       const int ob = bh / p.H, oh = bh - ob * p.H;
+      if constexpr (L::kTmaStoreO) {
+        // D = 64: each thread writes its row into this tile's staging buffer in the
+        // 128-byte-swizzled layout of the O tensor map (16-byte chunk c of row r at chunk
+        // position c ^ (r % 8)), and one thread stores the 128 x 64 tile with TMA; rows
+        // past Lq lie outside the tensor and are not written.
+        const uint32_t stage = sbase + L::kOffStage + wg * L::kTileBytes;
+        const bool leader = (threadIdx.x & 127) == 0;
+        if (leader) ptx::bulk_wait_read_all();   // the previous store has read the buffer
+        ptx::named_bar_sync(1 + wg, 128);
+        const uint32_t row_addr = stage + row * 128;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld32x32b_x32(t_o + c0, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack2<kF16>(__uint_as_float(o[2 * c]) * inv_l,
+                                __uint_as_float(o[2 * c + 1]) * inv_l);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t chunk = static_cast<uint32_t>((c0 >> 3) + v);
+            ptx::st_shared_v4(row_addr + ((chunk ^ static_cast<uint32_t>(row & 7)) << 4), pk[4 * v],
+                              pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        // O_i has been read into registers: the next unit's P_i V MMA may overwrite it.
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(1 + wg, 128);
+        if (leader) {
+          ptx::tma_store_4d(&p.tm_o, stage, 0, qt, oh, ob);
+          ptx::bulk_commit_group();
+        }
+      } else {
       uint16_t* orow = p.o + ob * p.o_sb + oh * p.o_sh + static_cast<long long>(store ? q : 0) * p.o_sl;
 #pragma unroll
       for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -669,6 +716,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       // O_i has been read into registers: the next unit's P_i V MMA may overwrite it.
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
+      }
       if (store) {
         p.lse[static_cast<size_t>(bh) * p.Lq + q] = (m + log2f(l)) * 0.69314718055994531f;
       }
@@ -693,16 +741,20 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (u.nblk[i] == 0) continue;
-          if (q_count[i] > 0 && !wait_phase(bar(L::kBarQEmpty + i), (q_count[i] - 1) & 1,
-                                            abort_flag, limit, kSiteLoadKV)) {
+          // Buffers alternate between units (D = 64); a buffer is refilled once the MMAs of
+          // its previous unit have read it.  uses = earlier loads into this buffer.
+          const int qi = 2 * (L::kQBufs == 2 ? static_cast<int>(q_count[i] & 1) : 0) + i;
+          const uint32_t uses = L::kQBufs == 2 ? (q_count[i] >> 1) : q_count[i];
+          if (uses > 0 && !wait_phase(bar(L::kBarQEmpty + qi), (uses - 1) & 1,
+                                      abort_flag, limit, kSiteLoadKV)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(bar(L::kBarQFull + i), L::kTileBytes);
+          ptx::mbar_arrive_expect_tx(bar(L::kBarQFull + qi), L::kTileBytes);
 #pragma unroll
           for (int rg = 0; rg < L::kRegions; ++rg)
-            ptx::tma_load_4d(sbase + L::kOffQ + i * L::kTileBytes + rg * L::kRegionBytes, &p.tm_q,
-                             bar(L::kBarQFull + i), 64 * rg, u.q0 + i * kBlockM, uh, ub);
+            ptx::tma_load_4d(sbase + L::kOffQ + qi * L::kTileBytes + rg * L::kRegionBytes, &p.tm_q,
+                             bar(L::kBarQFull + qi), 64 * rg, u.q0 + i * kBlockM, uh, ub);
           ++q_count[i];
         }
         for (int j = 0; j < u.nmax && ok; ++j) {
@@ -732,8 +784,14 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         if (last_fill[s] >= 0)
           drain_phase(bar(L::kBarKVFull + s), (last_fill[s] / L::kStages) & 1, limit);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        if (q_count[i] > 0) drain_phase(bar(L::kBarQFull + i), (q_count[i] - 1) & 1, limit);
+      for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int b = 0; b < L::kQBufs; ++b) {
+          // loads into buffer b of tile i: every kQBufs-th load, starting with load b
+          const uint32_t n = (q_count[i] + L::kQBufs - 1 - b) / L::kQBufs;
+          if (n > 0) drain_phase(bar(L::kBarQFull + 2 * b + i), (n - 1) & 1, limit);
+        }
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -748,8 +806,17 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       const uint64_t desc_q0 = sw128_desc(sbase + L::kOffQ, 16, 1024);
       const uint64_t desc_kv0 = sw128_desc(sbase + L::kOffKV, 16, 1024);
       const uint64_t desc_v0 = sw128_desc(sbase + L::kOffKV, L::kRegionBytes, 1024);
+      uint32_t q_count[2] = {0, 0};   // units in which tile i was present (q_full / o_empty phase)
+      // Q_i of the current unit is in buffer q_count[i] % kQBufs (index 2b + i): the
+      // buffers alternate between units when kQBufs = 2.
+      uint32_t q_alt = 0;             // bit i: tile i of the current unit uses buffer 1
+      auto q_buf = [&](int i) -> int { return 2 * static_cast<int>((q_alt >> i) & 1u) + i; };
+      // Phase of q_full for that buffer: the number of earlier loads into it.
+      auto q_phase = [&](int i) -> uint32_t {
+        return (L::kQBufs == 2 ? (q_count[i] >> 1) : q_count[i]) & 1;
+      };
       auto issue_s = [&](int i, int slot) {
-        const uint64_t a = desc_q0 + ((i * L::kTileBytes) >> 4);
+        const uint64_t a = desc_q0 + ((q_buf(i) * L::kTileBytes) >> 4);
         const uint64_t b = desc_kv0 + ((slot * L::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -767,7 +834,6 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         }
       };
       auto issue_pv = [&](int i, int slot, bool accumulate) { issue_pv_part(i, slot, accumulate, 0, kBlockN / 16); };
-      uint32_t q_count[2] = {0, 0};   // units in which tile i was present (q_full / o_empty phase)
       uint32_t p_base[2] = {0, 0};    // S_i tiles of earlier units (p_full phase)
       uint32_t it_base = 0;           // K/V ring position of this unit's K_0
       bool ok = true;
@@ -784,7 +850,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
 #pragma unroll
           for (int i = 0; i < 2; ++i)
             if (ok && nblk[i] > 0)
-              ok = wait_warp(bar(L::kBarQFull + i), q_count[i] & 1, abort_flag, limit, kSiteMmaQ);
+              ok = wait_warp(bar(L::kBarQFull + q_buf(i)), q_phase(i), abort_flag, limit, kSiteMmaQ);
           const int slot_k0 = it_base % L::kStages;
           if (ok) ok = wait_warp(bar(L::kBarKVFull + slot_k0), (it_base / L::kStages) & 1,
                                   abort_flag, limit, kSiteMmaK);
@@ -796,7 +862,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
               issue_s(i, slot_k0);
               ptx::mma_commit_warp(bar(L::kBarSFull + i));
               ++s_iss[i];
-              if (nblk[i] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));
+              if (nblk[i] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + q_buf(i)));
             }
           }
           ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k0));
@@ -829,7 +895,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
               issue_s(i, slot_k);
               ptx::mma_commit_warp(bar(L::kBarSFull + i));
               ++s_iss[i];
-              if (t == nblk[i] - 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));   // Q_i read for the last time
+              if (t == nblk[i] - 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + q_buf(i)));   // Q_i read for the last time
             }
             if (!ok) break;
             if (k_ready) ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k));
@@ -869,6 +935,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
             p_base[i] += nblk[i];
             if (nblk[i] > 0) ++q_count[i];
           }
+          if (L::kQBufs == 2) q_alt = (q_count[0] & 1u) | ((q_count[1] & 1u) << 1);
         }
       }
       for (int r = 0; !L::kDecoupled && ok && unit_of<kS>(p, r, u); ++r) {
@@ -880,7 +947,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (ok && nblk[i] > 0)
-            ok = wait_warp(bar(L::kBarQFull + i), q_count[i] & 1, abort_flag, limit, kSiteMmaQ);
+            ok = wait_warp(bar(L::kBarQFull + q_buf(i)), q_phase(i), abort_flag, limit, kSiteMmaQ);
         const int slot_k0 = it_base % L::kStages;
         if (ok) ok = wait_warp(bar(L::kBarKVFull + slot_k0), (it_base / L::kStages) & 1,
                                 abort_flag, limit, kSiteMmaK);
@@ -891,7 +958,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           if (nblk[i] > 0 && fst[i] == 0) {
             issue_s(i, slot_k0);
             ptx::mma_commit_warp(bar(L::kBarSFull + i));
-            if (nblk[i] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));
+            if (nblk[i] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + q_buf(i)));
           }
         }
         ptx::mma_commit_warp(bar(L::kBarKVEmpty + slot_k0));
@@ -934,7 +1001,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
             issue_pv_part(i, slot_v, true, kBlockN / 32, kBlockN / 16);
             if (jl == nblk[i] - 1) {
               ptx::mma_commit_warp(bar(L::kBarOFull + i));
-              if (nblk[i] > 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + i));   // Q_i no longer read
+              if (nblk[i] > 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + q_buf(i)));   // Q_i no longer read
             }
             if (jl + 1 < nblk[i]) {
               if (!k_ready) {
@@ -965,7 +1032,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
               if (ok) {
                 issue_s(1, slot_k);
                 ptx::mma_commit_warp(bar(L::kBarSFull + 1));
-                if (nblk[1] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + 1));
+                if (nblk[1] == 1) ptx::mma_commit_warp(bar(L::kBarQEmpty + q_buf(1)));
               }
             }
           }
@@ -979,6 +1046,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           p_base[i] += nblk[i];
           if (nblk[i] > 0) ++q_count[i];
         }
+        if (L::kQBufs == 2) q_alt = (q_count[0] & 1u) | ((q_count[1] & 1u) << 1);
       }
       // Drain: every MMA issued has completed before TMEM is freed.
       ptx::mma_commit_warp(bar(L::kBarDrain));
@@ -989,6 +1057,8 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
     ptx::setmaxnreg_dec<kRegsOther>();   // the two spare warps of the load/MMA warpgroup
   }
 
+  // The epilogue's TMA stores (D = 64) must be complete before the CTA exits.
+  if (L::kTmaStoreO && warp < 8 && (threadIdx.x & 127) == 0) ptx::bulk_wait_all();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -1428,6 +1498,10 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   if (!encode_map(&p.tm_q, pr.Q, pr.B, pr.H, pr.Lq, pr.D, pr.qs, pr.f16) ||
       !encode_map(&p.tm_k, pr.K, pr.B, pr.H, pr.Lk, pr.D, pr.ks, pr.f16) ||
       !encode_map(&p.tm_v, pr.V, pr.B, pr.H, pr.Lk, pr.D, pr.vs, pr.f16))
+    return FA_ERR_CUDA;
+  // D = 64 stores O through a tensor map as well (TMA stores from the epilogue's staging).
+  if (pr.D == 64 ? !encode_map(&p.tm_o, pr.O, pr.B, pr.H, pr.Lq, pr.D, pr.os, pr.f16)
+                 : (memset(&p.tm_o, 0, sizeof(p.tm_o)), false))
     return FA_ERR_CUDA;
   p.o = static_cast<uint16_t*>(pr.O);
   p.o_sb = pr.os[0];
