@@ -309,3 +309,31 @@ def test_chained_calls_see_previous_results(shape, kw):
     b = chain(sync=False)
     assert fa.fa_last_device_status() == fa.FA_OK
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("name", ["seq16k_d128_causal", "cross_q500_k8191_d128"])
+def test_workload_through_host_call(oracle_mod, name):
+    """The end-to-end path the benchmark times: pinned host Q, K, V through the C call
+    fa_fwd_host (chunks of heads, copies overlapped with the kernels) at full size, on the
+    seeded row sample of the workload."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    dev = torch.device("cuda:0")
+    left, right = -1, (0 if w.causal else -1)
+    st, nbytes = fa.fa_fwd_host_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, left, right)
+    assert st == fa.FA_OK
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lse = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    assert fa.fa_fwd_host(qp, kp, vp, o, lse, w.B, w.H, w.Lq, w.Lk, w.D, left, right, w.scale, ws,
+                          nbytes, stream) == fa.FA_OK
+    stream.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    extra = (383, 384, 499) if w.Lq == 500 else ()
+    check_rows(oracle_mod, q, k, v, w.causal, w.scale, sample_rows(w, 512, extra), o, lse)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    if w.causal:   # whole units in every chunk: the same bits as one launch on device buffers
+        od, ld = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=True, scale=w.scale)
+        assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
