@@ -76,7 +76,7 @@ constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // one second per 
 
 // Work schedules, one kernel instantiation each (template parameter kS).
 //   kSchedWhole: whole units, every query tile starts at key tile 0 (full or causal mask).
-//   kSchedSplit: non-causal key ranges cut across CTAs, merged by fa_combine_kernel.
+//   kSchedSplit: key ranges cut across CTAs, merged by fa_combine_kernel.
 //   kSchedBand : local (sliding-window) attention; each query tile covers its own band
 //                of key tiles, and only tiles cut by the band's edges are masked.
 //   kSchedTable: whole units in an order computed on the host (causal problems whose K/V
@@ -189,9 +189,9 @@ template <> struct ParamsOf<kSchedTable> { using type = TableParams; };
 // CTA g takes unit r*G + g when r is even, r*G + G-1-g when odd), which keeps
 // the per-CTA totals within a few percent of each other for causal loads.
 //
-// Split schedule (non-causal only, where every unit costs the same): the units'
-// key tiles form one sequence of n_units * nkv steps and CTA g takes the steps
-// [T*g/G, T*(g+1)/G).  A unit cut by a CTA boundary is processed in parts; each
+// Split schedule: the units' key tiles form one sequence of T steps (head after head,
+// each head's pairs in order; nkv per unit for the full mask, the key tiles up to the
+// diagonal with the causal mask) and CTA g takes the steps [T*g/G, T*(g+1)/G).  A unit cut by a CTA boundary is processed in parts; each
 // part leaves its rows' partial state (unnormalised O, running max m, sum l) in
 // the workspace, and a second kernel on the same stream merges the parts of every
 // split unit into the final O and LSE.  No CTA ever waits for another.
@@ -209,6 +209,44 @@ struct Unit {
 
 __device__ __forceinline__ long long split_lo(const Params& p, int g) {
   return p.total_steps * g / static_cast<int>(gridDim.x);
+}
+
+// Split schedule step space: the units of a head are its pairs of query tiles in order
+// (pair p = rows [256p, 256p + 256)), heads one after the other; a unit's steps are the key
+// tiles of its longer tile: all nkv of them for the full mask, with the causal mask the
+// tiles up to the diagonal of its last present tile.
+__host__ __device__ inline long long pair_steps(int pair, int nkv, int Lq, int causal) {
+  if (!causal) return nkv;
+  const int last = (pair * 2 * kBlockM + kBlockM < Lq) ? 2 * pair + 2 : 2 * pair + 1;
+  return last < nkv ? last : nkv;
+}
+// Steps of pairs [0, P) of one head (P <= n_pairs).
+__host__ __device__ inline long long head_prefix(int P, int nkv, int Lq, int n_pairs, int causal) {
+  if (!causal) return static_cast<long long>(P) * nkv;
+  const long long c = nkv / 2;   // pairs p with 2p + 2 <= nkv
+  long long s = (P <= c) ? static_cast<long long>(P) * (P + 1)
+                         : c * (c + 1) + static_cast<long long>(P - c) * nkv;
+  if (P == n_pairs && n_pairs > 0) {   // the head's last pair may lack its second tile
+    const long long full = 2ll * (n_pairs - 1) + 2 < nkv ? 2ll * (n_pairs - 1) + 2 : nkv;
+    s -= full - pair_steps(n_pairs - 1, nkv, Lq, causal);
+  }
+  return s;
+}
+// The unit that contains step x: its head, pair, first step and number of steps.
+__device__ __forceinline__ void split_locate(long long x, int nkv, int Lq, int n_pairs, int causal,
+                                             int* bh, int* pair, long long* start, long long* steps) {
+  const long long per_head = head_prefix(n_pairs, nkv, Lq, n_pairs, causal);
+  const long long h = x / per_head, xh = x - h * per_head;
+  int lo = 0, hi = n_pairs - 1;   // the last pair whose first step is <= xh
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (head_prefix(mid, nkv, Lq, n_pairs, causal) <= xh) lo = mid;
+    else hi = mid - 1;
+  }
+  *bh = static_cast<int>(h);
+  *pair = lo;
+  *start = h * per_head + head_prefix(lo, nkv, Lq, n_pairs, causal);
+  *steps = pair_steps(lo, nkv, Lq, causal);
 }
 
 __device__ __forceinline__ void unit_rows(const Params& p, int idx, Unit& u) {
@@ -309,21 +347,28 @@ __device__ __forceinline__ bool unit_of(const P& p, int r, Unit& u) {
   } else {
   const long long lo = split_lo(p, g), hi = split_lo(p, g + 1);
   long long x = lo;
+  int bh, pair;
+  long long start, steps;
   for (int k = 0; k < r && x < hi; ++k) {   // skip the first r parts of this CTA's range
-    const long long end = (x / p.nkv + 1) * p.nkv;
-    x = min(end, hi);
+    split_locate(x, p.nkv, p.Lq, p.n_pairs, p.causal, &bh, &pair, &start, &steps);
+    x = min(start + steps, hi);
   }
   if (x >= hi) return false;
-  const int idx = static_cast<int>(x / p.nkv);
-  const int a = static_cast<int>(x - static_cast<long long>(idx) * p.nkv);
-  const int len = static_cast<int>(min(static_cast<long long>(p.nkv - a), hi - x));
-  unit_rows(p, idx, u);
+  split_locate(x, p.nkv, p.Lq, p.n_pairs, p.causal, &bh, &pair, &start, &steps);
+  const int a = static_cast<int>(x - start);
+  const int len = static_cast<int>(min(start + steps - x, hi - x));
+  u.bh = bh;
+  u.q0 = pair * 2 * kBlockM;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) u.nblk[i] = (u.q0 + i * kBlockM >= p.Lq) ? 0 : len;
+  for (int i = 0; i < 2; ++i) {   // the tile's key tiles that fall in this part's [a, a + len)
+    const int qi = u.q0 + i * kBlockM;
+    const int all = p.causal ? min(p.nkv, qi / kBlockN + 1) : p.nkv;
+    u.nblk[i] = (qi >= p.Lq) ? 0 : max(0, min(all, a + len) - a);
+  }
   u.nmax = len;
   u.kv0 = a;
   u.first[0] = u.first[1] = 0;
-  u.partial = (len != p.nkv);
+  u.partial = (len != steps);
   if (u.partial) u.slot = 2 * g + (x == lo ? 0 : 1);
   return true;
   }
@@ -484,6 +529,19 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
     Unit u;
     for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
       const int n_blocks = wg ? u.nblk[1] : u.nblk[0];
+      if constexpr (kSplit) {
+        // Causal split: a part can hold no key tile of the first (shorter) query tile; its
+        // slot then holds an empty partial state (O = 0, m = -inf, l = 0) for the merge.
+        if (n_blocks == 0 && u.partial && u.q0 + wg * kBlockM < p.Lq) {
+          const size_t rowi = static_cast<size_t>(u.slot * 2 + wg) * kBlockM + row;
+          float* so = p.ws_o + rowi * HD;
+#pragma unroll
+          for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(so + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.ws_ml[rowi * 2] = -INFINITY;
+          p.ws_ml[rowi * 2 + 1] = 0.0f;
+          continue;
+        }
+      }
       if (n_blocks == 0) {
         // Band schedule: a present tile whose rows have no allowed key (key padding):
         // O = 0 and LSE = -inf, written here without any MMA.
@@ -1081,6 +1139,7 @@ struct CombineParams {
   int n_pairs;
   int bh_count;
   int Lq;
+  int causal;
 };
 
 // One CTA per (CTA boundary of the attention kernel, query tile, group of 16
@@ -1106,17 +1165,18 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
     const long long G = c.grid;
     auto lo = [&](long long g) { return c.total_steps * g / G; };
     const long long xb = lo(b);
-    const long long u = xb / c.nkv;
-    const long long step0 = u * c.nkv;
+    int bh, pair;
+    long long step0, steps;
+    split_locate(xb, c.nkv, c.Lq, c.n_pairs, c.causal, &bh, &pair, &step0, &steps);
     int n = 0;
-    // nothing to do on a boundary between units, or if an earlier boundary lies in u
+    // nothing to do on a boundary between units, or if an earlier boundary lies in the unit
     if (xb != step0 && !(b >= 2 && lo(b - 1) > step0)) {
-      for (long long g = b - 1; g < G && lo(g) <= step0 + c.nkv - 1 && n < kCombineMaxParts; ++g)
+      for (long long g = b - 1; g < G && lo(g) <= step0 + steps - 1 && n < kCombineMaxParts; ++g)
         s_slot[n++] = static_cast<int>(2 * g + (lo(g) >= step0 ? 0 : 1));
     }
     s_nparts = n;
-    s_bh = static_cast<int>(u / c.n_pairs);   // non-causal order: a head's pairs are neighbours
-    s_q0 = static_cast<int>(u % c.n_pairs) * 2 * kBlockM + tile * kBlockM;
+    s_bh = bh;
+    s_q0 = pair * 2 * kBlockM + tile * kBlockM;
   }
   __syncthreads();
   const int nparts = s_nparts;
@@ -1148,6 +1208,7 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
         x[0] = v.x; x[1] = v.y;
       }
       const float m_new = fmaxf(m[rr], ml.x);
+      if (m_new == -INFINITY) continue;   // no key of this row so far (an empty part)
       const float a = ptx::ex2_approx(m[rr] - m_new);   // 0 on the first part (m = -inf)
       const float w = ptx::ex2_approx(ml.x - m_new);
       l[rr] = l[rr] * a + ml.y * w;
@@ -1377,7 +1438,9 @@ fa_status check_problem(const void* Q, const void* K, const void* V, void* O, fl
 }
 
 // Schedule choice.  Causal units have different costs and are balanced by the
-// heaviest-first boustrophedon order.  Non-causal units all cost the same; when
+// heaviest-first boustrophedon order (or the host-computed table order); only when
+// the longest unit dwarfs an even share are their key ranges split (see below).
+// Non-causal units all cost the same; when
 // whole units would keep at most half of the SM-rounds busy (a quarter for D = 64,
 // whose parts are cheaper to compute and so relatively dearer to merge) and a unit
 // has at least two key tiles, the key ranges are split across CTAs (needs a
@@ -1392,16 +1455,36 @@ struct Plan {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Key-tile steps of all units in the split schedule's step space.
+long long split_total_steps(const Problem& pr) {
+  return pr.bh * fa::head_prefix(pr.n_pairs, pr.nkv, pr.Lq, pr.n_pairs, pr.causal);
+}
+
 Plan plan_schedule(const Problem& pr, int sm_count) {
   Plan pl{};
   const long long rounds = (pr.n_units + sm_count - 1) / sm_count;
   const double fill = static_cast<double>(pr.n_units) / (static_cast<double>(rounds) * sm_count);
-  pl.split = !pr.causal && pr.nkv >= 2 && fill <= (pr.D == 128 ? 0.5 : 0.25);
+  if (!pr.causal) {
+    pl.split = pr.nkv >= 2 && fill <= (pr.D == 128 ? 0.5 : 0.25);
+  } else {
+    // Causal units grow along the sequence; whole units finish no sooner than the longest
+    // one.  When that unit is well above an even share of all steps (few heads, long
+    // sequences), the key ranges are cut across CTAs as for the full mask.
+    // Each part reloads its Q tiles and parks fp32 partial rows, so the split pays only
+    // when the longest unit is far above the share: measured side by side, one or two heads
+    // of 8K-16K tokens at D = 64 (longest unit about 4.6x the share) ran 42-84 % faster,
+    // while shapes near 2.2x lost 4-23 % at D = 128.  Short sequences (units under 16 key
+    // tiles) and problems under two steps per SM stay whole.
+    const long long longest = fa::pair_steps(pr.n_pairs - 1, pr.nkv, pr.Lq, 1);
+    const long long total = split_total_steps(pr);
+    const double share = static_cast<double>(total) / sm_count;
+    pl.split = longest >= 16 && total >= 2ll * sm_count && static_cast<double>(longest) >= 4.0 * share;
+  }
   if (!pl.split) {
     pl.grid = std::min(pr.n_units, sm_count);
     return pl;
   }
-  const long long steps = static_cast<long long>(pr.n_units) * pr.nkv;
+  const long long steps = split_total_steps(pr);
   pl.grid = static_cast<int>(std::min<long long>(steps, sm_count));
   const size_t rows = static_cast<size_t>(pl.grid) * 2 * 2 * fa::kBlockM;   // 2 slots x 2 tiles
   pl.off_ml = round256(rows * pr.D * sizeof(float));
@@ -1522,7 +1605,7 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   // Heaviest units first: the last query tiles unless only the left side is bounded.
   p.band_desc = (pr.win_left >= 0 && pr.win_right < 0) ? 0 : 1;
   p.kv_len = pr.kv_len;
-  p.total_steps = static_cast<long long>(pr.n_units) * pr.nkv;
+  p.total_steps = split_total_steps(pr);
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
   if (pl.split) {
@@ -1587,6 +1670,7 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
     c.n_pairs = pr.n_pairs;
     c.bh_count = static_cast<int>(pr.bh);
     c.Lq = pr.Lq;
+    c.causal = pr.causal;
     cudaLaunchConfig_t cc = {};
     cc.gridDim = dim3(static_cast<unsigned>(pl.grid - 1), 2, fa::kBlockM / fa::kCombineRows);
     cc.blockDim = dim3(128);

@@ -78,6 +78,23 @@ def test_noalloc_call_allocates_no_device_memory():
     assert fa.fa_last_device_status() == fa.FA_OK
 
 
+def test_noalloc_causal_split_matches_workspace_entry_point():
+    """A causal problem of one long head also takes the split schedule, and its scratch."""
+    B, H, Lq, Lk, D = 1, 1, 16384, 16384, 128
+    st, nbytes = fa.fa_fwd_workspace_size(B, H, Lq, Lk, D, True)
+    assert st == fa.FA_OK and nbytes > 0
+    q, k, v, o_ref, l_ref = _buffers(B, H, Lq, Lk, D, seed=23)
+    scale = 1.0 / math.sqrt(D)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    assert fa.fa_fwd_ws(q, k, v, o_ref, l_ref, B, H, Lq, Lk, D, 1, scale, ws, nbytes) == fa.FA_OK
+    for _ in range(2):
+        o = torch.full_like(o_ref, float("nan"))
+        lse = torch.full_like(l_ref, float("nan"))
+        assert fa.fa_fwd_noalloc(q, k, v, o, lse, B, H, Lq, Lk, D, 1, scale) == fa.FA_OK
+        assert fa.fa_last_device_status() == fa.FA_OK
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
 def test_noalloc_without_scratch_matches_fa_fwd():
     """A causal shape runs on whole units and needs no scratch."""
     B, H, Lq, Lk, D = 2, 4, 700, 700, 128
