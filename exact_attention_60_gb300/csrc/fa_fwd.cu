@@ -86,7 +86,7 @@ enum Sched : int { kSchedWhole = 0, kSchedSplit = 1, kSchedBand = 2, kSchedTable
 
 enum WaitSite : uint32_t {
   kSiteLoadKV = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteSoftS, kSiteSoftO,
-  kSiteMmaSFree, kSiteSoftPV
+  kSiteMmaSFree, kSiteSoftPV, kSiteStage
 };
 
 template <int HD>
@@ -120,7 +120,11 @@ struct Layout {
   // D = 128 only: P_i is handed over in halves, p_full for its first 32 packed columns
   // (K-slices 0-3 of the P V MMA) and p_half for the other 32.
   static constexpr int kBarPHalf = kBarPVDone + 2;          // [2]
-  static constexpr int kNumBars = kBarPHalf + 2;
+  // D = 64 epilogue: tile i's O staging buffer may be written (the previous TMA store has
+  // read it; one arrival by the storing thread), and has been written (128 arrivals).
+  static constexpr int kBarStageFree = kBarPHalf + 2;       // [2]
+  static constexpr int kBarStageFull = kBarStageFree + 2;   // [2]
+  static constexpr int kNumBars = kBarStageFull + 2;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
@@ -487,6 +491,11 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       ptx::mbar_init(bar(L::kBarKVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kBarDrain), 1);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(L::kBarStageFree + i), 1);
+      ptx::mbar_init(bar(L::kBarStageFull + i), 4 * 32);
+    }
     if constexpr (L::kDecoupled) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -525,6 +534,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
     const float sl2 = p.scale_log2;
     uint32_t s_base = 0;    // S_i tiles consumed in earlier units (s_full / p_full phase)
     uint32_t o_count = 0;   // units finished by this warpgroup (o_full phase)
+    uint32_t n_stage = 0;   // epilogues through the O staging buffer (stage_free / stage_full phase)
     bool ok = true;
     Unit u;
     for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
@@ -725,8 +735,13 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         // past Lq lie outside the tensor and are not written.
         const uint32_t stage = sbase + L::kOffStage + wg * L::kTileBytes;
         const bool leader = (threadIdx.x & 127) == 0;
-        if (leader) ptx::bulk_wait_read_all();   // the previous store has read the buffer
-        ptx::named_bar_sync(1 + wg, 128);
+        if (leader) {
+          ptx::bulk_wait_read_all();   // the previous store has read the buffer
+          ptx::mbar_arrive(bar(L::kBarStageFree + wg));
+        }
+        ok = wait_phase(bar(L::kBarStageFree + wg), n_stage & 1, abort_flag, limit, kSiteStage);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
         const uint32_t row_addr = stage + row * 128;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -748,11 +763,17 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
         ptx::fence_proxy_async_smem();
-        ptx::named_bar_sync(1 + wg, 128);
+        ptx::mbar_arrive(bar(L::kBarStageFull + wg));
         if (leader) {
-          ptx::tma_store_4d(&p.tm_o, stage, 0, qt, oh, ob);
-          ptx::bulk_commit_group();
+          if (wait_phase(bar(L::kBarStageFull + wg), n_stage & 1, abort_flag, limit, kSiteStage)) {
+            ptx::tma_store_4d(&p.tm_o, stage, 0, qt, oh, ob);
+            ptx::bulk_commit_group();
+          } else {
+            ok = false;
+          }
         }
+        ok = __all_sync(0xffffffffu, ok);
+        ++n_stage;
       } else {
       uint16_t* orow = p.o + ob * p.o_sb + oh * p.o_sh + static_cast<long long>(store ? q : 0) * p.o_sl;
 #pragma unroll

@@ -337,3 +337,24 @@ def test_workload_through_host_call(oracle_mod, name):
     if w.causal:   # whole units in every chunk: the same bits as one launch on device buffers
         od, ld = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=True, scale=w.scale)
         assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_past_lq_untouched_between_heads(D, causal):
+    """O written into a strided view whose heads are separated by sentinel rows: rows at and
+    past Lq of every head (the ragged last query tile; at D = 64 the epilogue stores whole
+    tiles with TMA, clipped by the tensor's bounds) must stay untouched, and the values must
+    equal the contiguous call's bit for bit."""
+    dev = torch.device("cuda:0")
+    B, H, Lq, Lk, D_ = 2, 3, 300, 520, D
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, Lq, Lk, D_, seed=29 + D))
+    gap = 77   # sentinel rows after each head's Lq rows
+    o_buf = torch.full((B, H, Lq + gap, D_), float("nan"), device=dev, dtype=torch.bfloat16)
+    o = o_buf[:, :, :Lq, :]
+    o_ref, l_ref = fa.attention(q, k, v, causal=causal)
+    _, lse = fa.attention(q, k, v, causal=causal, out=o)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert torch.isnan(o_buf[:, :, Lq:, :].float()).all()
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
