@@ -1987,7 +1987,7 @@ extern "C" fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V,
 // Every device buffer lives in the caller's workspace, so the call allocates nothing.
 namespace {
 
-constexpr int kHostMaxChunks = 8;
+constexpr int kHostMaxChunks = 8;   // chunks of heads, plus possibly one single-head last chunk
 
 struct HostPipe {
   bool ready = false;
@@ -1995,8 +1995,8 @@ struct HostPipe {
   cudaStream_t down = nullptr;
   cudaEvent_t start = nullptr;
   cudaEvent_t end = nullptr;
-  cudaEvent_t up_done[kHostMaxChunks] = {};
-  cudaEvent_t cmp_done[kHostMaxChunks] = {};
+  cudaEvent_t up_done[kHostMaxChunks + 1] = {};
+  cudaEvent_t cmp_done[kHostMaxChunks + 1] = {};
 };
 
 std::mutex g_host_mutex[kMaxDevices];
@@ -2011,14 +2011,14 @@ fa_status host_pipe(int dev, HostPipe** out) {
               cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming) == cudaSuccess;
-    for (int c = 0; ok && c < kHostMaxChunks; ++c)
+    for (int c = 0; ok && c < kHostMaxChunks + 1; ++c)
       ok = cudaEventCreateWithFlags(&hp.up_done[c], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.cmp_done[c], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
       if (hp.up) cudaStreamDestroy(hp.up);
       if (hp.down) cudaStreamDestroy(hp.down);
       for (cudaEvent_t e : {hp.start, hp.end}) if (e) cudaEventDestroy(e);
-      for (int c = 0; c < kHostMaxChunks; ++c) {
+      for (int c = 0; c < kHostMaxChunks + 1; ++c) {
         if (hp.up_done[c]) cudaEventDestroy(hp.up_done[c]);
         if (hp.cmp_done[c]) cudaEventDestroy(hp.cmp_done[c]);
       }
@@ -2035,13 +2035,13 @@ fa_status host_pipe(int dev, HostPipe** out) {
 struct HostPlan {
   Problem pr;          // sizes, mask and scale; the pointers are the caller's host buffers
   int chunks = 1;
+  long long bounds[kHostMaxChunks + 2] = {};   // chunk c holds the heads [bounds[c], bounds[c + 1])
   size_t off_q = 0, off_k = 0, off_v = 0, off_o = 0, off_lse = 0, off_split = 0;
   size_t split_bytes = 0;
   size_t total = 0;
 };
 
-// Heads of chunk c: [bh * c / chunks, bh * (c + 1) / chunks).
-long long chunk_lo(const HostPlan& hp, int c) { return hp.pr.bh * c / hp.chunks; }
+long long chunk_lo(const HostPlan& hp, int c) { return hp.bounds[c]; }
 
 // The chunk of heads [a, b) as a problem of its own: B = 1, H = b - a, on the workspace copies.
 Problem chunk_problem(const HostPlan& hp, uint8_t* ws, long long a, long long b) {
@@ -2119,6 +2119,24 @@ fa_status host_plan(int B, int H, int Lq, int Lk, int D, int window_left, int wi
                                ? std::min<long long>(kHostMaxChunks, bh)
                                : std::min<long long>({kHostMaxChunks, pr.n_units / 256, bh});
   hp->chunks = static_cast<int>(std::max<long long>(1, chunks));
+  for (int c = 0; c <= hp->chunks; ++c) hp->bounds[c] = bh * c / hp->chunks;
+  // A causal chunk takes as long as its longest unit, which its last head alone also has:
+  // the last chunk's kernel is what remains once the last input has arrived.  When one head
+  // by itself would take the split-key schedule (its longest unit spread over every SM), the
+  // last chunk is that one head.
+  if (pr.causal && hp->chunks >= 2 && bh > hp->chunks) {
+    Problem one = pr;
+    one.B = 1;
+    one.H = 1;
+    one.bh = 1;
+    one.n_units = pr.n_pairs;
+    if (plan_schedule(one, *sm_count).split) {
+      const int rest = hp->chunks;   // the other heads keep the chunk count
+      for (int c = 0; c <= rest; ++c) hp->bounds[c] = (bh - 1) * c / rest;
+      hp->chunks = rest + 1;
+      hp->bounds[hp->chunks] = bh;
+    }
+  }
   pr.bytes_q = static_cast<size_t>(bh) * Lq * D * 2;
   pr.bytes_k = static_cast<size_t>(bh) * Lk * D * 2;
   pr.bytes_lse = static_cast<size_t>(bh) * Lq * 4;

@@ -263,7 +263,9 @@ fa_status fa_fwd_host_workspace_size(int B, int H, int Lq, int Lk, int D, int wi
  *             `stream` completes only once O and LSE are in host memory.
  *
  * How it runs: the B*H (batch, head) slices are cut into up to 8 chunks of whole heads
- * (each large enough to keep the GPU busy).  Chunk c's Q, K, V travel to the device on
+ * (each large enough to keep the GPU busy); a long causal problem whose single head would
+ * take the split-key schedule gets one more chunk, its last head alone, so that the
+ * kernel left after the last upload is short.  Chunk c's Q, K, V travel to the device on
  * an internal upload stream while chunk c-1 is computed on `stream` (the kernels of
  * fa_fwd_ws / fa_fwd_window) and chunk c-2's O and LSE travel back on an internal
  * download stream; events order the three.  One cudaMemcpyAsync per tensor and chunk.

@@ -334,9 +334,11 @@ def test_workload_through_host_call(oracle_mod, name):
     extra = (383, 384, 499) if w.Lq == 500 else ()
     check_rows(oracle_mod, q, k, v, w.causal, w.scale, sample_rows(w, 512, extra), o, lse)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-    if w.causal:   # whole units in every chunk: the same bits as one launch on device buffers
-        od, ld = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=True, scale=w.scale)
-        assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+    # every row against one launch on device buffers (equal up to the summation order where
+    # a chunk takes the split-key schedule)
+    od, ld = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=w.causal, scale=w.scale)
+    assert (o.float() - od.float().cpu()).abs().max().item() <= TOL_O
+    assert (lse - ld.cpu()).abs().max().item() <= TOL_LSE
 
 
 @pytest.mark.parametrize("D", [64, 128])
