@@ -78,33 +78,121 @@ def peak_value(peaks: dict, key: str, default: float) -> float:
         return default
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks, power and throttle reasons while running.
+class NvmlReader:
+    """Read-only NVML queries through ctypes: SM clock, its maximum, board power and the
+    active clock-event (throttle) reasons of one GPU, found by PCI bus id.  NVML ships
+    with the driver; `lib` may be a stand-in object with the same functions (tests)."""
+    CLOCK_SM = 1
+    # Public NVML clock-event reason bits.
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
 
-    Every sample carries nvidia-smi's own timestamp, so ``summary(t0, t1)`` can keep only
-    the samples taken inside a timed window (host wall-clock seconds, time.time())."""
+    def __init__(self, pci_bus_id: str, lib=None):
+        import ctypes
+        self.ct = ctypes
+        self.lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(),
+                                                     ctypes.byref(self.handle)) != 0:
+            self.lib.nvmlShutdown()
+            raise OSError(f"no NVML device at {pci_bus_id}")
+        self.reasons_fn = (getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or
+                           getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+        v = ctypes.c_uint()
+        self.max_mhz = (float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, self.CLOCK_SM, ctypes.byref(v)) == 0 else None)
+
+    def sample(self, with_power: bool):
+        """(sm MHz, max MHz, power W or None, set of reason names), or None on an error."""
+        ct = self.ct
+        v = ct.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, self.CLOCK_SM, ct.byref(v)) != 0:
+            return None
+        sm = float(v.value)
+        power = None
+        if with_power and self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(v)) == 0:
+            power = v.value / 1000.0
+        reasons = set()
+        if self.reasons_fn is not None:
+            r = ct.c_ulonglong()
+            if self.reasons_fn(self.handle, ct.byref(r)) == 0:
+                reasons = {n for n, bit in self.REASON_BITS.items() if r.value & bit}
+        return sm, (self.max_mhz if self.max_mhz is not None else sm), power, reasons
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+def pci_bus_id_of(index: int):
+    """NVML-style PCI bus id (domain:bus:device.function) of CUDA device `index`."""
+    import torch
+    p = torch.cuda.get_device_properties(index)
+    try:
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except AttributeError:
+        return None
+
+
+class ClockSampler:
+    """SM clocks, power and throttle reasons sampled while running.
+
+    Preferred source: NVML, polled from a thread every `period_ms` (2 ms by default, so
+    that a timed region of a few milliseconds still holds samples).  Fallback: nvidia-smi
+    at its 100 ms loop.  Every sample carries a host timestamp (time.time()), so
+    ``summary(t0, t1)`` can keep only the samples taken inside a timed window."""
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: float = 2.0, nvml=None):
         self.gpu_index = gpu_index
         self.period_ms = period_ms
+        self.nvml = nvml          # an NvmlReader, made in start() when not given
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.lines = []           # nvidia-smi CSV lines (fallback)
+        self.polled = []          # NVML samples (t, sm, smax, power, reasons)
+        self.source = None
         self.error = None
+        self._stop = threading.Event()
 
     def start(self):
+        if self.nvml is None:
+            try:
+                bus = pci_bus_id_of(self.gpu_index)
+                if bus is not None:
+                    self.nvml = NvmlReader(bus)
+            except (OSError, AttributeError, RuntimeError) as e:
+                self.error = f"NVML: {e}"
+                self.nvml = None
+        if self.nvml is not None:
+            self.source = f"NVML every {self.period_ms:g} ms"
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi every 100 ms"
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError as e:
             self.error = str(e)
+
+    def _poll(self):
+        n = 0
+        while not self._stop.is_set():
+            # Board power is the slowest query: every 10th sample only.
+            x = self.nvml.sample(with_power=(n % 10 == 0))
+            if x is not None:
+                self.polled.append((time.time(),) + x)
+            n += 1
+            self._stop.wait(self.period_ms / 1000.0)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -112,7 +200,7 @@ class ClockSampler:
 
     def _samples(self):
         import datetime
-        out = []
+        out = list(self.polled)
         for line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
@@ -146,17 +234,25 @@ class ClockSampler:
                "power_w_max": max(power) if power else None}
         if t0 is not None:
             res["window_s"] = t1 - t0
+        if self.source:
+            res["source"] = self.source
         return res
 
     def stop(self):
-        if self.proc is None:
-            return
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=2)
+        self._stop.set()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        if self.nvml is not None:
+            try:
+                self.nvml.close()
+            except OSError:
+                pass
 
 
 def dist_setup(n_gpus: int):
@@ -341,6 +437,18 @@ class ForwardSetup:
         else:
             self.ws_bytes = 0
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev) if self.ws_bytes else None
+        # The schedule the library takes (its own answer, not a guess from the sizes).
+        if w.window is not None:
+            self.schedule = "local-window band"
+        elif self.kv_len is not None:
+            self.schedule = "band (key padding)"
+        else:
+            st, sc = fa.fa_fwd_schedule(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
+            if st != fa.FA_OK:
+                raise RuntimeError(fa.fa_status_string(st))
+            self.schedule = {fa.FA_SCHED_WHOLE: "whole units",
+                             fa.FA_SCHED_SPLIT: "split key ranges",
+                             fa.FA_SCHED_TABLE: "whole units in host-computed table order"}[sc]
         self.left, self.right = w.window if w.window is not None else (-1, 0 if w.causal else -1)
         self.code = fa.FA_DTYPE_FP16 if dtype == "fp16" else fa.FA_DTYPE_BF16
         torch.cuda.synchronize(dev)
@@ -442,7 +550,7 @@ def measure_config(fa, w, dev, stream, peaks, peak_src, seconds, no_clocks):
         setup.launch(i)
     host_us = (time.perf_counter() - h0) / 100 * 1e6
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev.index)
+    sampler = ClockSampler(dev.index, period_ms=20.0)
     if not no_clocks:
         sampler.start()
         time.sleep(0.3)
@@ -467,7 +575,7 @@ def measure_config(fa, w, dev, stream, peaks, peak_src, seconds, no_clocks):
     entry = {"workload": w.name, "shape": w.describe(), "steps": steps,
              "ms_per_step": total_ms / steps, "tflops": flops / per_launch_s / 1e12,
              "us_per_step": total_ms / steps * 1e3, "host_us_per_launch": host_us,
-             "schedule": ("split key ranges" if setup.ws_bytes else "whole units"),
+             "schedule": setup.schedule,
              "roofline": roofline_of(setup, flops, per_launch_s, peaks, peak_src,
                                      measured_traffic(w.name), sustained=True),
              "clocks": clocks}
@@ -571,6 +679,7 @@ def run_ours(args, w):
     in_bytes, out_bytes, ws_bytes, n_copies = (setup.in_bytes, setup.out_bytes, setup.ws_bytes,
                                                setup.n_copies)
     kv_len_h = setup.kv_len_h
+    schedule = setup.schedule
     peaks, peak_src = load_peaks()
     traffic = measured_traffic(w.name) if not variant else None   # measured on bf16, [B,H,L,D]
     roofline = roofline_of(setup, flops, per_launch_s, peaks, peak_src, traffic)
@@ -655,8 +764,7 @@ def run_ours(args, w):
                        "l2": f"inputs rotate over {n_copies} copies "
                              f"({n_copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
                        "parallelism": f"replica per GPU x{world}",
-                       "schedule": ("local-window band" if w.window is not None else
-                                    "split key ranges" if ws_bytes else "whole units"),
+                       "schedule": schedule,
                        "workspace_bytes": ws_bytes},
             "pct_of_peak": 100.0 * kernel_tflops / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,

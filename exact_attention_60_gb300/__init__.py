@@ -8,10 +8,12 @@ from __future__ import annotations
 import math
 
 from ._native import (FA_DTYPE_BF16, FA_DTYPE_FP16, FA_ERR_CUDA, FA_ERR_INVALID_ARG,
-                      FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, fa_bwd, fa_bwd_masked,
+                      FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, FA_SCHED_BAND, FA_SCHED_SPLIT,
+                      FA_SCHED_TABLE, FA_SCHED_WHOLE, fa_bwd, fa_bwd_masked,
                       fa_bwd_strided, fa_bwd_workspace_size,
                       fa_debug_set, fa_fwd, fa_fwd_host, fa_fwd_host_workspace_size,
-                      fa_fwd_noalloc, fa_fwd_strided, fa_fwd_window, fa_fwd_workspace_size,
+                      fa_fwd_noalloc, fa_fwd_schedule, fa_fwd_strided, fa_fwd_window,
+                      fa_fwd_workspace_size,
                       fa_fwd_ws, fa_last_device_status, fa_status_string)
 
 

@@ -18,9 +18,13 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP16 = 1
+FA_SCHED_WHOLE = 0
+FA_SCHED_SPLIT = 1
+FA_SCHED_BAND = 2
+FA_SCHED_TABLE = 3
 
 # Every symbol include/fa.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_strided",
+EXPORTED = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_schedule", "fa_fwd_ws", "fa_fwd_window", "fa_fwd_strided",
             "fa_fwd_noalloc", "fa_fwd_host_workspace_size", "fa_fwd_host",
             "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_masked", "fa_bwd_strided", "fa_status_string",
             "fa_last_device_status",
@@ -44,6 +48,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
     lib.fa_fwd_workspace_size.restype = ctypes.c_int
     lib.fa_fwd_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_fwd_schedule.restype = ctypes.c_int
+    lib.fa_fwd_schedule.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int)]
     lib.fa_fwd_ws.restype = ctypes.c_int
     lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp,
@@ -113,6 +119,14 @@ def fa_fwd_workspace_size(B, H, Lq, Lk, D, causal):
     st = load().fa_fwd_workspace_size(int(B), int(H), int(Lq), int(Lk), int(D),
                                       int(bool(causal)), ctypes.byref(n))
     return st, int(n.value)
+
+
+def fa_fwd_schedule(B, H, Lq, Lk, D, causal):
+    """C ``fa_fwd_schedule``: returns (status, FA_SCHED_* code)."""
+    sc = ctypes.c_int(0)
+    st = load().fa_fwd_schedule(int(B), int(H), int(Lq), int(Lk), int(D), int(bool(causal)),
+                                ctypes.byref(sc))
+    return st, int(sc.value)
 
 
 def fa_fwd_ws(Q, K, V, O, LSE, B, H, Lq, Lk, D, causal, scale, workspace, workspace_bytes,

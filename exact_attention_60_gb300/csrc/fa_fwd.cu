@@ -1738,31 +1738,63 @@ extern "C" fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O
   return launch(pr, sm_count, pl, nullptr, stream);
 }
 
+namespace {
+// The problem fa_fwd_ws would plan, from sizes alone (no pointers).  *empty = true: no work.
+fa_status sized_problem(int B, int H, int Lq, int Lk, int D, int causal, Problem* pr,
+                        int* sm_count, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * Lq == 0) {
+    *empty = true;
+    return FA_OK;
+  }
+  if (Lk < 1) return FA_ERR_INVALID_ARG;
+  const long long n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+  if (bh > INT_MAX || n_pairs * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  const fa_status prep = current_device(D, sm_count);
+  if (prep != FA_OK) return prep;
+  *pr = Problem{};
+  pr->Lq = Lq;
+  pr->Lk = Lk;
+  pr->D = D;
+  pr->causal = causal ? 1 : 0;
+  pr->bh = bh;
+  pr->n_pairs = static_cast<int>(n_pairs);
+  pr->n_units = static_cast<int>(n_pairs * bh);
+  pr->nkv = (Lk + fa::kBlockN - 1) / fa::kBlockN;
+  pr->B = B;
+  pr->H = H;
+  return FA_OK;
+}
+}  // namespace
+
 extern "C" fa_status fa_fwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
                                            size_t* bytes) {
   if (!bytes) return FA_ERR_INVALID_ARG;
   *bytes = 0;
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  const long long bh = static_cast<long long>(B) * H;
-  if (bh * Lq == 0) return FA_OK;
-  if (Lk < 1) return FA_ERR_INVALID_ARG;
-  const long long n_pairs = (Lq + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-  if (bh > INT_MAX || n_pairs * bh > INT_MAX) return FA_ERR_INVALID_ARG;
+  Problem pr;
   int sm_count = 0;
-  const fa_status prep = current_device(D, &sm_count);
-  if (prep != FA_OK) return prep;
-  Problem pr{};
-  pr.Lq = Lq;
-  pr.Lk = Lk;
-  pr.D = D;
-  pr.causal = causal ? 1 : 0;
-  pr.bh = bh;
-  pr.n_pairs = static_cast<int>(n_pairs);
-  pr.n_units = static_cast<int>(n_pairs * bh);
-  pr.nkv = (Lk + fa::kBlockN - 1) / fa::kBlockN;
+  bool empty = false;
+  const fa_status st = sized_problem(B, H, Lq, Lk, D, causal, &pr, &sm_count, &empty);
+  if (st != FA_OK || empty) return st;
   const Plan pl = plan_schedule(pr, sm_count);
   *bytes = pl.split ? pl.ws_bytes : 0;
+  return FA_OK;
+}
+
+extern "C" fa_status fa_fwd_schedule(int B, int H, int Lq, int Lk, int D, int causal,
+                                     int* schedule) {
+  if (!schedule) return FA_ERR_INVALID_ARG;
+  *schedule = FA_SCHED_WHOLE;
+  Problem pr;
+  int sm_count = 0;
+  bool empty = false;
+  const fa_status st = sized_problem(B, H, Lq, Lk, D, causal, &pr, &sm_count, &empty);
+  if (st != FA_OK || empty) return st;
+  const Plan pl = plan_schedule(pr, sm_count);
+  *schedule = pl.split ? FA_SCHED_SPLIT : table_eligible(pr, pl) ? FA_SCHED_TABLE : FA_SCHED_WHOLE;
   return FA_OK;
 }
 

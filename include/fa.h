@@ -124,6 +124,31 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
                     int B, int H, int Lq, int Lk, int D, int causal, float scale,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Work schedules of the forward kernel, as fa_fwd_schedule reports them. */
+typedef enum {
+    FA_SCHED_WHOLE = 0,   /* whole units, heaviest first in a fixed order */
+    FA_SCHED_SPLIT = 1,   /* key ranges cut across CTAs, merged by a second kernel */
+    FA_SCHED_BAND = 2,    /* band-limited units (fa_fwd_window, key padding) */
+    FA_SCHED_TABLE = 3    /* whole units in an order computed on the host */
+} fa_schedule;
+
+/*
+ * fa_fwd_schedule -- the schedule fa_fwd_ws takes for this problem on the current
+ * device, given a workspace of the size fa_fwd_workspace_size reports, in *schedule:
+ *   FA_SCHED_SPLIT  when that size is nonzero (two kernels per call);
+ *   FA_SCHED_TABLE  for causal problems whose heads' K and V take more than 48 MiB: the
+ *                   host deals the units out head group by head group (about 32 MiB of
+ *                   K/V per group, each unit to the least-loaded CTA), so a group's K/V
+ *                   tiles stay in the L2 cache while its units run;
+ *   FA_SCHED_WHOLE  otherwise.
+ * The table and the fixed order give bit-identical results; the split schedule differs
+ * only in the merge's summation order (see fa_fwd_ws).  fa_fwd (no workspace) takes the
+ * same schedule except that it never splits.  Follows fa_debug_set (bit 4 turns the
+ * table order off).  Errors as fa_fwd_workspace_size (schedule == NULL:
+ * FA_ERR_INVALID_ARG); B*H*Lq == 0 gives FA_SCHED_WHOLE.
+ */
+fa_status fa_fwd_schedule(int B, int H, int Lq, int Lk, int D, int causal, int* schedule);
+
 /*
  * fa_fwd_window -- local (sliding-window) attention: the operation of fa_fwd with
  * the allowed keys of row i restricted to a band around it,

@@ -117,6 +117,14 @@ def test_workspace_size_rejects_bad_arguments(lib):
     assert lib.fa_fwd_workspace_size(1, 1, 16, 16, 64, 0, None) == fa.FA_ERR_INVALID_ARG
 
 
+def test_schedule_query_rejects_bad_arguments(lib):
+    assert fa.fa_fwd_schedule(1, 1, 16, 16, 96, 1)[0] == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_schedule(1, -1, 16, 16, 64, 1)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_schedule(1, 1, 16, 0, 64, 1)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_schedule(2, 3, 0, 16, 128, 1) == (fa.FA_OK, fa.FA_SCHED_WHOLE)
+    assert lib.fa_fwd_schedule(1, 1, 16, 16, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("kw,expect", [(dict(D=96), fa.FA_ERR_UNSUPPORTED), (dict(Lk=0), fa.FA_ERR_INVALID_ARG),
                                        (dict(Q=0), fa.FA_ERR_INVALID_ARG), (dict(scale=0.0), fa.FA_ERR_INVALID_ARG)])
 def test_fwd_ws_rejects_bad_arguments_before_any_cuda_call(lib, kw, expect):

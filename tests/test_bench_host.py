@@ -122,6 +122,65 @@ def test_clock_sampler_keeps_samples_inside_the_window():
     assert bench.ClockSampler(0).summary()["error"]
 
 
+class _FakeNvml:
+    """Stand-in for the NVML library: a clock that steps through `mhz`, and the
+    sw_power_cap reason bit from the third sample on."""
+    def __init__(self, mhz):
+        self.mhz = list(mhz)
+        self.n = 0
+        self.closed = False
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlShutdown(self):
+        self.closed = True
+        return 0
+
+    def nvmlDeviceGetHandleByPciBusId_v2(self, bus, ref):
+        assert bus == b"00000000:01:00.0"
+        ref._obj.value = 1234
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, h, clock, ref):
+        assert clock == 1
+        ref._obj.value = 2070
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, clock, ref):
+        ref._obj.value = self.mhz[min(self.n, len(self.mhz) - 1)]
+        self.n += 1
+        return 0
+
+    def nvmlDeviceGetPowerUsage(self, h, ref):
+        ref._obj.value = 1380000   # milliwatts
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, ref):
+        ref._obj.value = 0x4 | 0x1 if self.n >= 3 else 0x1   # sw_power_cap (+ idle bit)
+        return 0
+
+
+def test_nvml_sampler_reads_clocks_power_and_reasons_from_a_fake_library():
+    import time as _time
+    lib = _FakeNvml([2070, 2070, 1800, 1700, 1700])
+    reader = bench.NvmlReader("00000000:01:00.0", lib=lib)
+    assert reader.max_mhz == 2070.0
+    sm, smax, power, reasons = reader.sample(with_power=True)
+    assert (sm, smax, power, reasons) == (2070.0, 2070.0, 1380.0, set())
+    s = bench.ClockSampler(0, period_ms=1.0, nvml=reader)
+    t0 = _time.time()
+    s.start()
+    _time.sleep(0.05)
+    s.stop()
+    t1 = _time.time()
+    r = s.summary(t0, t1)
+    assert lib.closed and r["source"].startswith("NVML")
+    assert r["samples_in_window"] >= 5 and r["sm_max_mhz"] == 2070.0
+    assert r["reasons"] == ["sw_power_cap"] and r["power_w_max"] == 1380.0
+    assert r["sm_mhz"] == 1700.0    # most samples sit at the last clock
+
+
 def test_per_config_covers_every_specified_configuration():
     """C1, C2 (both masks), C3, C4 and C5 of the specification, each once."""
     shapes = {(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)

@@ -73,3 +73,26 @@ def test_table_order_on_strided_fp16_and_window_entry_points():
         a = run(q, k, v, fn, 0)
         b = run(q, k, v, fn, 16)
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("B,H,L,D,causal,expect", [
+    (1, 16, 16384, 128, 1, fa.FA_SCHED_TABLE),   # 128 MiB of K/V
+    (2, 32, 4096, 128, 1, fa.FA_SCHED_TABLE),
+    (1, 1, 16384, 128, 1, fa.FA_SCHED_SPLIT),    # one long head: key ranges split
+    (4, 16, 1024, 64, 1, fa.FA_SCHED_WHOLE),     # 16 MiB of K/V stay in L2
+    (4, 16, 1024, 64, 0, fa.FA_SCHED_WHOLE),
+    (1, 4, 2048, 128, 0, fa.FA_SCHED_SPLIT)])    # 16 units on 152 SMs
+def test_schedule_query_names_the_schedule_taken(B, H, L, D, causal, expect):
+    """fa_fwd_schedule agrees with the workspace query (split iff a workspace is needed)
+    and reports the table order exactly when it is on (debug bit 4 turns it off)."""
+    st, sc = fa.fa_fwd_schedule(B, H, L, L, D, causal)
+    assert st == fa.FA_OK and sc == expect
+    st, ws = fa.fa_fwd_workspace_size(B, H, L, L, D, causal)
+    assert st == fa.FA_OK and (ws > 0) == (sc == fa.FA_SCHED_SPLIT)
+    fa.fa_debug_set(16, 0)
+    try:
+        st, sc_off = fa.fa_fwd_schedule(B, H, L, L, D, causal)
+    finally:
+        fa.fa_debug_set(0, 0)
+    assert st == fa.FA_OK
+    assert sc_off == (fa.FA_SCHED_WHOLE if expect == fa.FA_SCHED_TABLE else expect)
