@@ -187,8 +187,8 @@ class ClockSampler:
     def _poll(self):
         n = 0
         while not self._stop.is_set():
-            # Board power is the slowest query: every 10th sample only.
-            x = self.nvml.sample(with_power=(n % 10 == 0))
+            # Board power is the slowest query: every other sample only.
+            x = self.nvml.sample(with_power=(n % 2 == 0))
             if x is not None:
                 self.polled.append((time.time(),) + x)
             n += 1

@@ -228,6 +228,68 @@ def test_scheduler_shapes(oracle_mod, B, H, Lq, Lk, causal, D):
                o, lse)
 
 
+@pytest.mark.parametrize("B,H,Lq,Lk,D,causal,sched", [
+    (4, 64, 4096, 4096, 64, True, fa.FA_SCHED_TABLE),      # 4096 units: the host table's limit
+    (5, 64, 4096, 4096, 64, True, fa.FA_SCHED_WHOLE),      # 5120 units: past it, fixed order
+    (1, 1, 131072, 131072, 128, True, fa.FA_SCHED_TABLE),  # one head of 128K tokens (64 MiB of K/V)
+    (1, 2, 256, 1 << 20, 64, False, fa.FA_SCHED_SPLIT),    # a million keys per row
+    (1, 65536, 64, 64, 64, False, fa.FA_SCHED_WHOLE),      # 65,536 heads of one short tile
+])
+def test_size_limits(oracle_mod, B, H, Lq, Lk, D, causal, sched):
+    """The largest shapes each schedule is built for, and one past the host table's limit:
+    the schedule the library reports, then sampled rows (first, last, tile edges) against
+    the oracle."""
+    assert fa.fa_fwd_schedule(B, H, Lq, Lk, D, causal) == (fa.FA_OK, sched)
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed=(B * H + Lq + Lk) % 100003)
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse = o.cpu(), lse.cpu()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    BH = B * H
+    rng = np.random.default_rng(BH + Lq)
+    n = 24 if Lk >= 1 << 17 else 96
+    pairs = np.stack([rng.integers(0, BH, n), rng.integers(0, Lq, n)], axis=1)
+    edge = np.array([[0, 0], [BH - 1, Lq - 1], [BH - 1, 0], [0, Lq - 1],
+                     [BH // 2, min(Lq - 1, 127)], [BH // 2, min(Lq - 1, 128)]])
+    check_rows(oracle_mod, q, k, v, causal, 1.0 / math.sqrt(D), np.concatenate([pairs, edge]),
+               o, lse)
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,D,causal", [(1, 2, 300, 300, 64, True),
+                                                 (2, 1, 129, 1000, 128, False),
+                                                 (1, 3, 600, 600, 128, True)])
+@pytest.mark.parametrize("level", [0.0, 64.0])
+def test_equal_scores_give_the_mean_of_v(B, H, Lq, Lk, D, causal, level):
+    """Degenerate softmax: every allowed key of a row has the same score s, so the row's
+    weights are uniform.  Closed form (no oracle): O_i = the mean of the allowed V rows,
+    LSE_i = s + ln(n_i), n_i = i + 1 (causal) or Lk.  With level 64 the scores are
+    64 * 64 / sqrt(D) (362 at D = 128), whose exponentials overflow fp32 unless the row
+    maximum is subtracted first."""
+    g = torch.Generator().manual_seed(Lq + Lk + D)
+    q = torch.zeros(B, H, Lq, D)
+    k = torch.zeros(B, H, Lk, D)
+    q[..., 0] = level
+    k[..., 0] = level
+    v = torch.randn(B, H, Lk, D, generator=g).to(torch.bfloat16)
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse = o.float().cpu().double(), lse.cpu().double()
+    vd = v.double()
+    if causal:
+        n = torch.arange(1, Lq + 1, dtype=torch.float64)
+        ref_o = vd[:, :, :Lq].cumsum(2) / n[:, None]
+    else:
+        n = torch.full((Lq,), float(Lk), dtype=torch.float64)
+        ref_o = vd.mean(2, keepdim=True).expand(B, H, Lq, D)
+    s = level * level / math.sqrt(D)
+    ref_l = (s + torch.log(n)).expand(B, H, Lq)
+    assert float((o - ref_o).abs().max()) <= TOL_O
+    assert float((lse - ref_l).abs().max()) <= TOL_LSE
+
+
 # non-causal shapes with few units (query-tile pairs) per SM: the split-key schedule
 SPLIT_SHAPES = [(1, 4, 2048, 32768, 128), (1, 8, 2048, 16384, 128), (1, 4, 2048, 32768, 64),
                 (1, 2, 256, 256, 64), (3, 5, 700, 1300, 128), (1, 1, 128, 40000, 128),
