@@ -100,13 +100,18 @@ struct Layout {
   // writes O / l there and one TMA store moves the tile to global memory).
   static constexpr int kQBufs = (HD == 64) ? 2 : 1;
   static constexpr bool kTmaStoreO = (HD == 64);
-  static constexpr int kOffQ = 0;                        // Q_i of buffer b: kOffQ + (2b + i) * kTileBytes
-  static constexpr int kOffKV = 2 * kQBufs * kTileBytes;
+  // D = 128: three Q buffers used as a ring by both tiles (a unit takes the next one or
+  // two), so the next unit's Q_0 loads at any time and its Q_1 once tile 0 of the current
+  // unit is done.
+  static constexpr bool kQRing = (HD == 128);
+  static constexpr int kQSlots = kQRing ? 3 : 2 * kQBufs;
+  static constexpr int kOffQ = 0;                        // Q buffer b at kOffQ + b * kTileBytes
+  static constexpr int kOffKV = kQSlots * kTileBytes;
   static constexpr int kOffStage = kOffKV + kStages * kTileBytes;   // [2] O staging (D = 64)
   static constexpr int kOffBar = kOffStage + (kTmaStoreO ? 2 : 0) * kTileBytes;
-  static constexpr int kBarQFull = 0;                    // [2 kQBufs]  Q_i of buffer b landed (2b + i)
-  static constexpr int kBarQEmpty = 2 * kQBufs;          // [2 kQBufs]  last MMA reading it done
-  static constexpr int kBarKVFull = 4 * kQBufs;          // [kStages]
+  static constexpr int kBarQFull = 0;                    // [kQSlots]  Q buffer landed
+  static constexpr int kBarQEmpty = kQSlots;             // [kQSlots]  last MMA reading it done
+  static constexpr int kBarKVFull = 2 * kQSlots;         // [kStages]
   static constexpr int kBarKVEmpty = kBarKVFull + kStages;
   static constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_i in TMEM
   static constexpr int kBarPFull = kBarSFull + 2;           // [2] P_i in TMEM, O_i rescaled
@@ -473,7 +478,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int i = 0; i < 2 * L::kQBufs; ++i) {
+    for (int i = 0; i < L::kQSlots; ++i) {
       ptx::mbar_init(bar(L::kBarQFull + i), 1);
       ptx::mbar_init(bar(L::kBarQEmpty + i), 1);
     }
@@ -776,25 +781,27 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         ++n_stage;
       } else {
       uint16_t* orow = p.o + ob * p.o_sb + oh * p.o_sh + static_cast<long long>(store ? q : 0) * p.o_sl;
+      // Read the whole row of O first and release O_i (the next unit's first P_i V MMA
+      // may overwrite it), then normalise and store from registers.
+      uint32_t o[HD / 32][32];
 #pragma unroll
-      for (int c0 = 0; c0 < HD; c0 += 32) {
-        uint32_t o[32];
-        ptx::tmem_ld32x32b_x32(t_o + c0, o);
+      for (int k = 0; k < HD / 32; ++k) ptx::tmem_ld32x32b_x32(t_o + 32 * k, o[k]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
+#pragma unroll
+      for (int k = 0; k < HD / 32; ++k) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = pack2<kF16>(__uint_as_float(o[2 * c]) * inv_l,
-                              __uint_as_float(o[2 * c + 1]) * inv_l);
+          pk[c] = pack2<kF16>(__uint_as_float(o[k][2 * c]) * inv_l,
+                              __uint_as_float(o[k][2 * c + 1]) * inv_l);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      // O_i has been read into registers: the next unit's P_i V MMA may overwrite it.
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
       }
       if (store) {
         p.lse[static_cast<size_t>(bh) * p.Lq + q] = (m + log2f(l)) * 0.69314718055994531f;
@@ -808,6 +815,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       ptx::prefetch_tensormap(&p.tm_k);
       ptx::prefetch_tensormap(&p.tm_v);
       uint32_t q_count[2] = {0, 0};   // Q_i loads issued so far
+      uint32_t q_pos = 0;             // Q ring position of the next load (kQRing)
       uint32_t it = 0;                // K/V ring position (K_j and V_j alternate)
       int last_fill[L::kStages];
 #pragma unroll
@@ -822,8 +830,16 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           if (u.nblk[i] == 0) continue;
           // Buffers alternate between units (D = 64); a buffer is refilled once the MMAs of
           // its previous unit have read it.  uses = earlier loads into this buffer.
-          const int qi = 2 * (L::kQBufs == 2 ? static_cast<int>(q_count[i] & 1) : 0) + i;
-          const uint32_t uses = L::kQBufs == 2 ? (q_count[i] >> 1) : q_count[i];
+          int qi;
+          uint32_t uses;
+          if constexpr (L::kQRing) {
+            qi = static_cast<int>(q_pos % 3u);
+            uses = q_pos / 3u;
+            ++q_pos;
+          } else {
+            qi = 2 * (L::kQBufs == 2 ? static_cast<int>(q_count[i] & 1) : 0) + i;
+            uses = L::kQBufs == 2 ? (q_count[i] >> 1) : q_count[i];
+          }
           if (uses > 0 && !wait_phase(bar(L::kBarQEmpty + qi), (uses - 1) & 1,
                                       abort_flag, limit, kSiteLoadKV)) {
             ok = false;
@@ -862,13 +878,21 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       for (int s = 0; s < L::kStages; ++s)
         if (last_fill[s] >= 0)
           drain_phase(bar(L::kBarKVFull + s), (last_fill[s] / L::kStages) & 1, limit);
+      if constexpr (L::kQRing) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+        for (int b = 0; b < 3; ++b) {   // loads into ring buffer b: positions b, b + 3, ...
+          const uint32_t n = (q_pos + 2u - b) / 3u;
+          if (n > 0) drain_phase(bar(L::kBarQFull + b), (n - 1) & 1, limit);
+        }
+      } else {
 #pragma unroll
-        for (int b = 0; b < L::kQBufs; ++b) {
-          // loads into buffer b of tile i: every kQBufs-th load, starting with load b
-          const uint32_t n = (q_count[i] + L::kQBufs - 1 - b) / L::kQBufs;
-          if (n > 0) drain_phase(bar(L::kBarQFull + 2 * b + i), (n - 1) & 1, limit);
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+          for (int b = 0; b < L::kQBufs; ++b) {
+            // loads into buffer b of tile i: every kQBufs-th load, starting with load b
+            const uint32_t n = (q_count[i] + L::kQBufs - 1 - b) / L::kQBufs;
+            if (n > 0) drain_phase(bar(L::kBarQFull + 2 * b + i), (n - 1) & 1, limit);
+          }
         }
       }
     }
@@ -885,15 +909,34 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       const uint64_t desc_q0 = sw128_desc(sbase + L::kOffQ, 16, 1024);
       const uint64_t desc_kv0 = sw128_desc(sbase + L::kOffKV, 16, 1024);
       const uint64_t desc_v0 = sw128_desc(sbase + L::kOffKV, L::kRegionBytes, 1024);
-      uint32_t q_count[2] = {0, 0};   // units in which tile i was present (q_full / o_empty phase)
-      // Q_i of the current unit is in buffer q_count[i] % kQBufs (index 2b + i): the
-      // buffers alternate between units when kQBufs = 2.
-      uint32_t q_alt = 0;             // bit i: tile i of the current unit uses buffer 1
-      auto q_buf = [&](int i) -> int { return 2 * static_cast<int>((q_alt >> i) & 1u) + i; };
-      // Phase of q_full for that buffer: the number of earlier loads into it.
-      auto q_phase = [&](int i) -> uint32_t {
-        return (L::kQBufs == 2 ? (q_count[i] >> 1) : q_count[i]) & 1;
+      uint32_t q_count[2] = {0, 0};   // units in which tile i was present (o_empty phase)
+      uint32_t q_pos = 0;             // Q ring position of the next unit's first tile (kQRing)
+      // Buffer of Q_i in the current unit and the phase of its q_full (the number of
+      // earlier loads into it): ring positions in load order (kQRing), else buffer
+      // 2b + i with b alternating between units when kQBufs = 2.
+      int qb[2] = {0, 1};
+      uint32_t qp[2] = {0, 0};
+      auto set_q = [&](const int* nb) {
+        if constexpr (L::kQRing) {
+          uint32_t pos = q_pos;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (nb[i] > 0) {
+              qb[i] = static_cast<int>(pos % 3u);
+              qp[i] = (pos / 3u) & 1u;
+              ++pos;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            qb[i] = 2 * (L::kQBufs == 2 ? static_cast<int>(q_count[i] & 1u) : 0) + i;
+            qp[i] = (L::kQBufs == 2 ? (q_count[i] >> 1) : q_count[i]) & 1u;
+          }
+        }
       };
+      auto q_buf = [&](int i) -> int { return qb[i]; };
+      auto q_phase = [&](int i) -> uint32_t { return qp[i]; };
       auto issue_s = [&](int i, int slot) {
         const uint64_t a = desc_q0 + ((q_buf(i) * L::kTileBytes) >> 4);
         const uint64_t b = desc_kv0 + ((slot * L::kTileBytes) >> 4);
@@ -926,6 +969,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           const int nblk[2] = {u.nblk[0], u.nblk[1]};
           const int nmax = u.nmax;
           const int fst[2] = {0, kBand ? u.first[1] : 0};
+          set_q(nblk);
 #pragma unroll
           for (int i = 0; i < 2; ++i)
             if (ok && nblk[i] > 0)
@@ -1014,13 +1058,14 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
             p_base[i] += nblk[i];
             if (nblk[i] > 0) ++q_count[i];
           }
-          if (L::kQBufs == 2) q_alt = (q_count[0] & 1u) | ((q_count[1] & 1u) << 1);
+          if constexpr (L::kQRing) q_pos += (nblk[0] > 0 ? 1u : 0u) + (nblk[1] > 0 ? 1u : 0u);
         }
       }
       for (int r = 0; !L::kDecoupled && ok && unit_of<kS>(p, r, u); ++r) {
         if (kBand && u.nmax == 0) continue;   // no keys at all (key padding): nothing to issue
         const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
         const int nblk[2] = {nb0, nb1};
+        set_q(nblk);
         // Step j of the unit (key tile kv0 + j) is step j - fst[i] of query tile i.
         const int fst[2] = {0, kBand ? u.first[1] : 0};
 #pragma unroll
@@ -1125,7 +1170,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           p_base[i] += nblk[i];
           if (nblk[i] > 0) ++q_count[i];
         }
-        if (L::kQBufs == 2) q_alt = (q_count[0] & 1u) | ((q_count[1] & 1u) << 1);
+        if constexpr (L::kQRing) q_pos += (nblk[0] > 0 ? 1u : 0u) + (nblk[1] > 0 ? 1u : 0u);
       }
       // Drain: every MMA issued has completed before TMEM is freed.
       ptx::mma_commit_warp(bar(L::kBarDrain));
