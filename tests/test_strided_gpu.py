@@ -53,6 +53,34 @@ def test_strided_output_equals_contiguous():
     assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("layout", ["offset16", "rowpad8"])
+def test_output_aligned_to_16_bytes_only(layout, causal):
+    """At D = 128 the epilogue stores O 32 bytes a time when O's base and strides allow it;
+    an output that is only 16-byte aligned (its base 16 bytes into a buffer, or rows
+    padded by 8 elements) takes the 16-byte stores.  Same bits as the contiguous call, and
+    nothing outside the output written."""
+    B, H, L, D = 2, 3, 300, 128
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, L, L, D, seed=17))
+    o_ref, l_ref = fa.attention(q, k, v, causal=causal, split=False)
+    n = B * H * L * D
+    if layout == "offset16":
+        buf = torch.full((n + 16,), 7.0, dtype=torch.bfloat16, device=DEV)
+        out = buf[8:8 + n].view(B, H, L, D)
+        assert out.data_ptr() % 32 == 16
+    else:
+        buf = torch.full((B, H, L, D + 8), 7.0, dtype=torch.bfloat16, device=DEV)
+        out = buf[..., :D]
+        assert out.stride(2) * 2 % 32 == 16
+    o, lse = fa.attention(q, k, v, causal=causal, out=out, split=False)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
+    if layout == "offset16":
+        assert bool((buf[:8] == 7.0).all()) and bool((buf[8 + n:] == 7.0).all())
+    else:
+        assert bool((buf[..., D:] == 7.0).all())
+
+
 @pytest.mark.parametrize("window", [(100, 0), (64, 64), (-1, 3)])
 def test_strided_band_equals_contiguous(window):
     (qv, kv, vv), (q, k, v) = packed_qkv(2, 2, 700, 128, seed=11)
