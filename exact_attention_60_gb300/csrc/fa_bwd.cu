@@ -154,6 +154,7 @@ struct BwdParams {
   uint16_t* dk;
   uint16_t* dv;
   long long dq_s[3], dk_s[3], dv_s[3];   // element strides {batch, head, row}
+  int dq_v8, dkv_v8;   // dQ / dK and dV: base and strides multiples of 32 bytes (32-byte stores)
   int bh_count;
   int H;
   int Lq;
@@ -517,25 +518,33 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       ++acc_count;
       ptx::tc_fence_after();
       {
+        // The whole accumulator row first, released at once (the next unit's first dV / dK
+        // MMA may overwrite it), then scaled, packed and stored from registers.
         const uint32_t t_acc = tmem + lane_off + (g ? L::kColDk : L::kColDv);
         const float mul = g ? p.scale : 1.0f;
+        uint32_t a[HD / 32][32];
 #pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-          uint32_t a[32];
-          ptx::tmem_ld32x32b_x32(t_acc + c0, a);
+        for (int k2 = 0; k2 < HD / 32; ++k2) ptx::tmem_ld32x32b_x32(t_acc + 32 * k2, a[k2]);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarAccEmpty));
+#pragma unroll
+        for (int k2 = 0; k2 < HD / 32; ++k2) {
           uint32_t pk16[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            pk16[c] = pack2<kF16>(__uint_as_float(a[2 * c]) * mul, __uint_as_float(a[2 * c + 1]) * mul);
+            pk16[c] = pack2<kF16>(__uint_as_float(a[k2][2 * c]) * mul, __uint_as_float(a[k2][2 * c + 1]) * mul);
           if (k < p.Lk) {
+            if (p.dkv_v8) {
+              ptx::st_global_v8(mine + 32 * k2, pk16);
+              ptx::st_global_v8(mine + 32 * k2 + 16, pk16 + 8);
+            } else {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              reinterpret_cast<uint4*>(mine + c0)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+              for (int v = 0; v < 4; ++v)
+                reinterpret_cast<uint4*>(mine + 32 * k2)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+            }
           }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::kBarAccEmpty));
     }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------ load warp
@@ -897,22 +906,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (threadIdx.x == 0) ptx::mbar_arrive(bar(L::kBarKEmpty + static_cast<int>((it - 1) % L::kKStages)));
       // Epilogue: each warpgroup writes its half of the row's columns.
       uint16_t* dst = p.dq + row_offset(p.dq_s, p.H, bh, valid ? q : 0) + (HD / 2) * g;
+      // This warpgroup's half of the row first, released at once, then stored.
+      uint32_t a[HD / 64][32];
 #pragma unroll
-      for (int c0 = 0; c0 < HD / 2; c0 += 32) {
-        uint32_t a[32];
-        ptx::tmem_ld32x32b_x32(tmem + lane_off + L::kColDq + (HD / 2) * g + c0, a);
+      for (int k2 = 0; k2 < HD / 64; ++k2)
+        ptx::tmem_ld32x32b_x32(tmem + lane_off + L::kColDq + (HD / 2) * g + 32 * k2, a[k2]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::kBarAccEmpty));
+#pragma unroll
+      for (int k2 = 0; k2 < HD / 64; ++k2) {
         uint32_t pk16[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk16[c] = pack2<kF16>(__uint_as_float(a[2 * c]) * p.scale, __uint_as_float(a[2 * c + 1]) * p.scale);
+          pk16[c] = pack2<kF16>(__uint_as_float(a[k2][2 * c]) * p.scale, __uint_as_float(a[k2][2 * c + 1]) * p.scale);
         if (valid) {
+          if (p.dq_v8) {
+            ptx::st_global_v8(dst + 32 * k2, pk16);
+            ptx::st_global_v8(dst + 32 * k2 + 16, pk16 + 8);
+          } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            reinterpret_cast<uint4*>(dst + c0)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(dst + 32 * k2)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+          }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::kBarAccEmpty));
     }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------ load warp
@@ -1335,6 +1352,12 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.dq = static_cast<uint16_t*>(dQ);
   p.dk = static_cast<uint16_t*>(dK);
   p.dv = static_cast<uint16_t*>(dV);
+  auto v8_ok = [](const void* base, const long long* st) {
+    return reinterpret_cast<uintptr_t>(base) % 32 == 0 && (st[0] * 2) % 32 == 0 &&
+           (st[1] * 2) % 32 == 0 && (st[2] * 2) % 32 == 0;
+  };
+  p.dq_v8 = v8_ok(dQ, sd.dq) ? 1 : 0;
+  p.dkv_v8 = (v8_ok(dK, sd.dk) && v8_ok(dV, sd.dv)) ? 1 : 0;
   for (int i = 0; i < 3; ++i) {
     p.dq_s[i] = sd.dq[i];
     p.dk_s[i] = sd.dk[i];

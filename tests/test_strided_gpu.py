@@ -186,6 +186,33 @@ def test_workload_bshd_equals_contiguous_both_passes():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_gradients_aligned_to_16_bytes_only(D):
+    """The backward's epilogues store dQ, dK and dV 32 bytes a time when their bases and
+    strides allow it; gradients whose buffers start 16 bytes in (or whose rows are padded by
+    8 elements) take 16-byte stores.  Same bits as the contiguous call; the padding untouched."""
+    B, H, Lq, Lk = 2, 3, 300, 260
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, Lq, Lk, D, seed=23))
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).to(DEV)
+    o, lse = fa.attention(q, k, v, causal=True)
+    grads = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    n_q, n_k = B * H * Lq * D, B * H * Lk * D
+    buf_q = torch.full((n_q + 16,), 7.0, dtype=torch.bfloat16, device=DEV)
+    dq = buf_q[8:8 + n_q].view(B, H, Lq, D)                  # base 16 bytes into the buffer
+    buf_k = torch.full((B, H, Lk, D + 8), 7.0, dtype=torch.bfloat16, device=DEV)
+    dk = buf_k[..., :D]                                      # rows padded by 8 elements
+    buf_v = torch.full((n_k + 16,), 7.0, dtype=torch.bfloat16, device=DEV)
+    dv = buf_v[8:8 + n_k].view(B, H, Lk, D)
+    assert dq.data_ptr() % 32 == 16 and dv.data_ptr() % 32 == 16 and dk.stride(2) * 2 % 32 == 16
+    fa.attention_backward(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for a, b in zip(grads, (dq, dk, dv)):
+        assert torch.equal(a, b)
+    assert bool((buf_q[:8] == 7.0).all()) and bool((buf_q[8 + n_q:] == 7.0).all())
+    assert bool((buf_v[:8] == 7.0).all()) and bool((buf_v[8 + n_k:] == 7.0).all())
+    assert bool((buf_k[..., D:] == 7.0).all())
+
+
 def test_workload_fp16_sampled(oracle_mod):
     """The benchmark's fp16 variant of the 16K causal workload against the oracle at
     sampled rows (the bf16 draws are exact in fp16)."""
