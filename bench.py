@@ -723,18 +723,25 @@ def run_ours(args, w):
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize(dev)
-        barrier(dist, dev)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        if fa.fa_last_device_status(stream) != fa.FA_OK:
-            raise RuntimeError("e2e steps reported a device error")
-        e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
+        # Three timed windows of e2e_steps calls each; the median window is reported (the
+        # host link is shared with the machine's other GPUs, and one window can catch a
+        # burst of someone else's copies).  Every window is listed in "windows_ms".
+        windows = []
+        for _ in range(3):
+            barrier(dist, dev)
+            e0.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if fa.fa_last_device_status(stream) != fa.FA_OK:
+                raise RuntimeError("e2e steps reported a device error")
+            windows.append(reduce_max(dist, e0.elapsed_time(e1), dev))
+        e2e_ms = statistics.median(windows)
         e2e = {"value": aggregate_tflops(world, flops, e2e_steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+               "windows_ms": [x / e2e_steps for x in windows],
                "call": "fa_fwd_host (C ABI, pinned host buffers, device workspace allocated once)",
                "upload_only_ms": upload_ms, "upload_gbs": in_bytes / upload_ms / 1e6}
 

@@ -299,6 +299,10 @@ struct DeltaArgs {
 
 template <int HD, bool kF16>
 __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const __grid_constant__ DeltaArgs a) {
+  // Launched as a programmatic dependent for short problems: the previous kernel (possibly
+  // the last backward's dQ kernel, which reads this workspace) completes before any access.
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
   constexpr int kT = HD / 8;   // threads per row, 8 elements (16 bytes) each
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / kT;
@@ -412,6 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
+  // Launched as a programmatic dependent for short problems: the set-up above overlapped the
+  // previous kernel; nothing in global memory is touched before it completes.
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
 
   if (warp < 8) {
     // ------------------------------------------------ compute warpgroups: thread = key row
@@ -811,6 +819,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
+  // Launched as a programmatic dependent for short problems: the set-up above overlapped the
+  // previous kernel; nothing in global memory is touched before it completes.
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
 
   if (warp < 8) {
     // ------------------------------------------------ compute warpgroups: thread = query row
@@ -1379,6 +1391,16 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.flags = fa_internal_debug_flags();
   if (p.flags & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
 
+  // Short problems launch the three kernels as programmatic dependents: each one's set-up
+  // (barriers, TMEM) overlaps the kernel ahead of it, which it waits for before touching
+  // memory.  Long ones launch plainly (the forward measured bimodal times with dependent
+  // launches of long kernels).  Work per CTA: the query-key tile pairs of the problem.
+  const long long pairs_per_cta = bh * static_cast<long long>(p.nq) * p.nk / std::max(1, sm_count);
+  const bool dependent = pairs_per_cta <= 256;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+
   // 1. Delta = rowsum(dO * O) and LSE * log2(e), padded to whole tiles.  Launch errors
   // come from the launch call itself (not cudaGetLastError, which would also report an
   // earlier error of the calling thread).
@@ -1403,12 +1425,16 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
     dc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
     dc.blockDim = dim3(256);
     dc.stream = stream;
+    dc.attrs = pdl;
+    dc.numAttrs = dependent ? 1 : 0;
     if (cudaLaunchKernelEx(&dc, delta_kernel(D, f16), da) != cudaSuccess) return FA_ERR_CUDA;
   }
   // 2. dK, dV (one unit per key tile) and 3. dQ (one unit per query tile)
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(fab::kThreads);
   cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = dependent ? 1 : 0;
   p.n_units = static_cast<int>(bh * p.nk);
   p.unit_ctr = unit_ctr;
   p.group_heads = bwd_group_heads(4ll * Lq * D, bh);   // dK/dV streams Q and dO

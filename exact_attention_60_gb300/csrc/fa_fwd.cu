@@ -521,6 +521,26 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
+  // While the previous kernel finishes, warm L2 with this CTA's first Q and K/V tiles: a
+  // prefetch only reads, and L2 is where the previous kernel's writes land, so a tile it
+  // writes is still read fresh after the wait below.  (Key padding reads its counts from
+  // memory to find the unit, so that schedule skips it.)
+  if (warp == kLoadWarp && lane == 0 && !(kBand && p.kv_len)) {
+    Unit u0;
+    if (unit_of<kS>(p, 0, u0)) {
+      const int ub = u0.bh / p.H, uh = u0.bh - ub * p.H;
+#pragma unroll
+      for (int rg = 0; rg < L::kRegions; ++rg) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (u0.nblk[i] > 0) ptx::tma_prefetch_l2_4d(&p.tm_q, 64 * rg, u0.q0 + i * kBlockM, uh, ub);
+        if (u0.nmax > 0) {
+          ptx::tma_prefetch_l2_4d(&p.tm_k, 64 * rg, u0.kv0 * kBlockN, uh, ub);
+          ptx::tma_prefetch_l2_4d(&p.tm_v, 64 * rg, u0.kv0 * kBlockN, uh, ub);
+        }
+      }
+    }
+  }
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above overlapped its tail; nothing in global memory is touched before it completes.
   // The next kernel may be scheduled now (it waits the same way before touching memory).

@@ -272,6 +272,36 @@ def test_backward_deterministic():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("B,H,L,D", [(4, 16, 1024, 64), (2, 8, 700, 128)])
+def test_backward_chained_calls_see_previous_results(B, H, L, D):
+    """Short backward problems launch their kernels as programmatic dependents.  Each call
+    here consumes the previous call's dK as its dO and overwrites the buffers the call before
+    read (the workspace included): back to back they must give the bits of calls separated
+    by a device sync."""
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, L, L, D, seed=9))
+    o, lse = fa.attention(q, k, v, causal=True)
+    do0 = make_do(B, H, L, D, seed=9).to(dev)
+
+    def chain(sync):
+        do = do0.clone()
+        outs = []
+        for i in range(5):
+            dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append((dq, dk, dv))
+            do = dk   # [B, H, L, D] with Lq == Lk: the next call reads what this one wrote
+        torch.cuda.synchronize()
+        return outs
+
+    a, b = chain(True), chain(False)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for ga, gb in zip(a, b):
+        for x, y in zip(ga, gb):
+            assert torch.equal(x, y)
+
+
 def test_autograd_function_matches_direct_calls():
     dev = torch.device("cuda:0")
     q, k, v = (t.to(dev).requires_grad_(True) for t in make_qkv(1, 2, 300, 400, 64, seed=9))

@@ -347,22 +347,29 @@ def test_workspace_argument_errors():
     assert fa.fa_last_device_status() == fa.FA_OK
 
 
-@pytest.mark.parametrize("shape,kw", [((4, 16, 1024, 1024, 64), dict(causal=True)),          # dependent launches
-                                      ((1, 4, 512, 8192, 128), dict(causal=False)),          # split + combine
-                                      ((2, 8, 700, 700, 128), dict(window=(100, 0)))])       # band
-def test_chained_calls_see_previous_results(shape, kw):
-    """Each call's output is the next call's Q (read after write) and the previous call's
-    input buffer is the next call's output (write after read): back-to-back launches, which
-    may overlap their set-up, must give the same bits as calls separated by a device sync."""
+@pytest.mark.parametrize("shape,kw,feed", [((4, 16, 1024, 1024, 64), dict(causal=True), "q"),   # dependent launches
+                                           ((1, 4, 512, 8192, 128), dict(causal=False), "q"),   # split + combine
+                                           ((2, 8, 700, 700, 128), dict(window=(100, 0)), "q"),  # band
+                                           ((4, 16, 1024, 1024, 64), dict(causal=True), "kv"),
+                                           ((2, 16, 2048, 2048, 128), dict(causal=False), "kv")])
+def test_chained_calls_see_previous_results(shape, kw, feed):
+    """Each call's output is the next call's Q (or K and V: read after write, including the
+    tiles a kernel prefetches into L2 while the previous one finishes) and the previous
+    call's input buffer is the next call's output (write after read): back-to-back launches,
+    which may overlap their set-up, must give the same bits as calls separated by a device
+    sync."""
     B, H, Lq, Lk, D = shape
     dev = torch.device("cuda:0")
     q0, k, v = (t.to(dev) for t in make_qkv(B, H, Lq, Lk, D, seed=61))
     def chain(sync):
-        bufs = [q0.clone(), torch.empty_like(q0)]
+        bufs = [(q0 if feed == "q" else k).clone(), torch.empty_like(q0)]
         lse = torch.empty((B, H, Lq), device=dev, dtype=torch.float32)
         for i in range(6):
             src, dst = bufs[i % 2], bufs[(i + 1) % 2]
-            fa.attention(src, k, v, out=dst, lse=lse, **kw)
+            if feed == "q":
+                fa.attention(src, k, v, out=dst, lse=lse, **kw)
+            else:
+                fa.attention(q0, src, src, out=dst, lse=lse, **kw)
             if sync:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
