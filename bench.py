@@ -775,7 +775,9 @@ def run_ours(args, w):
                        "workspace_bytes": ws_bytes},
             "pct_of_peak": 100.0 * kernel_tflops / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps, "per_config": per_config,
+            # one attention kernel per step; the split-key schedule adds its merge kernel
+            "gpu_launches": args.steps * (2 if schedule == "split key ranges" else 1),
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
