@@ -335,6 +335,9 @@ def time_oracle(w, q, k, v, budget_s: float, heads: int = 2, rows_per_call: int 
         b, h = divmod(int(bh), w.H)
         per_head.append(tuple(np.ascontiguousarray(t[b, h].float().numpy(), dtype=np.float64)
                               for t in (q, k, v)))
+    # Every host core this process may run on, whatever OMP_NUM_THREADS says (a multi-process
+    # launcher sets it to 1 for each rank, and only one rank times the oracle).
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     flops = 0
     spent = 0.0
     nrows = 0
@@ -344,14 +347,15 @@ def time_oracle(w, q, k, v, budget_s: float, heads: int = 2, rows_per_call: int 
         rows = rng.integers(0, w.Lq, size=rows_per_call)
         t0 = time.perf_counter()
         if w.window is not None:
-            oracle.attn_head_window(qq, kk, vv, w.window[0], w.window[1], w.scale, rows=rows)
+            oracle.attn_head_window(qq, kk, vv, w.window[0], w.window[1], w.scale, rows=rows,
+                                    nthreads=threads)
         else:
-            oracle.attn_head(qq, kk, vv, w.causal, w.scale, rows=rows)
+            oracle.attn_head(qq, kk, vv, w.causal, w.scale, rows=rows, nthreads=threads)
         spent += time.perf_counter() - t0
         flops += row_flops(w, rows)
         nrows += rows_per_call
         it += 1
-    return flops, spent, nrows, oracle.max_threads()
+    return flops, spent, nrows, threads
 
 
 # ----------------------------------------------------------------------------- arms

@@ -189,3 +189,51 @@ def test_per_config_covers_every_specified_configuration():
                       (4, 16, 1024, 1024, 64, True), (2, 32, 4096, 4096, 128, True),
                       (1, 16, 16384, 16384, 128, True), (8, 16, 500, 8191, 128, False)}
     assert len(bench.PER_CONFIG) == 6
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm (the fp64 oracle on the host cores, a bounded row sample per step)
+    prints one JSON line with the fields the benchmark contract asks of it; no GPU needed."""
+    import os
+    import subprocess
+    import sys
+    root = bench.ROOT
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "seq1k_d64_causal", "--steps", "1", "--warmup", "0",
+                        "--ref-seconds-per-step", "0.5"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "seq1k_d64_causal"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_under_two_ranks_prints_once():
+    """Launched as two ranks (gloo on the CPU), only rank 0 times the oracle and prints; the
+    other rank exits 0, and the oracle uses the host's cores despite the launcher's
+    OMP_NUM_THREADS=1."""
+    import os
+    import subprocess
+    import sys
+    root = bench.ROOT
+    env = dict(os.environ, BENCH_DIST_BACKEND="gloo")
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port", "29617",
+                        os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "seq1k_d64_causal", "--steps", "1", "--warmup", "0",
+                        "--ref-seconds-per-step", "0.5"],
+                       capture_output=True, text=True, timeout=300, cwd=root, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    assert d["cpu_baseline"]["cores"] == cores
