@@ -819,9 +819,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long limit = p.wait_limit_ns;
-  // Launched as a programmatic dependent for short problems: the set-up above overlapped the
-  // previous kernel; nothing in global memory is touched before it completes.
-  ptx::grid_dependency_wait();
+  // Always launched as a programmatic dependent of the dK/dV kernel.  What dQ reads (the
+  // inputs, Delta, LSE * log2 e, its unit counter) was complete before that kernel let
+  // this one launch: the dK/dV kernel allows it only after its own wait for the Delta
+  // kernel.  So this kernel starts on the SMs that the dK/dV kernel's last units leave
+  // free, and waits for the dK/dV kernel only before it exits, so that its completion
+  // still implies both (the next call may read dK or dV).
   ptx::grid_launch_dependents();
 
   if (warp < 8) {
@@ -1091,6 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     __syncwarp();
   }
 
+  ptx::grid_dependency_wait();   // the dK/dV kernel ahead has completed
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -1391,10 +1395,12 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.flags = fa_internal_debug_flags();
   if (p.flags & 2u) return FA_ERR_CUDA;   // test hook: simulated launch failure
 
-  // Short problems launch the three kernels as programmatic dependents: each one's set-up
-  // (barriers, TMEM) overlaps the kernel ahead of it, which it waits for before touching
-  // memory.  Long ones launch plainly (the forward measured bimodal times with dependent
-  // launches of long kernels).  Work per CTA: the query-key tile pairs of the problem.
+  // Short problems launch the Delta and dK/dV kernels as programmatic dependents: each
+  // one's set-up (barriers, TMEM) overlaps the kernel ahead of it, which it waits for
+  // before touching memory.  Long ones launch them plainly (the forward measured bimodal
+  // times with dependent launches of long kernels).  Work per CTA: the query-key tile
+  // pairs of the problem.  The dQ kernel, which does not read what dK/dV writes, is
+  // always a dependent of the dK/dV kernel and fills the SMs its last units leave.
   const long long pairs_per_cta = bh * static_cast<long long>(p.nq) * p.nk / std::max(1, sm_count);
   const bool dependent = pairs_per_cta <= 256;
   cudaLaunchAttribute pdl[1];
@@ -1446,6 +1452,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.group_heads = bwd_group_heads(4ll * Lk * D, bh);   // dQ streams K and V
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.dynamicSmemBytes = (D == 128) ? fab::DqLayout<128>::kAlloc : fab::DqLayout<64>::kAlloc;
+  cfg.numAttrs = 1;   // dependent launch, whatever the problem's length
   if (cudaLaunchKernelEx(&cfg, dq_kernel(D, f16), p) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }

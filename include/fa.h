@@ -342,7 +342,9 @@ fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
  *   B, H, Lq, Lk, D, causal, scale, stream: as fa_fwd.
  * All pointers are device pointers, 16-byte aligned; dQ, dK, dV and the workspace
  * must not overlap each other or any input.  Three kernels are queued on `stream`
- * (Delta, then dK/dV, then dQ).  B*H*Lq == 0 with B*H*Lk > 0 zero-fills dK and dV;
+ * (Delta, then dK/dV, then dQ; dQ may start beside the last dK/dV units and
+ * completes only after them, so stream order holds for whatever follows on
+ * `stream`).  B*H*Lq == 0 with B*H*Lk > 0 zero-fills dK and dV;
  * B*H*Lk == 0 returns FA_OK with nothing queued.  Errors as fa_fwd; a pipeline
  * wait that runs out is reported by fa_last_device_status().
  */
