@@ -302,6 +302,40 @@ def test_backward_chained_calls_see_previous_results(B, H, L, D):
             assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("B,H,L,D", [(4, 16, 1024, 64), (1, 16, 8192, 64)])
+def test_forward_after_backward_sees_its_gradients(B, H, L, D):
+    """The dQ kernel runs beside the dK/dV kernel's last units and waits for that kernel
+    only before it exits.  Forward and backward calls alternate here, each forward taking
+    the previous backward's dQ, dK, dV as its Q, K, V (a short problem, whose backward
+    kernels all launch as dependents, and a long one, whose Delta and dK/dV kernels launch
+    plainly): back to back they must give the bits of calls separated by a device sync."""
+    dev = torch.device("cuda:0")
+    q0, k0, v0 = (t.to(dev) for t in make_qkv(B, H, L, L, D, seed=13))
+    do = make_do(B, H, L, D, seed=13).to(dev)
+
+    def chain(sync):
+        q, k, v = q0, k0, v0
+        outs = []
+        for i in range(3):
+            o, lse = fa.attention(q, k, v, causal=True)
+            if sync:
+                torch.cuda.synchronize()
+            dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append((o, lse, dq, dk, dv))
+            q, k, v = dq, dk, dv   # the next forward follows the dQ kernel directly
+        torch.cuda.synchronize()
+        return outs
+
+    a, b = chain(True), chain(False)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for ga, gb in zip(a, b):
+        for x, y in zip(ga, gb):
+            assert torch.isfinite(x.float()).all()
+            assert torch.equal(x, y)
+
+
 def test_autograd_function_matches_direct_calls():
     dev = torch.device("cuda:0")
     q, k, v = (t.to(dev).requires_grad_(True) for t in make_qkv(1, 2, 300, 400, 64, seed=9))
