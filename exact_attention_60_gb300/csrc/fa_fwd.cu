@@ -132,7 +132,14 @@ struct Layout {
   static constexpr int kNumBars = kBarStageFull + 2;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kBytes = kOffAbort + 4;
+  // Split schedule: the CTA's parts (kMaxParts x 8 ints: bh, q0, kv0, nblk[0] | nblk[1],
+  // nmax, partial, slot), listed once when the kernel starts.  Every role reads its next
+  // part from here: the search through the step space stays out of the roles' loops
+  // (inlined there it made every key-tile step about 20 % slower).
+  static constexpr int kMaxParts = 24;
+  static constexpr int kOffNParts = kOffAbort + 4;
+  static constexpr int kOffParts = (kOffNParts + 4 + 15) & ~15;
+  static constexpr int kBytes = kOffParts + kMaxParts * 32;
   static constexpr int kAlloc = kBytes + 1024;           // slack to align the base to 1 KB
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: S_0 | S_1 | O_0 | O_1.  At D = 128 P_i (bf16 pairs) overwrites the
@@ -473,6 +480,28 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
+  volatile int* s_nparts = reinterpret_cast<volatile int*>(smem + L::kOffNParts);
+  int4* s_parts = reinterpret_cast<int4*>(smem + L::kOffParts);
+  // The r-th unit of this CTA (false: none left); split parts come from the list that
+  // thread 0 writes before the CTA-wide barrier below.
+  auto unit_at = [&](int r, Unit& u) -> bool {
+    if constexpr (kSplit) {
+      if (r >= *s_nparts) return false;
+      const int4 a = s_parts[2 * r], b = s_parts[2 * r + 1];
+      u.bh = a.x;
+      u.q0 = a.y;
+      u.kv0 = a.z;
+      u.nblk[0] = a.w;
+      u.nblk[1] = b.x;
+      u.nmax = b.y;
+      u.partial = b.z;
+      u.slot = b.w;
+      u.first[0] = u.first[1] = 0;
+      return true;
+    } else {
+      return unit_of<kS>(p, r, u);
+    }
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -497,6 +526,17 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       ptx::mbar_init(bar(L::kBarKVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kBarDrain), 1);
+    if constexpr (kSplit) {
+      // The host only takes the split schedule when no CTA has more than kMaxParts parts.
+      int n = 0;
+      Unit t;
+      while (n < L::kMaxParts && unit_of<kS>(p, n, t)) {
+        s_parts[2 * n] = make_int4(t.bh, t.q0, t.kv0, t.nblk[0]);
+        s_parts[2 * n + 1] = make_int4(t.nblk[1], t.nmax, t.partial, t.partial ? t.slot : 0);
+        ++n;
+      }
+      *s_nparts = n;
+    }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(L::kBarStageFree + i), 1);
@@ -527,7 +567,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
   // memory to find the unit, so that schedule skips it.)
   if (warp == kLoadWarp && lane == 0 && !(kBand && p.kv_len)) {
     Unit u0;
-    if (unit_of<kS>(p, 0, u0)) {
+    if (unit_at(0, u0)) {
       const int ub = u0.bh / p.H, uh = u0.bh - ub * p.H;
 #pragma unroll
       for (int rg = 0; rg < L::kRegions; ++rg) {
@@ -563,7 +603,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
     uint32_t n_stage = 0;   // epilogues through the O staging buffer (stage_free / stage_full phase)
     bool ok = true;
     Unit u;
-    for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+    for (int r = 0; ok && unit_at(r, u); ++r) {
       const int n_blocks = wg ? u.nblk[1] : u.nblk[0];
       if constexpr (kSplit) {
         // Causal split: a part can hold no key tile of the first (shorter) query tile; its
@@ -732,19 +772,17 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         // A part of a split unit: park this row's state (unnormalised O, m, l) for
         // the combine kernel that runs after this one.
         const size_t rowi = static_cast<size_t>(u.slot * 2 + wg) * kBlockM + row;
-        float* so = p.ws_o + rowi * HD;
+        float* so = p.ws_o + rowi * HD;   // 32-byte aligned: 256-byte base, HD * 4-byte rows
+        // The whole row first, O released at once, then whole 32-byte sectors from registers.
+        uint32_t o[HD / 32][32];
 #pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-          uint32_t o[32];
-          ptx::tmem_ld32x32b_x32(t_o + c0, o);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            reinterpret_cast<float4*>(so + c0)[v] =
-                make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                            __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
-        }
+        for (int k = 0; k < HD / 32; ++k) ptx::tmem_ld32x32b_x32(t_o + 32 * k, o[k]);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarOEmpty + wg));
+#pragma unroll
+        for (int k = 0; k < HD / 32; ++k)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) ptx::st_global_v8(so + 32 * k + 8 * v, o[k] + 8 * v);
         p.ws_ml[rowi * 2] = m;
         p.ws_ml[rowi * 2 + 1] = l;
         continue;
@@ -851,7 +889,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
       bool ok = true;
       bool first = true;
       Unit u;
-      for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+      for (int r = 0; ok && unit_at(r, u); ++r) {
         const int ub = u.bh / p.H, uh = u.bh - ub * p.H;   // batch and head of the unit
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -992,7 +1030,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         // Per key tile j: first the S GEMMs of key tile j+1 (each as soon as the
         // softmax has read the tile's previous S), then the P V GEMMs of key tile j.
         uint32_t s_iss[2] = {0, 0};   // S_i GEMMs issued so far (s_free phase)
-        for (int r = 0; ok && unit_of<kS>(p, r, u); ++r) {
+        for (int r = 0; ok && unit_at(r, u); ++r) {
           if (kBand && u.nmax == 0) continue;   // no keys at all (key padding): nothing to issue
           const int nblk[2] = {u.nblk[0], u.nblk[1]};
           const int nmax = u.nmax;
@@ -1089,7 +1127,7 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
           if constexpr (L::kQRing) q_pos += (nblk[0] > 0 ? 1u : 0u) + (nblk[1] > 0 ? 1u : 0u);
         }
       }
-      for (int r = 0; !L::kDecoupled && ok && unit_of<kS>(p, r, u); ++r) {
+      for (int r = 0; !L::kDecoupled && ok && unit_at(r, u); ++r) {
         if (kBand && u.nmax == 0) continue;   // no keys at all (key padding): nothing to issue
         const int nb0 = u.nblk[0], nb1 = u.nblk[1], nmax = u.nmax;
         const int nblk[2] = {nb0, nb1};
@@ -1554,25 +1592,52 @@ long long split_total_steps(const Problem& pr) {
   return pr.bh * fa::head_prefix(pr.n_pairs, pr.nkv, pr.Lq, pr.n_pairs, pr.causal);
 }
 
+// The most parts any CTA of a split launch with `grid` CTAs takes: the units that meet its
+// step range [T g / G, T (g + 1) / G) (the kernel's own division of the step space).
+int split_max_parts(const Problem& pr, int grid) {
+  const long long T = split_total_steps(pr);
+  const long long per_head = fa::head_prefix(pr.n_pairs, pr.nkv, pr.Lq, pr.n_pairs, pr.causal);
+  // index of the unit (in step order) that holds step x
+  auto unit_index = [&](long long x) {
+    const long long h = x / per_head, xh = x - h * per_head;
+    int lo = 0, hi = pr.n_pairs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (fa::head_prefix(mid, pr.nkv, pr.Lq, pr.n_pairs, pr.causal) <= xh) lo = mid;
+      else hi = mid - 1;
+    }
+    return h * pr.n_pairs + lo;
+  };
+  long long most = 0;
+  for (int g = 0; g < grid; ++g) {
+    const long long a = T * g / grid, b = T * (g + 1) / grid;
+    if (b > a) most = std::max(most, unit_index(b - 1) - unit_index(a) + 1);
+  }
+  return static_cast<int>(std::min<long long>(most, INT_MAX));
+}
+
 Plan plan_schedule(const Problem& pr, int sm_count) {
   Plan pl{};
   const long long rounds = (pr.n_units + sm_count - 1) / sm_count;
   const double fill = static_cast<double>(pr.n_units) / (static_cast<double>(rounds) * sm_count);
   if (!pr.causal) {
-    pl.split = pr.nkv >= 2 && fill <= (pr.D == 128 ? 0.5 : 0.25);
+    // Cut key ranges when at most half of the last round of units would be filled
+    // (measured side by side: at D = 64 a fill of 0.42 ran 80 % faster split; at D = 128 a
+    // fill of 0.63 ran 1 % slower split).
+    pl.split = pr.nkv >= 2 && fill <= 0.5;
   } else {
     // Causal units grow along the sequence; whole units finish no sooner than the longest
     // one.  When that unit is well above an even share of all steps (few heads, long
-    // sequences), the key ranges are cut across CTAs as for the full mask.
-    // Each part reloads its Q tiles and parks fp32 partial rows, so the split pays only
-    // when the longest unit is far above the share: measured side by side, one or two heads
-    // of 8K-16K tokens at D = 64 (longest unit about 4.6x the share) ran 42-84 % faster,
-    // while shapes near 2.2x lost 4-23 % at D = 128.  Short sequences (units under 16 key
-    // tiles) and problems under two steps per SM stay whole.
+    // sequences), the key ranges are cut across CTAs as for the full mask.  Each part
+    // reloads its Q tiles and parks fp32 partial rows, and a merge kernel follows, so the
+    // split pays only when the longest unit is at least twice the share: measured side by
+    // side, one or two heads of 16K-32K tokens (2.3-2.4x) ran 29-42 % faster split and four
+    // heads of 8K (2.3x) 10 %, while shapes at 1.6-1.8x ran 6-9 % slower.  Short sequences
+    // (units under 16 key tiles) and problems under two steps per SM stay whole.
     const long long longest = fa::pair_steps(pr.n_pairs - 1, pr.nkv, pr.Lq, 1);
     const long long total = split_total_steps(pr);
     const double share = static_cast<double>(total) / sm_count;
-    pl.split = longest >= 16 && total >= 2ll * sm_count && static_cast<double>(longest) >= 4.0 * share;
+    pl.split = longest >= 16 && total >= 2ll * sm_count && static_cast<double>(longest) >= 2.0 * share;
   }
   if (!pl.split) {
     pl.grid = std::min(pr.n_units, sm_count);
@@ -1580,6 +1645,14 @@ Plan plan_schedule(const Problem& pr, int sm_count) {
   }
   const long long steps = split_total_steps(pr);
   pl.grid = static_cast<int>(std::min<long long>(steps, sm_count));
+  // Each CTA lists its parts in shared memory (at most kMaxParts); a problem whose step
+  // ranges would cut more units than that (many tiny causal units in one range) keeps
+  // whole units.
+  if (split_max_parts(pr, pl.grid) > fa::Layout<128>::kMaxParts) {
+    pl.split = false;
+    pl.grid = std::min(pr.n_units, sm_count);
+    return pl;
+  }
   const size_t rows = static_cast<size_t>(pl.grid) * 2 * 2 * fa::kBlockM;   // 2 slots x 2 tiles
   pl.off_ml = round256(rows * pr.D * sizeof(float));
   pl.ws_bytes = pl.off_ml + round256(rows * 2 * sizeof(float));
