@@ -538,6 +538,12 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
         s_parts[2 * n + 1] = make_int4(t.nblk[1], t.nmax, t.partial, t.partial ? t.slot : 0);
         ++n;
       }
+      // More units than the list holds would be a host planning error: report it and do
+      // nothing rather than drop units silently.
+      if (n == L::kMaxParts && unit_of<kS>(p, n, t)) {
+        atomicCAS(&g_status, 0u, static_cast<unsigned>(FA_ERR_UNSUPPORTED));
+        n = 0;
+      }
       *s_nparts = n;
     }
 #pragma unroll
@@ -1295,7 +1301,8 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
   __shared__ int s_nparts, s_bh, s_q0;
   const int b = blockIdx.x + 1;   // boundary between CTA b-1 and CTA b
   const int tile = blockIdx.y;
-  ptx::grid_dependency_wait();   // the parts come from the attention kernel before this one
+  // Which parts this CTA merges follows from the launch's sizes alone: found while the
+  // attention kernel ahead may still be running (under a dependent launch).
   if (threadIdx.x == 0) {
     const long long G = c.grid;
     auto lo = [&](long long g) { return c.total_steps * g / G; };
@@ -1314,6 +1321,11 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
     s_q0 = pair * 2 * kBlockM + tile * kBlockM;
   }
   __syncthreads();
+  // The parts come from the attention kernel ahead.  Every CTA waits for it, even one with
+  // nothing to merge, so that this kernel's completion implies that kernel's.  A dependent
+  // launch after this one may start its set-up now (it waits for this kernel in turn).
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
   const int nparts = s_nparts;
   if (nparts == 0 || s_q0 >= c.Lq) return;
   constexpr int kPerLane = HD / 32;   // 4 (D = 128) or 2 (D = 64) columns per lane

@@ -395,7 +395,10 @@ const char* fa_status_string(fa_status s);
  * library's device status words (forward and backward kernels) on the current device.  Returns FA_OK if no
  * kernel launched since the last read reported a problem, FA_ERR_TIMEOUT if a
  * pipeline wait inside a kernel gave up (the kernel then stops early and its
- * outputs are undefined), or FA_ERR_CUDA if the synchronisation failed.
+ * outputs are undefined), FA_ERR_UNSUPPORTED if a forward kernel found more work
+ * units for one CTA than its shared-memory list holds (a planning error the host
+ * is built to rule out; the CTA then computes nothing), or FA_ERR_CUDA if the
+ * synchronisation failed.
  */
 fa_status fa_last_device_status(cudaStream_t stream);
 

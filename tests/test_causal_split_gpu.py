@@ -2,7 +2,7 @@
 
 With the causal mask the units (pairs of query tiles of one head) grow along the sequence,
 so whole units finish no sooner than the longest one.  When that unit is far above an
-even share of all key-tile steps -- one or two heads of long sequences -- fa_fwd_ws cuts the key
+even share of all key-tile steps (at least twice it) -- a few heads of long sequences -- fa_fwd_ws cuts the key
 ranges across CTAs: each unit's steps are the key tiles up to the diagonal of its last
 tile, parts park their rows' partial state and a second kernel merges them.  A part may
 hold no key tile of the pair's first (shorter) tile; it then parks an empty state.
@@ -26,6 +26,9 @@ DEV = torch.device("cuda:0")
 
 SHAPES = [(1, 1, 16384, 16384, 128),  # one head of 16K tokens: 64 units for 152 SMs
           (1, 1, 16384, 16384, 64),
+          (1, 1, 32768, 32768, 128),  # longest unit 2.4x the even share: split since it is >= 2x
+          (1, 2, 16384, 16384, 128),  # 2.3x
+          (1, 4, 8192, 8192, 128),    # 2.3x
           (1, 2, 8192, 8192, 64),
           (2, 2, 4096, 4096, 128),
           (1, 3, 3900, 3900, 128),    # last pair without its second tile
