@@ -91,12 +91,12 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
  * Same operation as fa_fwd, scheduled differently when few query tiles face long
  * key ranges.  Work is handed out in units of two 128-row query tiles of one head.
  * Causal units differ in cost and are balanced by ordering them heaviest first; when
- * the longest causal unit still takes at least four times an even share of all the
- * key tiles (one or two heads of long sequences, units of at least 16 key tiles, at
- * least two key tiles per SM in all), its key range is cut as below.
+ * the longest causal unit still takes at least twice an even share of all the key
+ * tiles (a few heads of long sequences, units of at least 16 key tiles, at least two
+ * key tiles per SM in all), its key range is cut as below.
  * Non-causal units all cost the same; when whole units would keep at most half of
- * the SMs busy per round (a quarter for D = 64) and each unit has at least two
- * 128-key tiles, the key range of each unit is cut into consecutive pieces (the
+ * the SMs busy in their last round and each unit has at least two 128-key tiles,
+ * the key range of each unit is cut into consecutive pieces (the
  * FA-2 post's loop over K/V blocks, split between CTAs so every SM gets the same
  * number of key tiles).  Each piece leaves its rows' partial online-softmax state
  * (unnormalised O, running max m, exp-sum l -- the three per-row quantities of the
