@@ -97,6 +97,10 @@ WORKLOADS = {
                                      index=5, window=(4095, 0)),
     "seq4k_d64_local256": Workload("seq4k_d64_local256", 2, 16, 4096, 4096, 64, False,
                                    index=6, window=(256, 256)),
+    # one causal head of 16K tokens: too few units for whole units to fill the GPU, so
+    # fa_fwd_ws cuts key ranges across CTAs (the split-key schedule)
+    "seq16k_d128_causal_h1": Workload("seq16k_d128_causal_h1", 1, 1, 16384, 16384, 128, True,
+                                      index=7),
 }
 
 

@@ -65,7 +65,7 @@ def test_workload_full(oracle_mod, name):
 
 
 @pytest.mark.parametrize("name", ["seq4k_d128_causal", "seq16k_d128_causal",
-                                  "cross_q500_k8191_d128"])
+                                  "cross_q500_k8191_d128", "seq16k_d128_causal_h1"])
 def test_workload_sampled(oracle_mod, name):
     w = WORKLOADS[name]
     q, k, v = make_workload_inputs(w)
