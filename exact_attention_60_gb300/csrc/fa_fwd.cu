@@ -179,7 +179,8 @@ struct Params {
   int n_units;        // n_pairs * bh_count
   int nkv;            // key tiles per unit: ceil(Lk / 128)
   int split;          // 0: whole units, boustrophedon; 1: split key ranges (stream-K)
-  long long total_steps;   // n_units * nkv (split schedule)
+  long long total_steps;   // split schedule: key-tile steps of all units plus unit_cost per unit
+  int unit_cost;           // split schedule: virtual steps in front of each unit
   float* ws_o;        // split schedule: partial O rows   [2 * grid][2 tiles][128 rows][D] fp32
   float* ws_ml;       //                 partial (m, l)   [2 * grid][2 tiles][128 rows][2] fp32
   int win_left;       // band schedule: key j allowed for row i iff i - win_left <= j <= i + win_right,
@@ -234,15 +235,21 @@ __device__ __forceinline__ long long split_lo(const Params& p, int g) {
 // Split schedule step space: the units of a head are its pairs of query tiles in order
 // (pair p = rows [256p, 256p + 256)), heads one after the other; a unit's steps are the key
 // tiles of its longer tile: all nkv of them for the full mask, with the causal mask the
-// tiles up to the diagonal of its last present tile.
+// tiles up to the diagonal of its last present tile.  Each unit is preceded by `cost`
+// virtual steps that stand for what a part costs besides its key tiles (loading its Q
+// tiles, its first S, parking its rows), so that a CTA whose range holds many short units
+// gets fewer key tiles.  A part is the intersection of a CTA's range with a unit's key
+// tiles; a range that meets only a unit's virtual steps holds no part of it.
 __host__ __device__ inline long long pair_steps(int pair, int nkv, int Lq, int causal) {
   if (!causal) return nkv;
   const int last = (pair * 2 * kBlockM + kBlockM < Lq) ? 2 * pair + 2 : 2 * pair + 1;
   return last < nkv ? last : nkv;
 }
-// Steps of pairs [0, P) of one head (P <= n_pairs).
-__host__ __device__ inline long long head_prefix(int P, int nkv, int Lq, int n_pairs, int causal) {
-  if (!causal) return static_cast<long long>(P) * nkv;
+// Steps of pairs [0, P) of one head (P <= n_pairs), `cost` virtual steps per pair included.
+__host__ __device__ inline long long head_prefix(int P, int nkv, int Lq, int n_pairs, int causal,
+                                                 int cost) {
+  const long long virt = static_cast<long long>(P) * cost;
+  if (!causal) return static_cast<long long>(P) * nkv + virt;
   const long long c = nkv / 2;   // pairs p with 2p + 2 <= nkv
   long long s = (P <= c) ? static_cast<long long>(P) * (P + 1)
                          : c * (c + 1) + static_cast<long long>(P - c) * nkv;
@@ -250,22 +257,24 @@ __host__ __device__ inline long long head_prefix(int P, int nkv, int Lq, int n_p
     const long long full = 2ll * (n_pairs - 1) + 2 < nkv ? 2ll * (n_pairs - 1) + 2 : nkv;
     s -= full - pair_steps(n_pairs - 1, nkv, Lq, causal);
   }
-  return s;
+  return s + virt;
 }
-// The unit that contains step x: its head, pair, first step and number of steps.
-__device__ __forceinline__ void split_locate(long long x, int nkv, int Lq, int n_pairs, int causal,
-                                             int* bh, int* pair, long long* start, long long* steps) {
-  const long long per_head = head_prefix(n_pairs, nkv, Lq, n_pairs, causal);
+// The unit whose steps (virtual ones included) contain step x: its head, pair, first step
+// (its first virtual step) and number of key-tile steps.
+__host__ __device__ inline void split_locate(long long x, int nkv, int Lq, int n_pairs, int causal,
+                                             int cost, int* bh, int* pair, long long* start,
+                                             long long* steps) {
+  const long long per_head = head_prefix(n_pairs, nkv, Lq, n_pairs, causal, cost);
   const long long h = x / per_head, xh = x - h * per_head;
   int lo = 0, hi = n_pairs - 1;   // the last pair whose first step is <= xh
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (head_prefix(mid, nkv, Lq, n_pairs, causal) <= xh) lo = mid;
+    if (head_prefix(mid, nkv, Lq, n_pairs, causal, cost) <= xh) lo = mid;
     else hi = mid - 1;
   }
   *bh = static_cast<int>(h);
   *pair = lo;
-  *start = h * per_head + head_prefix(lo, nkv, Lq, n_pairs, causal);
+  *start = h * per_head + head_prefix(lo, nkv, Lq, n_pairs, causal, cost);
   *steps = pair_steps(lo, nkv, Lq, causal);
 }
 
@@ -367,16 +376,18 @@ __device__ __forceinline__ bool unit_of(const P& p, int r, Unit& u) {
   } else {
   const long long lo = split_lo(p, g), hi = split_lo(p, g + 1);
   long long x = lo;
-  int bh, pair;
-  long long start, steps;
-  for (int k = 0; k < r && x < hi; ++k) {   // skip the first r parts of this CTA's range
-    split_locate(x, p.nkv, p.Lq, p.n_pairs, p.causal, &bh, &pair, &start, &steps);
-    x = min(start + steps, hi);
+  int bh = 0, pair = 0, k = 0;
+  long long start = 0, steps = 0, ra = 0, rb = 0;
+  for (; x < hi; x = min(start + p.unit_cost + steps, hi)) {   // the r-th part of the range
+    split_locate(x, p.nkv, p.Lq, p.n_pairs, p.causal, p.unit_cost, &bh, &pair, &start, &steps);
+    const long long ks = start + p.unit_cost;   // the unit's first key-tile step
+    ra = max(x, ks);
+    rb = min(ks + steps, hi);
+    if (ra < rb && k++ == r) break;
   }
   if (x >= hi) return false;
-  split_locate(x, p.nkv, p.Lq, p.n_pairs, p.causal, &bh, &pair, &start, &steps);
-  const int a = static_cast<int>(x - start);
-  const int len = static_cast<int>(min(start + steps - x, hi - x));
+  const int a = static_cast<int>(ra - (start + p.unit_cost));
+  const int len = static_cast<int>(rb - ra);
   u.bh = bh;
   u.q0 = pair * 2 * kBlockM;
 #pragma unroll
@@ -389,7 +400,8 @@ __device__ __forceinline__ bool unit_of(const P& p, int r, Unit& u) {
   u.kv0 = a;
   u.first[0] = u.first[1] = 0;
   u.partial = (len != steps);
-  if (u.partial) u.slot = 2 * g + (x == lo ? 0 : 1);
+  // A cut unit is its range's first or last part (the ones between are whole).
+  if (u.partial) u.slot = 2 * g + (r == 0 ? 0 : 1);
   return true;
   }
 }
@@ -1275,6 +1287,7 @@ struct CombineParams {
   int H;
   float* lse;
   long long total_steps;
+  int unit_cost;     // virtual steps in front of each unit (as in Params)
   int grid;          // CTAs of the attention kernel that made the parts
   int nkv;
   int n_pairs;
@@ -1309,11 +1322,14 @@ __global__ void __launch_bounds__(128) fa_combine_kernel(const __grid_constant__
     const long long xb = lo(b);
     int bh, pair;
     long long step0, steps;
-    split_locate(xb, c.nkv, c.Lq, c.n_pairs, c.causal, &bh, &pair, &step0, &steps);
+    split_locate(xb, c.nkv, c.Lq, c.n_pairs, c.causal, c.unit_cost, &bh, &pair, &step0, &steps);
+    const long long ks = step0 + c.unit_cost, ke = ks + steps;   // the unit's key-tile steps
     int n = 0;
-    // nothing to do on a boundary between units, or if an earlier boundary lies in the unit
-    if (xb != step0 && !(b >= 2 && lo(b - 1) > step0)) {
-      for (long long g = b - 1; g < G && lo(g) <= step0 + steps - 1 && n < kCombineMaxParts; ++g)
+    // Nothing to do unless this boundary cuts the unit's key tiles and no earlier one does.
+    // The unit's parts are those of CTA b-1 (its first part when nothing precedes the unit
+    // in its range) and of the CTAs after it whose ranges start inside the unit.
+    if (xb > ks && !(b >= 2 && lo(b - 1) > ks)) {
+      for (long long g = b - 1; g < G && lo(g) < ke && n < kCombineMaxParts; ++g)
         s_slot[n++] = static_cast<int>(2 * g + (lo(g) >= step0 ? 0 : 1));
     }
     s_nparts = n;
@@ -1604,30 +1620,38 @@ struct Plan {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Key-tile steps of all units in the split schedule's step space.
-long long split_total_steps(const Problem& pr) {
-  return pr.bh * fa::head_prefix(pr.n_pairs, pr.nkv, pr.Lq, pr.n_pairs, pr.causal);
+// Virtual steps in front of each unit of the split step space: what a part costs besides
+// its key tiles (its Q loads, first S and parked rows took about four key-tile steps in a
+// trace of one long causal head), so that ranges holding many short units carry fewer key
+// tiles.  Causal units differ in length and the short ones gather in a few ranges; measured
+// side by side, 5 at D = 128 and 3 at D = 64 ran 15-23 % faster than no cost on one to four
+// long causal heads (higher and lower values slower).  Non-causal units are all alike and
+// take none (a cost measured 0-1 % slower there).
+int split_unit_cost(const Problem& pr) { return pr.causal ? (pr.D == 128 ? 5 : 3) : 0; }
+
+// Steps of all units in the split schedule's step space, `cost` virtual steps per unit
+// included (0: key-tile steps only).
+long long split_total_steps(const Problem& pr, int cost) {
+  return pr.bh * fa::head_prefix(pr.n_pairs, pr.nkv, pr.Lq, pr.n_pairs, pr.causal, cost);
 }
 
-// The most parts any CTA of a split launch with `grid` CTAs takes: the units that meet its
-// step range [T g / G, T (g + 1) / G) (the kernel's own division of the step space).
-int split_max_parts(const Problem& pr, int grid) {
-  const long long T = split_total_steps(pr);
-  const long long per_head = fa::head_prefix(pr.n_pairs, pr.nkv, pr.Lq, pr.n_pairs, pr.causal);
-  // index of the unit (in step order) that holds step x
-  auto unit_index = [&](long long x) {
-    const long long h = x / per_head, xh = x - h * per_head;
-    int lo = 0, hi = pr.n_pairs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (fa::head_prefix(mid, pr.nkv, pr.Lq, pr.n_pairs, pr.causal) <= xh) lo = mid;
-      else hi = mid - 1;
-    }
-    return h * pr.n_pairs + lo;
-  };
+// The most parts any CTA of a split launch with `grid` CTAs takes: the units whose key tiles
+// meet its step range [T g / G, T (g + 1) / G) (the kernel's own division of the step space).
+int split_max_parts(const Problem& pr, int grid, int cost) {
+  const long long T = split_total_steps(pr, cost);
   long long most = 0;
   for (int g = 0; g < grid; ++g) {
     const long long a = T * g / grid, b = T * (g + 1) / grid;
-    if (b > a) most = std::max(most, unit_index(b - 1) - unit_index(a) + 1);
+    long long n = 0;
+    for (long long x = a; x < b;) {
+      int bh, pair;
+      long long start, steps;
+      fa::split_locate(x, pr.nkv, pr.Lq, pr.n_pairs, pr.causal, cost, &bh, &pair, &start, &steps);
+      const long long ks = start + cost, ke = ks + steps;
+      if (std::max(x, ks) < std::min(ke, b)) ++n;
+      x = std::min(ke, b);
+    }
+    most = std::max(most, n);
   }
   return static_cast<int>(std::min<long long>(most, INT_MAX));
 }
@@ -1651,7 +1675,7 @@ Plan plan_schedule(const Problem& pr, int sm_count) {
     // heads of 8K (2.3x) 10 %, while shapes at 1.6-1.8x ran 6-9 % slower.  Short sequences
     // (units under 16 key tiles) and problems under two steps per SM stay whole.
     const long long longest = fa::pair_steps(pr.n_pairs - 1, pr.nkv, pr.Lq, 1);
-    const long long total = split_total_steps(pr);
+    const long long total = split_total_steps(pr, 0);
     const double share = static_cast<double>(total) / sm_count;
     pl.split = longest >= 16 && total >= 2ll * sm_count && static_cast<double>(longest) >= 2.0 * share;
   }
@@ -1659,12 +1683,12 @@ Plan plan_schedule(const Problem& pr, int sm_count) {
     pl.grid = std::min(pr.n_units, sm_count);
     return pl;
   }
-  const long long steps = split_total_steps(pr);
+  const long long steps = split_total_steps(pr, 0);
   pl.grid = static_cast<int>(std::min<long long>(steps, sm_count));
   // Each CTA lists its parts in shared memory (at most kMaxParts); a problem whose step
   // ranges would cut more units than that (many tiny causal units in one range) keeps
   // whole units.
-  if (split_max_parts(pr, pl.grid) > fa::Layout<128>::kMaxParts) {
+  if (split_max_parts(pr, pl.grid, split_unit_cost(pr)) > fa::Layout<128>::kMaxParts) {
     pl.split = false;
     pl.grid = std::min(pr.n_units, sm_count);
     return pl;
@@ -1790,7 +1814,8 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
   // Heaviest units first: the last query tiles unless only the left side is bounded.
   p.band_desc = (pr.win_left >= 0 && pr.win_right < 0) ? 0 : 1;
   p.kv_len = pr.kv_len;
-  p.total_steps = split_total_steps(pr);
+  p.unit_cost = split_unit_cost(pr);
+  p.total_steps = split_total_steps(pr, p.unit_cost);
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
   if (pl.split) {
@@ -1856,6 +1881,7 @@ fa_status launch(const Problem& pr, int sm_count, const Plan& pl, void* ws, cuda
     c.H = p.H;
     c.lse = p.lse;
     c.total_steps = p.total_steps;
+    c.unit_cost = p.unit_cost;
     c.grid = pl.grid;
     c.nkv = pr.nkv;
     c.n_pairs = pr.n_pairs;
