@@ -497,8 +497,9 @@ fa_fwd_kernel(const __grid_constant__ typename ParamsOf<kS>::type p) {
   auto bar = [&](int idx) -> uint32_t { return sbase + L::kOffBar + 8u * idx; };
   volatile int* s_nparts = reinterpret_cast<volatile int*>(smem + L::kOffNParts);
   int4* s_parts = reinterpret_cast<int4*>(smem + L::kOffParts);
-  // The r-th unit of this CTA (false: none left); split parts come from the list that
-  // thread 0 writes before the CTA-wide barrier below.
+  // The r-th unit of this CTA (false: none left).  Split parts and listed whole units come
+  // from the list that thread 0 writes before the CTA-wide barrier below; the other
+  // schedules find their units directly.
   auto unit_at = [&](int r, Unit& u) -> bool {
     if constexpr (kSplit || kS == kSchedWholeList) {
       if (r >= *s_nparts) return false;
@@ -1639,6 +1640,11 @@ long long split_total_steps(const Problem& pr, int cost) {
 // meet its step range [T g / G, T (g + 1) / G) (the kernel's own division of the step space).
 int split_max_parts(const Problem& pr, int grid, int cost) {
   const long long T = split_total_steps(pr, cost);
+  // Every unit takes at least 1 + cost steps, so a range of R steps meets at most
+  // R / (1 + cost) + 2 of them; when that bound is small enough the walk below is skipped.
+  const long long range = (T + grid - 1) / grid;
+  const long long bound = range / (1 + cost) + 2;
+  if (bound <= fa::Layout<128>::kMaxParts) return static_cast<int>(bound);
   long long most = 0;
   for (int g = 0; g < grid; ++g) {
     const long long a = T * g / grid, b = T * (g + 1) / grid;
