@@ -18,6 +18,7 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
   cpu_baseline the fp64 oracle timed on the host cores on a bounded row sample;
   clocks       SM clocks, power and throttle reasons sampled during the timed region;
   per_config   every configuration of the specification (C1-C5, C2 with both masks),
+               the two local-attention workloads and the 16K causal backward pass,
                each timed over at least --per-config-seconds of back-to-back launches
                with its own roofline and the clock samples taken inside that window.
 With --impl reference the fp64 CPU oracle is the measured arm (bounded row
@@ -528,6 +529,85 @@ def roofline_of(setup, flops, per_launch_s, peaks, peak_src, traffic, sustained=
 PER_CONFIG = [("C1", "tiny_d64"), ("C2", "seq1k_d64"), ("C2-causal", "seq1k_d64_causal"),
               ("C3", "seq4k_d128_causal"), ("C4", "seq16k_d128_causal"),
               ("C5", "cross_q500_k8191_d128")]
+# The extensions beyond the forward's plain masks, timed the same way: local attention
+# (a causal window and a symmetric band) and the backward pass.
+PER_CONFIG_LOCAL = [("window-16k-d128", "seq16k_d128_window4k"), ("local256-4k-d64", "seq4k_d64_local256")]
+PER_CONFIG_BACKWARD = [("backward-16k-causal-d128", "seq16k_d128_causal")]
+
+
+def measure_backward(fa, w, dev, stream, peaks, peak_src, seconds, no_clocks):
+    """The backward pass (one fa_bwd call: Delta, dK/dV and dQ kernels) timed over at least
+    ``seconds`` of back-to-back calls on resident inputs, clocks sampled inside that window.
+    TFLOP/s at the conventional count of five GEMMs of the forward's size."""
+    import torch
+    q_h, k_h, v_h = make_workload_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 99)
+    do_h = torch.randn(q_h.shape, generator=g).to(torch.bfloat16)
+    per_copy = 2 * (3 * q_h.numel() + 4 * k_h.numel()) + 8 * w.B * w.H * w.Lq
+    n_copies = max(2, math.ceil(2 * L2_BYTES / per_copy) + 1)
+    bufs = []
+    for c in range(n_copies):
+        q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+        o, lse = fa.attention(q, k, v, causal=w.causal, scale=w.scale)
+        bufs.append((q, k, v, o, do, lse, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)))
+    st, ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D, w.causal)
+    if st != fa.FA_OK:
+        raise RuntimeError(fa.fa_status_string(st))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def launch(i):
+        q, k, v, o, do, lse, dq, dk, dv = bufs[i % n_copies]
+        st = fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.B, w.H, w.Lq, w.Lk, w.D, w.causal,
+                       w.scale, ws, ws_bytes, stream)
+        if st != fa.FA_OK:
+            raise RuntimeError(fa.fa_status_string(st))
+
+    for i in range(3):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(5):
+        launch(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = max(e0.elapsed_time(e1) / 5, 1e-3)
+    steps = int(min(100000, max(20, math.ceil(seconds * 1000.0 / est_ms))))
+    sampler = ClockSampler(dev.index, period_ms=20.0)
+    if not no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(steps):
+        launch(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if not no_clocks:
+        time.sleep(0.15)
+        sampler.stop()
+    clocks = None if no_clocks else sampler.summary(t0, t1)
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"{w.name} backward: {fa.fa_status_string(st)}")
+    total_ms = e0.elapsed_time(e1)
+    flops = 2.5 * w.flops()
+    tflops = flops / (total_ms / steps / 1e3) / 1e12
+    peak = peak_value(peaks, "bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    entry = {"workload": w.name, "shape": w.describe(), "pass": "backward", "steps": steps,
+             "ms_per_step": total_ms / steps, "tflops": tflops,
+             "flop_count": "2.5x forward (five GEMMs); the kernels execute seven",
+             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": UNIT,
+                          "frac": tflops / peak, "traffic": None,
+                          "peak_source": f"{peak_src} bf16 dense (sustained)",
+                          "kernel": f"fa_bwd (Delta + fa_bwd_dkdv_kernel<{w.D}> + "
+                                    f"fa_bwd_dq_kernel<{w.D}>), whole pass"},
+             "clocks": clocks}
+    del bufs, ws
+    torch.cuda.empty_cache()
+    return entry
 
 
 def measure_config(fa, w, dev, stream, peaks, peak_src, seconds, no_clocks):
@@ -759,9 +839,12 @@ def run_ours(args, w):
     per_config = None
     if rank == 0 and not args.skip_per_config and not variant:
         per_config = {}
-        for label, name in PER_CONFIG:
+        for label, name in PER_CONFIG + PER_CONFIG_LOCAL:
             per_config[label] = measure_config(fa, WORKLOADS[name], dev, stream, peaks, peak_src,
                                                args.per_config_seconds, args.no_clocks)
+        for label, name in PER_CONFIG_BACKWARD:
+            per_config[label] = measure_backward(fa, WORKLOADS[name], dev, stream, peaks, peak_src,
+                                                 args.per_config_seconds, args.no_clocks)
 
     if rank == 0:
         line = {
