@@ -1129,6 +1129,40 @@ std::mutex g_bwd_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
 bool g_bwd_ready[64][2][2] = {};   // [device][D == 128][fp16]: shared-memory opt-in done
 
+// Problems with fewer key tiles than SMs run the dQ kernel on a second stream beside the
+// dK/dV kernel (see the launch sequence below): one stream and two events per device,
+// owned by the library and created at first use.  An event's record and the wait that
+// reads it are made together under `mu`, so concurrent callers cannot interleave them.
+struct BwdFork {
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork = nullptr;   // recorded on the caller's stream after the Delta kernel
+  cudaEvent_t join = nullptr;   // recorded on `aux` after the dQ kernel
+  std::mutex mu;
+};
+BwdFork g_bwd_fork[64];
+
+// The device's fork state, created on first use; nullptr if it cannot be created.
+BwdFork* bwd_fork(int dev) {
+  if (dev < 0 || dev >= 64) return nullptr;
+  BwdFork& f = g_bwd_fork[dev];
+  std::lock_guard<std::mutex> lock(f.mu);
+  if (!f.aux) {
+    cudaStream_t aux = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&e0, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e1, cudaEventDisableTiming) != cudaSuccess) {
+      if (e0) cudaEventDestroy(e0);
+      cudaStreamDestroy(aux);
+      return nullptr;
+    }
+    f.fork = e0;
+    f.join = e1;
+    f.aux = aux;
+  }
+  return &f;
+}
+
 using BwdKernel = void (*)(const BwdParams);
 BwdKernel dkdv_kernel(int D, bool f16) {
   if (D == 128) return f16 ? fab::fa_bwd_dkdv_kernel<128, true> : fab::fa_bwd_dkdv_kernel<128, false>;
@@ -1399,10 +1433,25 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   // one's set-up (barriers, TMEM) overlaps the kernel ahead of it, which it waits for
   // before touching memory.  Long ones launch them plainly (the forward measured bimodal
   // times with dependent launches of long kernels).  Work per CTA: the query-key tile
-  // pairs of the problem.  The dQ kernel, which does not read what dK/dV writes, is
-  // always a dependent of the dK/dV kernel and fills the SMs its last units leave.
+  // pairs of the problem.  The dQ kernel, which does not read what dK/dV writes, is a
+  // dependent of the dK/dV kernel and fills the SMs its last units leave.  With fewer key
+  // tiles than SMs, the dK/dV grid leaves SMs idle from the start and its units end at
+  // very different times.  A dependent grid that fits beside it starts at once, but one
+  // that does not was measured to take none of the SMs the dK/dV units free early (one
+  // causal head of 16K tokens: 323 us, against 320 us launched plainly after dK/dV).
+  // Those problems fork instead: the dQ kernel goes to a second stream that waits for the
+  // Delta kernel only, and the caller's stream waits for it at the end (189 us; two heads
+  // of 8K 180 -> 105 us).  Where both grids fit at once the fork only adds its events
+  // (one head of 8K or 4K: 2-7 % slower), so it is not taken there.
   const long long pairs_per_cta = bh * static_cast<long long>(p.nq) * p.nk / std::max(1, sm_count);
   const bool dependent = pairs_per_cta <= 256;
+  const long long grid_kv = bh * static_cast<long long>(p.nk);
+  const long long grid_q = std::min<long long>(bh * static_cast<long long>(p.nq), sm_count);
+  BwdFork* fk = nullptr;
+  if (grid_kv < sm_count && grid_kv + grid_q > sm_count) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || !(fk = bwd_fork(dev))) return FA_ERR_CUDA;
+  }
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1435,12 +1484,18 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
     dc.numAttrs = dependent ? 1 : 0;
     if (cudaLaunchKernelEx(&dc, delta_kernel(D, f16), da) != cudaSuccess) return FA_ERR_CUDA;
   }
+  if (fk) {   // the dQ kernel's stream starts after the Delta kernel
+    std::lock_guard<std::mutex> lock(fk->mu);
+    if (cudaEventRecord(fk->fork, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(fk->aux, fk->fork, 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
   // 2. dK, dV (one unit per key tile) and 3. dQ (one unit per query tile)
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(fab::kThreads);
   cfg.stream = stream;
   cfg.attrs = pdl;
-  cfg.numAttrs = dependent ? 1 : 0;
+  cfg.numAttrs = (dependent && !fk) ? 1 : 0;   // an event record now separates it from Delta
   p.n_units = static_cast<int>(bh * p.nk);
   p.unit_ctr = unit_ctr;
   p.group_heads = bwd_group_heads(4ll * Lq * D, bh);   // dK/dV streams Q and dO
@@ -1452,8 +1507,19 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   p.group_heads = bwd_group_heads(4ll * Lk * D, bh);   // dQ streams K and V
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.n_units, sm_count)));
   cfg.dynamicSmemBytes = (D == 128) ? fab::DqLayout<128>::kAlloc : fab::DqLayout<64>::kAlloc;
-  cfg.numAttrs = 1;   // dependent launch, whatever the problem's length
+  if (fk) {
+    cfg.stream = fk->aux;
+    cfg.numAttrs = 0;
+  } else {
+    cfg.numAttrs = 1;   // dependent launch, whatever the problem's length
+  }
   if (cudaLaunchKernelEx(&cfg, dq_kernel(D, f16), p) != cudaSuccess) return FA_ERR_CUDA;
+  if (fk) {   // the caller's stream continues once dQ is done
+    std::lock_guard<std::mutex> lock(fk->mu);
+    if (cudaEventRecord(fk->join, fk->aux) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, fk->join, 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
   return FA_OK;
 }
 }  // namespace

@@ -238,7 +238,8 @@ fa_status fa_fwd_strided(const void* Q, const long long* q_stride, const void* K
  * that device current); make that first call before any stream capture.  The
  * address is kept for the life of the process: a cudaDeviceReset (or anything
  * else that destroys the device's primary context) makes it, like the library's
- * other per-device settings, stale, so after a reset no entry point of this
+ * other per-device settings (among them the backward's stream and events), stale,
+ * so after a reset no entry point of this
  * library may be called on that device again in the same process.  Every
  * call shares the one array and leaves scratch in it (it needs no clearing):
  * calls whose kernels can overlap on the GPU -- on different streams, or from
@@ -344,7 +345,15 @@ fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
  * must not overlap each other or any input.  Three kernels are queued on `stream`
  * (Delta, then dK/dV, then dQ; dQ may start beside the last dK/dV units and
  * completes only after them, so stream order holds for whatever follows on
- * `stream`).  B*H*Lq == 0 with B*H*Lk > 0 zero-fills dK and dV;
+ * `stream`).  When B*H*ceil(Lk/128) (the dK/dV kernel's grid) is below the device's
+ * SM count but that grid and the dQ kernel's, min(B*H*ceil(Lq/128), SMs), together
+ * exceed it, the dQ kernel runs instead on a stream the library owns (one per device,
+ * created by the first such call, with two events), beside the dK/dV kernel: that stream waits for the
+ * Delta kernel through an event recorded on `stream`, and `stream` waits for the dQ
+ * kernel through another, so stream order holds all the same.  A call that is being
+ * captured into a CUDA graph takes the library's stream into the capture for its
+ * duration; two such captures on one device at once are not supported.  B*H*Lq == 0
+ * with B*H*Lk > 0 zero-fills dK and dV;
  * B*H*Lk == 0 returns FA_OK with nothing queued.  Errors as fa_fwd; a pipeline
  * wait that runs out is reported by fa_last_device_status().
  */

@@ -336,6 +336,84 @@ def test_forward_after_backward_sees_its_gradients(B, H, L, D):
             assert torch.equal(x, y)
 
 
+def test_few_key_tiles_fork_and_join():
+    """With fewer key tiles than SMs the dQ kernel runs on the library's own stream beside
+    the dK/dV kernel, and the caller's stream waits for it.  One causal head of 16K tokens
+    (128 key tiles; its dQ kernel takes about 0.1 ms) on a side stream, with a reduction
+    of each gradient queued on that stream right behind the call: the sums and the bits
+    must be those of the same call followed by a device sync."""
+    dev = torch.device("cuda:0")
+    B, H, L, D = 1, 1, 16384, 128
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, L, L, D, seed=21))
+    do = make_do(B, H, L, D, seed=21).to(dev)
+    o, lse = fa.attention(q, k, v, causal=True)
+    ref = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    ref_sums = torch.stack([r.float().sum() for r in ref])
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        grads = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+        sums = torch.stack([g.float().sum() for g in grads])
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for g, r in zip(grads, ref):
+        assert torch.isfinite(g.float()).all()
+        assert torch.equal(g, r)
+    assert torch.equal(sums, ref_sums)
+
+
+def test_few_key_tiles_from_two_threads():
+    """Two host threads, each on its own stream, call the backward of few-key-tile
+    problems (both take the library's second stream: 128 key tiles and 128 query tiles
+    against 152 SMs) while the other does: every result must equal the same call made
+    alone."""
+    import threading
+    dev = torch.device("cuda:0")
+    cases = [(1, 1, 16384, 64, 31), (1, 2, 8192, 128, 32)]
+    inputs, refs = [], []
+    for B, H, L, D, seed in cases:
+        q, k, v = (t.to(dev) for t in make_qkv(B, H, L, L, D, seed=seed))
+        do = make_do(B, H, L, D, seed=seed).to(dev)
+        o, lse = fa.attention(q, k, v, causal=True)
+        inputs.append((q, k, v, o, lse, do))
+        refs.append(fa.attention_backward(q, k, v, o, lse, do, causal=True))
+    torch.cuda.synchronize()
+    out = {}
+
+    def work(i):
+        try:   # the C entry point with this thread's own workspace and outputs
+            q, k, v, o, lse, do = inputs[i]
+            B, H, L, D = q.shape
+            st, nb = fa.fa_bwd_workspace_size(B, H, L, L, D, 1)
+            assert st == fa.FA_OK
+            ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            s = torch.cuda.Stream(dev)
+            res = []
+            for _ in range(4):
+                g = tuple(torch.empty_like(t) for t in (q, k, v))
+                st = fa.fa_bwd(q, k, v, o, do, lse, *g, B, H, L, L, D, 1, 1.0 / math.sqrt(D), ws, nb, s)
+                assert st == fa.FA_OK, fa.fa_status_string(st)
+                res.append(g)
+            s.synchronize()
+            out[i] = res
+        except Exception as e:   # reported in the main thread
+            out[f"err{i}"] = e
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not [k for k in out if str(k).startswith("err")], out
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for i in range(2):
+        for grads in out[i]:
+            for g, r in zip(grads, refs[i]):
+                assert torch.equal(g, r)
+
+
 def test_autograd_function_matches_direct_calls():
     dev = torch.device("cuda:0")
     q, k, v = (t.to(dev).requires_grad_(True) for t in make_qkv(1, 2, 300, 400, 64, seed=9))
