@@ -352,7 +352,8 @@ fa_status fa_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
  * Delta kernel through an event recorded on `stream`, and `stream` waits for the dQ
  * kernel through another, so stream order holds all the same.  A call that is being
  * captured into a CUDA graph takes the library's stream into the capture for its
- * duration; two such captures on one device at once are not supported.  B*H*Lq == 0
+ * duration (make a first such call before capturing, as it creates the stream); two
+ * such captures on one device at once are not supported.  B*H*Lq == 0
  * with B*H*Lk > 0 zero-fills dK and dV;
  * B*H*Lk == 0 returns FA_OK with nothing queued.  Errors as fa_fwd; a pipeline
  * wait that runs out is reported by fa_last_device_status().

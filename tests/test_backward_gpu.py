@@ -363,6 +363,32 @@ def test_few_key_tiles_fork_and_join():
     assert torch.equal(sums, ref_sums)
 
 
+def test_few_key_tiles_backward_in_a_cuda_graph():
+    """The forked backward captured into a CUDA graph (the library's stream joins the
+    capture through the fork event and leaves it through the join event): replays give
+    the bits of an eager call.  The first call, which creates the library's stream and
+    the cached workspace, is made before the capture."""
+    dev = torch.device("cuda:0")
+    B, H, L, D = 1, 2, 8192, 128   # 128 key tiles and 128 query tiles against 152 SMs
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, L, L, D, seed=23))
+    do = make_do(B, H, L, D, seed=23).to(dev)
+    o, lse = fa.attention(q, k, v, causal=True)
+    ref = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    grads = tuple(torch.empty_like(t) for t in (q, k, v))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.attention_backward(q, k, v, o, lse, do, causal=True, dq=grads[0], dk=grads[1], dv=grads[2])
+    for _ in range(2):
+        for t in grads:
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_last_device_status() == fa.FA_OK
+        for x, r in zip(grads, ref):
+            assert torch.equal(x, r)
+
+
 def test_few_key_tiles_from_two_threads():
     """Two host threads, each on its own stream, call the backward of few-key-tile
     problems (both take the library's second stream: 128 key tiles and 128 query tiles
